@@ -1,0 +1,351 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each pin is a hand-derived fixture (tests/golden), a closed form, an identity
+of the mathematics, exact integer arithmetic or a brute force on tiny inputs.
+The last group plants plausible mistakes in copies of the oracle functions and
+checks that some pin catches each one.
+"""
+
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------------------
+# Indexer score
+# ---------------------------------------------------------------------------
+
+def test_indexer_golden():
+    g = _golden("indexer_tiny.json")
+    s = oracle.indexer_score(np.array(g["q"], float), np.array(g["w"]), np.array(g["keys"], float))
+    assert s.tolist() == g["scores"]
+
+
+def _indexer_exact(q, w, keys):
+    """Exact rational brute force with Python integers / Fractions and loops."""
+    out = []
+    for k in keys:
+        total = Fraction(0)
+        for h in range(len(q)):
+            dot = Fraction(0)
+            for d in range(len(k)):
+                dot += Fraction(q[h][d]) * Fraction(k[d])
+            total += Fraction(w[h]) * max(dot, Fraction(0))
+        out.append(total)
+    return out
+
+
+def test_indexer_integer_inputs_exact():
+    rng = np.random.default_rng(11)
+    q = rng.integers(-3, 4, size=(5, 7))
+    w = rng.integers(-3, 4, size=5)
+    keys = rng.integers(-3, 4, size=(9, 7))
+    exact = _indexer_exact(q.tolist(), w.tolist(), keys.tolist())
+    s = oracle.indexer_score(q.astype(float), w.astype(float), keys.astype(float))
+    assert [Fraction(x) for x in s] == exact
+
+
+def test_indexer_relu_identity():
+    """relu(x) - relu(-x) = x, so s(q) - s(-q) = sum_h w_h (q_h . k) exactly
+    in exact arithmetic: a plain weighted sum of dot products, no ReLU."""
+    rng = np.random.default_rng(12)
+    q = rng.standard_normal((6, 8))
+    w = rng.standard_normal(6)
+    keys = rng.standard_normal((10, 8))
+    diff = oracle.indexer_score(q, w, keys) - oracle.indexer_score(-q, w, keys)
+    lin = [sum(w[h] * sum(q[h, d] * k[d] for d in range(8)) for h in range(6)) for k in keys]
+    np.testing.assert_allclose(diff, lin, rtol=1e-12, atol=1e-12)
+
+
+def test_indexer_one_hot_weights_select_head():
+    """w = e_h reduces the score to max(0, q_h . k): pairs weights with heads."""
+    rng = np.random.default_rng(13)
+    q = rng.standard_normal((4, 5))
+    keys = rng.standard_normal((7, 5))
+    for h in range(4):
+        w = np.zeros(4)
+        w[h] = 1.0
+        s = oracle.indexer_score(q, w, keys)
+        expect = [max(0.0, sum(q[h, d] * k[d] for d in range(5))) for k in keys]
+        np.testing.assert_allclose(s, expect, rtol=1e-13, atol=1e-14)
+
+
+def test_indexer_nonfinite_becomes_minus_inf():
+    q = np.ones((2, 3))
+    w = np.ones(2)
+    keys = np.array([[1.0, 1.0, 1.0], [np.nan, 0, 0], [np.inf, 0, 0], [1e38, 1e38, 1e38]])
+    s = oracle.indexer_score(q, w, keys)
+    assert s[0] == 6.0
+    assert s[1] == -np.inf and s[2] == -np.inf
+    assert s[3] == -np.inf          # 6e38 overflows fp32
+
+
+def test_indexer_causal_mask():
+    rng = np.random.default_rng(14)
+    q, w, keys = rng.standard_normal((3, 4)), rng.standard_normal(3), rng.standard_normal((10, 4))
+    s = oracle.indexer_score_causal(q, w, keys, start_pos=22, ratio=4)   # valid = 23 // 4 = 5
+    assert np.all(s[5:] == -np.inf)
+    np.testing.assert_array_equal(s[:5], oracle.indexer_score(q, w, keys)[:5])
+
+
+# ---------------------------------------------------------------------------
+# Top-k
+# ---------------------------------------------------------------------------
+
+def test_topk_golden():
+    g = _golden("indexer_tiny.json")
+    for width, expect in g["topk"].items():
+        assert oracle.topk(np.array(g["scores"]), int(width)).tolist() == expect
+
+
+def _topk_bruteforce(s, width):
+    """Rank every finite entry by counting the entries that beat it."""
+    n = len(s)
+    finite = [math.isfinite(x) for x in s]
+    out = [-1] * width
+    for j in range(n):
+        if not finite[j]:
+            continue
+        rank = sum(1 for i in range(n) if finite[i] and (s[i] > s[j] or (s[i] == s[j] and i < j)))
+        if rank < width:
+            out[rank] = j
+    return out
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_topk_bruteforce_with_ties_and_nonfinite(seed):
+    rng = np.random.default_rng(100 + seed)
+    n = int(rng.integers(1, 60))
+    s = rng.integers(-4, 5, size=n).astype(float) * 0.5
+    s[rng.random(n) < 0.15] = np.nan
+    s[rng.random(n) < 0.05] = np.inf
+    s[rng.random(n) < 0.05] = -np.inf
+    s[rng.random(n) < 0.2] = -0.0
+    for width in (1, 3, n, n + 4):
+        assert oracle.topk(s, width).tolist() == _topk_bruteforce(s.tolist(), width)
+
+
+def test_topk_matches_stable_argsort():
+    s = workloads.random_scores(7, [3000], ties=True)[0].astype(float)
+    ref = np.argsort(-s, kind="stable")[:512]
+    assert oracle.topk(s, 512).tolist() == ref.tolist()
+
+
+def test_topk_signed_zero_ties():
+    s = np.array([-0.0, 0.0, -0.0, -1.0, 0.0])
+    assert oracle.topk(s, 5).tolist() == [0, 1, 2, 4, 3]
+
+
+def test_topk_causal_offset_and_fill():
+    s = np.arange(10, dtype=float)                  # best is the highest index
+    out = oracle.topk_causal(s, start_pos=15, offset=100, ratio=4, width=6)  # valid = 4
+    assert out.tolist() == [103, 102, 101, 100, -1, -1]
+
+
+# ---------------------------------------------------------------------------
+# Sparse attention
+# ---------------------------------------------------------------------------
+
+def test_attention_golden():
+    g = _golden("attention_tiny.json")
+    out, inv = oracle.sparse_attention(np.array(g["q"], float), np.array(g["kv"], float),
+                                       np.array(g["indices"]), np.array(g["sinks"]), g["scale"])
+    np.testing.assert_allclose(out, g["out"], rtol=1e-15, atol=1e-15)
+    assert not inv.any()
+    k1 = g["kv_len_1"]
+    out, inv = oracle.sparse_attention(np.array(k1["q"], float), np.array(k1["kv"], float),
+                                       np.array(k1["indices"]), np.array(k1["sinks"]), k1["scale"])
+    np.testing.assert_allclose(out, k1["out"], rtol=1e-15)
+
+
+def test_attention_dense_closed_form():
+    """width = kv_len, every row selected and a sink whose exp is 0 in fp32:
+    dense softmax attention softmax(scale q K^T) K."""
+    rng = np.random.default_rng(21)
+    H, F, L = 4, 16, 9
+    q, kv = rng.standard_normal((H, F)), rng.standard_normal((L, F))
+    scale = 1 / math.sqrt(F)
+    out, inv = oracle.sparse_attention(q, kv, np.arange(L), np.full(H, -3.0e38), scale)
+    dense = scipy.special.softmax(scale * np.einsum("hf,lf->hl", q, kv), axis=1) @ kv
+    np.testing.assert_allclose(out, dense, rtol=1e-12, atol=1e-14)
+    assert not inv.any()
+
+
+def test_attention_sink_identity():
+    """O(sink) = O(no sink) * S / (S + e^sink), S = sum_t e^{l_t} per head."""
+    rng = np.random.default_rng(22)
+    H, F, L = 5, 12, 20
+    q, kv = rng.standard_normal((H, F)), rng.standard_normal((L, F))
+    idx = rng.permutation(L)[:11]
+    scale = 0.3
+    sinks = rng.standard_normal(H) * 2
+    with_sink, _ = oracle.sparse_attention(q, kv, idx, sinks, scale)
+    no_sink, _ = oracle.sparse_attention(q, kv, idx, np.full(H, -3.0e38), scale)
+    for h in range(H):
+        S = sum(math.exp(scale * float(np.dot(q[h], kv[j]))) for j in idx)
+        np.testing.assert_allclose(with_sink[h], no_sink[h] * S / (S + math.exp(sinks[h])),
+                                   rtol=1e-12, atol=1e-15)
+
+
+def test_attention_slot_order_and_sentinels():
+    """A set function of the selected rows: slot order and -1 sentinels do not matter."""
+    rng = np.random.default_rng(23)
+    H, F, L = 3, 8, 30
+    q, kv, sinks = rng.standard_normal((H, F)), rng.standard_normal((L, F)), rng.standard_normal(H)
+    idx = rng.permutation(L)[:10]
+    a, _ = oracle.sparse_attention(q, kv, idx, sinks, 0.5)
+    mixed = np.insert(idx[::-1], [2, 5, 5], -1)
+    b, _ = oracle.sparse_attention(q, kv, mixed, sinks, 0.5)
+    np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-15)
+
+
+def test_attention_all_sentinels_is_zero():
+    q, kv = np.ones((2, 4)), np.ones((3, 4))
+    out, inv = oracle.sparse_attention(q, kv, np.array([-1, -1]), np.zeros(2), 1.0)
+    assert np.all(out == 0) and not inv.any()
+
+
+def test_attention_fail_closed():
+    rng = np.random.default_rng(24)
+    H, F, L = 4, 8, 12
+    q, kv, sinks = rng.standard_normal((H, F)), rng.standard_normal((L, F)), rng.standard_normal(H)
+    idx = np.array([3, 7, 1, -1])
+    base, inv = oracle.sparse_attention(q, kv, idx, sinks, 0.5)
+    assert not inv.any() and np.all(base != 0)
+    # non-finite q in head 2 -> head 2 zero only
+    q2 = q.copy(); q2[2, 5] = np.nan
+    out, inv = oracle.sparse_attention(q2, kv, idx, sinks, 0.5)
+    assert inv.tolist() == [False, False, True, False] and np.all(out[2] == 0)
+    np.testing.assert_array_equal(out[[0, 1, 3]], base[[0, 1, 3]])
+    # non-finite KV on a selected row -> every head zero
+    kv2 = kv.copy(); kv2[7, 0] = np.inf
+    out, inv = oracle.sparse_attention(q, kv2, idx, sinks, 0.5)
+    assert inv.all() and np.all(out == 0)
+    # ... but not on an unselected row
+    kv3 = kv.copy(); kv3[0, 0] = np.nan
+    out, inv = oracle.sparse_attention(q, kv3, idx, sinks, 0.5)
+    np.testing.assert_array_equal(out, base)
+    # out-of-range index -> every head zero
+    for bad in (L, -2):
+        out, inv = oracle.sparse_attention(q, kv, np.array([3, bad, 1]), sinks, 0.5)
+        assert inv.all() and np.all(out == 0)
+    # non-finite sink -> that head zero
+    s2 = sinks.copy(); s2[1] = np.inf
+    out, inv = oracle.sparse_attention(q, kv, idx, s2, 0.5)
+    assert inv.tolist() == [False, True, False, False]
+
+
+def test_attention_lazy_rows_equal_dense():
+    """`sparse_attention_rows` (widens only selected rows) equals `sparse_attention`."""
+    rng = np.random.default_rng(25)
+    L = 40
+    bits = workloads.bf16_bits(rng.standard_normal((L, 16)).astype(np.float32))
+    q = rng.standard_normal((3, 16))
+    sinks = rng.standard_normal(3)
+    for idx in (np.array([5, 5, -1, 39, 0]), np.array([2, L, 1]), np.array([-1, -1])):
+        a = oracle.sparse_attention(q, oracle.bf16_to_f64(bits), idx, sinks, 0.25)
+        b = oracle.sparse_attention_rows(q, oracle._LazyRows(bits, L), idx, sinks, 0.25)
+        np.testing.assert_array_equal(a[0], b[0])
+        np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_round_bf16_against_bit_rounding():
+    """fp32-representable values: the log/rint rounding equals the integer
+    round-half-even on the fp32 bit pattern (an independent method)."""
+    rng = np.random.default_rng(26)
+    x = rng.standard_normal(20000).astype(np.float32) * np.float32(3.0)
+    x[:8] = [1.00390625, 1.01171875, -1.00390625, 0.0, 2.0 ** -130, 3.0, -7.5, 1e-3]
+    via_bits = workloads.bits_to_f32(workloads.bf16_bits(x)).astype(np.float64)
+    np.testing.assert_array_equal(oracle.round_bf16(x.astype(np.float64)), via_bits)
+
+
+def test_bf16_decode_exact():
+    vals = np.array([1.0, -2.5, 3.140625, 0.0078125], np.float32)
+    bits = (vals.view(np.uint32) >> 16).astype(np.uint16)
+    np.testing.assert_array_equal(oracle.bf16_to_f64(bits), vals.astype(np.float64))
+
+
+# ---------------------------------------------------------------------------
+# Decode composition on a small workload
+# ---------------------------------------------------------------------------
+
+def test_decode_integer_workload_exact_scores():
+    """Config-1-style integer inputs: every score is an exact integer, and the
+    selected set's minimum beats every unselected score (ties: lower index)."""
+    wl = workloads.make_workload("t", 5, [40, 600], integer=True, per_row_sinks=False)
+    res = oracle.decode(wl)
+    for e, r in enumerate(wl.rows):
+        q = oracle.bf16_to_f64(wl.q_index[r.q_row]).astype(int).tolist()
+        w = wl.w_index[r.q_row].astype(int).tolist()
+        keys = oracle.bf16_to_f64(wl.keys[e]).astype(int).tolist()
+        assert [Fraction(x) for x in res[e]["scores"]] == _indexer_exact(q, w, keys)
+        assert res[e]["indices"].tolist() == _topk_bruteforce(res[e]["scores"].tolist(), r.width)
+
+
+# ---------------------------------------------------------------------------
+# Planted mistakes: each must be caught by one of the pins above
+# ---------------------------------------------------------------------------
+
+def _no_relu(q, w, keys):
+    return (np.asarray(keys) @ np.asarray(q).T) @ np.asarray(w)
+
+
+def _transposed_weights(q, w, keys):
+    d = np.asarray(keys) @ np.asarray(q).T
+    return np.maximum(d, 0) @ np.asarray(w)[::-1]
+
+
+def _topk_high_index_ties(scores, width):
+    s = np.asarray(scores, float)
+    cand = np.nonzero(np.isfinite(s))[0]
+    order = cand[np.lexsort((-cand, -s[cand]))]
+    out = np.full(width, -1, np.int32)
+    out[: min(width, len(order))] = order[:width]
+    return out
+
+
+_REAL_ATTENTION = oracle.sparse_attention
+
+
+def _attention_sink_with_value(q, kv, idx, sinks, scale):
+    out, inv = _REAL_ATTENTION(q, kv, idx, sinks, scale)
+    # mistake: the sink's mass goes to a value row (the first selected one)
+    return out * 0.9 + 0.1 * np.asarray(kv)[max(int(idx[0]), 0)], inv
+
+
+def test_planted_mistakes_are_caught(monkeypatch):
+    caught = []
+    for name, fake in [("indexer_score", _no_relu), ("indexer_score", _transposed_weights),
+                       ("topk", _topk_high_index_ties),
+                       ("sparse_attention", _attention_sink_with_value)]:
+        monkeypatch.setattr(oracle, name, fake)
+        tests = {
+            "indexer_score": [test_indexer_golden, test_indexer_relu_identity,
+                              test_indexer_one_hot_weights_select_head],
+            "topk": [test_topk_golden, test_topk_signed_zero_ties],
+            "sparse_attention": [test_attention_golden, test_attention_dense_closed_form],
+        }[name]
+        failed = 0
+        for t in tests:
+            try:
+                t()
+            except AssertionError:
+                failed += 1
+        caught.append(failed > 0)
+        monkeypatch.undo()
+    assert all(caught), caught
