@@ -1,0 +1,319 @@
+"""Benchmark of the fused ragged decode step (indexer -> top-512 -> gather -> sink attention).
+
+Workload: 8 rows x 131072 keys (the long-context, bandwidth-bound decode case),
+seeded synthetic bf16 inputs shaped like the DeepSeek-V4 decode rows.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line. `value` is decode rows/s over all ranks (each rank runs
+its own 8 rows: rows are independent, so N GPUs are N replicas, weak scaling,
+no data exchange). Every timed step is bracketed by CUDA events on the
+launching stream; between steps a 512 MiB buffer is written to flush L2.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+CONFIG_INDEX = 3
+METRIC = "decode rows/s (8 rows, 128K ctx) and achieved HBM GB/s vs GB300 peak"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--config", type=int, default=CONFIG_INDEX)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx = [], []
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, single-threaded BLAS, bounded sample
+# ---------------------------------------------------------------------------
+
+_CPU_SNIPPET = r"""
+import json, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np, oracle, workloads
+wl = workloads.config({cfg})
+budget = {budget}
+t0 = time.perf_counter(); rows = 0
+for e in range(wl.num_rows):
+    oracle.decode(wl, entries=[e]); rows += 1
+    if time.perf_counter() - t0 > budget: break
+dt = time.perf_counter() - t0
+print(json.dumps({{"rows": rows, "seconds": dt}}))
+"""
+
+
+def cpu_baseline(cfg: int, budget_s: float = 12.0):
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[v] = "1"
+    env.pop("CUDA_VISIBLE_DEVICES", None)
+    code = _CPU_SNIPPET.format(root=ROOT, cfg=cfg, budget=budget_s)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        return {"value": None, "unit": "rows/s", "cores": 1, "kind": "oracle", "error": r.stderr[-300:]}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": d["rows"] / d["seconds"], "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": f"{d['rows']} of the 8 rows (131072 keys each), numpy float64 oracle, "
+                      f"single-threaded BLAS, {d['seconds']:.1f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    cb = cpu_baseline(args.config, budget_s=max(5.0, 20.0 / max(1, args.steps)))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "rows/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": (8 / cb["value"] * 1e3) if cb.get("value") else None,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "8 rows x 131072 keys (bounded sample of rows)", "rows": 8, "kv_len": 131072},
+        "cpu_baseline": {k: cb.get(k) for k in ("value", "kind", "cores", "sample", "unit")},
+        "e2e": {"value": cb["value"], "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# native arm
+# ---------------------------------------------------------------------------
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", torch.cuda.current_device() if world == 1 else local)
+
+    import deepseek_sparse_attention_ragged_gb300 as ds
+    import workloads
+    from workloads.device import to_device
+
+    ds.build()
+    ds.load()
+
+    wl = workloads.config(args.config)
+    dev = to_device(wl, device)
+    R = wl.num_rows
+    nq = max(r.q_row for r in wl.rows) + 1
+    out = torch.empty((nq, 64, 512), dtype=torch.bfloat16, device=device)
+    idx = torch.empty((wl.index_elements,), dtype=torch.int32, device=device)
+    ws = ds.workspace(wl.rows, device)
+    stream = torch.cuda.Stream(device)
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device)
+
+    def step():
+        ds.ds_rows_decode(dev.rows, dev.q_index, dev.w_index, dev.keys, dev.q_attn, dev.kv, dev.sinks,
+                          dev.sinks_row_stride, dev.scale, out, indices=idx, stream=stream)
+
+    def barrier():
+        torch.cuda.synchronize(device)
+        if world > 1:
+            torch.distributed.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    barrier()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(device.index or 0) as clocks:
+        barrier()
+        with torch.cuda.stream(stream):
+            for k in range(args.steps):
+                flush.fill_(k & 0xFF)
+                starts[k].record(stream)
+                step()
+                ends[k].record(stream)
+        barrier()
+    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(times)
+    if world > 1:
+        t = torch.tensor([total_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * R * args.steps / (total_ms / 1e3)
+    alg_bytes = wl.algorithmic_bytes()
+    step_gbs = alg_bytes / (ms_per_step / 1e3) / 1e9
+
+    # Dominant kernel (the indexer) alone: same kernel, same launch shape, through its entry point.
+    stride = max(r.kv_len for r in wl.rows)
+    scores = torch.empty((R, stride), dtype=torch.float32, device=device)
+    n_idx = 20
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_idx)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            ds.ds_rows_indexer_score(dev.rows, dev.q_index, dev.w_index, dev.keys, scores, stride, stream=stream)
+        for a, b in ev:
+            flush.fill_(1)
+            a.record(stream)
+            ds.ds_rows_indexer_score(dev.rows, dev.q_index, dev.w_index, dev.keys, scores, stride, stream=stream)
+            b.record(stream)
+    torch.cuda.synchronize(device)
+    idx_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    idx_bytes = sum(256 * r.kv_len + 4 * r.kv_len + 16384 + 256 for r in wl.rows)
+    peak, peak_kind = peaks()
+    idx_gbs = idx_bytes / (idx_ms / 1e3) / 1e9
+
+    # End to end through the public call: per step the queries, head weights and
+    # sinks go host->device from pinned memory, the output comes back (caches stay
+    # resident: they are the decode state).
+    h_qI = dev.q_index.cpu().pin_memory()
+    h_wI = dev.w_index.cpu().pin_memory()
+    h_qA = dev.q_attn.cpu().pin_memory()
+    h_sk = dev.sinks.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_qI, h_wI, h_qA, h_sk))
+    d2h = h_out.numel() * h_out.element_size()
+    e2e_steps = max(5, args.steps // 2)
+    barrier()
+    with torch.cuda.stream(stream):
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(e2e_steps):
+            dev.q_index.copy_(h_qI, non_blocking=True)
+            dev.w_index.copy_(h_wI, non_blocking=True)
+            dev.q_attn.copy_(h_qA, non_blocking=True)
+            dev.sinks.copy_(h_sk, non_blocking=True)
+            step()
+            h_out.copy_(out, non_blocking=True)
+        t1.record(stream)
+    barrier()
+    e2e_ms = t0.elapsed_time(t1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank == 0:
+        cb = None
+        if world == 1 and not args.no_cpu_baseline:
+            cb = cpu_baseline(args.config)
+        line = {
+            "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{R} rows x {stride} keys (indexer 64x128, attention 64x512, top-512)",
+                       "rows": R, "kv_len": stride, "l2": "flushed between steps (512 MiB write)",
+                       "parallelism": f"replicas{world}"},
+            "step_gbs": step_gbs, "step_frac_of_peak": step_gbs / peak,
+            "algorithmic_bytes_per_step": alg_bytes,
+            "roofline": {"kernel": "indexer_score_kernel", "bound": "hbm", "achieved": idx_gbs, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": idx_gbs / peak, "traffic": None,
+                         "bytes_per_launch": idx_bytes, "ms_per_launch": idx_ms},
+            "e2e": {"value": world * R / (e2e_ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": 4 * args.steps,
+            "clocks": clocks.summary(),
+            "cpu_baseline": cb,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

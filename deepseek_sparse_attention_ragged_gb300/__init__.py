@@ -1,0 +1,278 @@
+"""Python binding of libdsrows: ragged DeepSeek sparse-attention decode on GB300.
+
+Thin ctypes marshalling over the C-ABI declared in ``include/dsrows.h``. Every
+step of the computation runs in the library's CUDA kernels; this module only
+checks tensor types and sizes (as the mlx-native dispatch functions of
+``src/ops/deepseek_rows.rs`` do with their ``require`` checks), gathers raw
+pointers and calls the entry point of the same name. PyTorch provides device
+memory and streams.
+
+The library must be built first (``build()``); without it every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Iterable, List, Optional, Sequence
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "DsRowsError", "Row", "load", "build", "library_path",
+    "ds_rows_workspace_bytes", "workspace", "ds_rows_indexer_score", "ds_rows_topk",
+    "ds_rows_sparse_attn", "ds_rows_decode", "ds_rows_version",
+    "ROWS_MAX", "INDEX_HEADS", "INDEX_DIM", "TOP_K", "HEADS", "DIM",
+]
+
+ROWS_MAX = 8
+INDEX_HEADS = 64
+INDEX_DIM = 128
+TOP_K = 512
+HEADS = 64
+DIM = 512
+
+DS_OK = 0
+
+
+class DsRowsError(RuntimeError):
+    """A call rejected by the library (bad argument, size, alignment, CUDA error)."""
+
+    def __init__(self, code: int, message: str):
+        super().__init__(f"[{code}] {message}")
+        self.code = code
+
+
+class Row(ctypes.Structure):
+    """One entry of the row table: ds_row_t {kv_len, width, index_offset, q_row}."""
+
+    _fields_ = [("kv_len", ctypes.c_uint32), ("width", ctypes.c_uint32),
+                ("index_offset", ctypes.c_uint32), ("q_row", ctypes.c_uint32)]
+
+
+class _RowSet(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int), ("table", ctypes.POINTER(Row)),
+                ("index_keys", ctypes.POINTER(ctypes.c_void_p)), ("kv", ctypes.POINTER(ctypes.c_void_p))]
+
+
+_LIB = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def build(force: bool = False) -> str:
+    """Compile libdsrows.so in-tree (nvcc, sm_103a)."""
+    return _build.build(force=force)
+
+
+def load():
+    """Load libdsrows.so; raises if it has not been built."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libdsrows is not built ({path} missing); call "
+                           "deepseek_sparse_attention_ragged_gb300.build()")
+    lib = ctypes.CDLL(path)
+    vp, sz, i32, u32p = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p
+    rs = ctypes.POINTER(_RowSet)
+    lib.ds_rows_workspace_bytes.argtypes = [i32, ctypes.POINTER(Row)]
+    lib.ds_rows_workspace_bytes.restype = sz
+    lib.ds_rows_indexer_score.argtypes = [rs, vp, vp, vp, sz, vp]
+    lib.ds_rows_indexer_score.restype = i32
+    lib.ds_rows_topk.argtypes = [rs, vp, sz, vp, vp, sz, vp]
+    lib.ds_rows_topk.restype = i32
+    lib.ds_rows_sparse_attn.argtypes = [rs, vp, vp, sz, vp, ctypes.c_float, vp, u32p, vp, sz, vp]
+    lib.ds_rows_sparse_attn.restype = i32
+    lib.ds_rows_decode.argtypes = [rs, vp, vp, vp, vp, sz, ctypes.c_float, vp, vp, u32p, vp, sz, vp]
+    lib.ds_rows_decode.restype = i32
+    lib.ds_rows_last_error.argtypes = []
+    lib.ds_rows_last_error.restype = ctypes.c_char_p
+    lib.ds_rows_version.argtypes = []
+    lib.ds_rows_version.restype = ctypes.c_char_p
+    _LIB = lib
+    return lib
+
+
+def ds_rows_version() -> str:
+    return load().ds_rows_version().decode()
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+
+def _table(rows) -> "ctypes.Array":
+    rows = list(rows)
+    arr = (Row * max(1, len(rows)))()
+    for i, r in enumerate(rows):
+        if isinstance(r, Row):
+            arr[i] = r
+        elif hasattr(r, "kv_len"):
+            arr[i] = Row(r.kv_len, r.width, r.index_offset, r.q_row)
+        else:
+            arr[i] = Row(*r)
+    return arr, len(rows)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _check(lib, rc: int):
+    if rc != DS_OK:
+        raise DsRowsError(rc, lib.ds_rows_last_error().decode())
+
+
+def _require(t: Optional[torch.Tensor], name: str, dtype, numel: int, *, optional=False):
+    """`t` must be a contiguous CUDA tensor of `dtype` holding >= numel elements."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, needs {numel}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _rowset(tab, n, keys=None, kv=None, rows=None):
+    ks = kvs = None
+    if keys is not None:
+        ks = (ctypes.c_void_p * n)(*[k.data_ptr() for k in keys])
+    if kv is not None:
+        kvs = (ctypes.c_void_p * n)(*[k.data_ptr() for k in kv])
+    rs = _RowSet(n, ctypes.cast(tab, ctypes.POINTER(Row)),
+                 ctypes.cast(ks, ctypes.POINTER(ctypes.c_void_p)) if ks is not None else None,
+                 ctypes.cast(kvs, ctypes.POINTER(ctypes.c_void_p)) if kvs is not None else None)
+    return rs, (ks, kvs)
+
+
+def _rows_list(rows) -> List:
+    out = []
+    for r in rows:
+        if isinstance(r, Row) or hasattr(r, "kv_len"):
+            out.append((int(r.kv_len), int(r.width), int(r.index_offset), int(r.q_row)))
+        else:
+            out.append(tuple(int(x) for x in r))
+    return out
+
+
+def _check_caches(caches: Sequence[torch.Tensor], rows, dim: int, name: str):
+    if len(caches) != len(rows):
+        raise ValueError(f"{name}: {len(caches)} caches for {len(rows)} rows")
+    for e, (c, r) in enumerate(zip(caches, rows)):
+        _require(c, f"{name}[{e}]", torch.bfloat16, r[0] * dim)
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+
+def ds_rows_workspace_bytes(rows) -> int:
+    lib = load()
+    tab, n = _table(rows)
+    b = lib.ds_rows_workspace_bytes(n, tab)
+    if b == 0:
+        raise DsRowsError(-1, lib.ds_rows_last_error().decode())
+    return int(b)
+
+
+def workspace(rows, device=None) -> torch.Tensor:
+    """A workspace tensor (uint8, 256-byte aligned by the caching allocator)."""
+    return torch.empty(ds_rows_workspace_bytes(rows), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def ds_rows_indexer_score(rows, q_index, w_index, index_keys, scores, score_stride=None, stream=None):
+    """Indexer scores of every row into `scores` (fp32, row e at e*score_stride)."""
+    lib = load()
+    rl = _rows_list(rows)
+    q_rows = max(r[3] for r in rl) + 1
+    _require(q_index, "q_index", torch.bfloat16, q_rows * INDEX_HEADS * INDEX_DIM)
+    _require(w_index, "w_index", torch.float32, q_rows * INDEX_HEADS)
+    _check_caches(index_keys, rl, INDEX_DIM, "index_keys")
+    if score_stride is None:
+        score_stride = scores.shape[-1] if scores.dim() > 1 else max(r[0] for r in rl)
+    _require(scores, "scores", torch.float32, (len(rl) - 1) * score_stride + max(r[0] for r in rl))
+    tab, n = _table(rl)
+    rs, keep = _rowset(tab, n, keys=index_keys)
+    _check(lib, lib.ds_rows_indexer_score(ctypes.byref(rs), _ptr(q_index), _ptr(w_index), _ptr(scores),
+                                          int(score_stride), _stream(stream)))
+
+
+def ds_rows_topk(rows, scores, score_stride, indices, workspace_t, stream=None):
+    """Top-`width` indices of each row's scores into `indices` at index_offset."""
+    lib = load()
+    rl = _rows_list(rows)
+    _require(scores, "scores", torch.float32, (len(rl) - 1) * score_stride + max(r[0] for r in rl))
+    _require(indices, "indices", torch.int32, max(r[2] + r[1] for r in rl))
+    _require(workspace_t, "workspace", torch.uint8, 0)
+    tab, n = _table(rl)
+    rs, keep = _rowset(tab, n)
+    _check(lib, lib.ds_rows_topk(ctypes.byref(rs), _ptr(scores), int(score_stride), _ptr(indices),
+                                 _ptr(workspace_t), workspace_t.numel(), _stream(stream)))
+
+
+def _attn_checks(rl, q_attn, sinks, sinks_row_stride, out, kv, invalid):
+    q_rows = max(r[3] for r in rl) + 1
+    _require(q_attn, "q_attn", torch.bfloat16, q_rows * HEADS * DIM)
+    _require(out, "out", torch.bfloat16, q_rows * HEADS * DIM)
+    _require(sinks, "sinks", torch.float32, HEADS if sinks_row_stride == 0 else q_rows * sinks_row_stride)
+    _require(invalid, "invalid", torch.int32, q_rows * HEADS, optional=True)
+    _check_caches(kv, rl, DIM, "kv")
+
+
+def ds_rows_sparse_attn(rows, q_attn, sinks, sinks_row_stride, indices, scale, out, kv,
+                        invalid=None, workspace_t=None, stream=None):
+    """Gather + sink-softmax attention of each row over its selected indices."""
+    lib = load()
+    rl = _rows_list(rows)
+    _attn_checks(rl, q_attn, sinks, sinks_row_stride, out, kv, invalid)
+    _require(indices, "indices", torch.int32, max(r[2] + r[1] for r in rl))
+    if workspace_t is None:
+        workspace_t = workspace(rl, q_attn.device)
+    tab, n = _table(rl)
+    rs, keep = _rowset(tab, n, kv=kv)
+    _check(lib, lib.ds_rows_sparse_attn(ctypes.byref(rs), _ptr(q_attn), _ptr(sinks), int(sinks_row_stride),
+                                        _ptr(indices), float(scale), _ptr(out), _ptr(invalid),
+                                        _ptr(workspace_t), workspace_t.numel(), _stream(stream)))
+
+
+def ds_rows_decode(rows, q_index, w_index, index_keys, q_attn, kv, sinks, sinks_row_stride, scale, out,
+                   indices=None, invalid=None, workspace_t=None, stream=None):
+    """The whole decode step: indexer score -> top-k -> gather + sink attention."""
+    lib = load()
+    rl = _rows_list(rows)
+    q_rows = max(r[3] for r in rl) + 1
+    _require(q_index, "q_index", torch.bfloat16, q_rows * INDEX_HEADS * INDEX_DIM)
+    _require(w_index, "w_index", torch.float32, q_rows * INDEX_HEADS)
+    _check_caches(index_keys, rl, INDEX_DIM, "index_keys")
+    _attn_checks(rl, q_attn, sinks, sinks_row_stride, out, kv, invalid)
+    _require(indices, "indices", torch.int32, max(r[2] + r[1] for r in rl), optional=True)
+    if workspace_t is None:
+        workspace_t = workspace(rl, q_attn.device)
+    tab, n = _table(rl)
+    rs, keep = _rowset(tab, n, keys=index_keys, kv=kv)
+    _check(lib, lib.ds_rows_decode(ctypes.byref(rs), _ptr(q_index), _ptr(w_index), _ptr(q_attn), _ptr(sinks),
+                                   int(sinks_row_stride), float(scale), _ptr(out), _ptr(indices), _ptr(invalid),
+                                   _ptr(workspace_t), workspace_t.numel(), _stream(stream)))

@@ -1,0 +1,385 @@
+// C-ABI entry points of libdsrows: validation, workspace layout, launches.
+//
+// Validation mirrors the row checks of mlx-native src/ops/deepseek_rows.rs
+// (check_rows, sparse_params, sparse_io_checks, the indexer's per-row
+// checks and `disjoint`), adapted to raw pointers: rows 1..8, kv_len and
+// width nonzero, scale finite and positive, q_row unique for outputs,
+// indices ranges disjoint for outputs, 32-bit ranges, plus pointer presence
+// and alignment. Everything is checked before anything is enqueued.
+
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace dsrows;
+
+namespace {
+
+thread_local std::string g_error;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_error = std::string("dsrows: ") + buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t err, const char* what) {
+    return fail(DS_ECUDA, "%s failed: %s", what, cudaGetErrorString(err));
+}
+
+constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// ---- workspace layout ------------------------------------------------------
+struct Layout {
+    size_t status = 0;  // u32 status word at offset 0
+    size_t hist, ctl, flags, ctl_end;
+    size_t cand, topk, part, scores, total;
+    uint32_t attn_chunks;
+    uint64_t score_stride;  // floats per row of the decode scores
+};
+
+Layout make_layout(int rows, const ds_row_t* table) {
+    Layout L;
+    L.hist = 256;
+    L.ctl = align256(L.hist + (size_t)kRowsMax * kHistBins * 4);
+    L.flags = align256(L.ctl + (size_t)kRowsMax * kCtlWords * 4);
+    L.ctl_end = align256(L.flags + ((size_t)kRowsMax * kHeads + kRowsMax) * 4);
+    L.cand = L.ctl_end;
+    L.topk = align256(L.cand + (size_t)rows * kCandCap * 8);
+    L.part = align256(L.topk + (size_t)kRowsMax * kTopK * 4);
+    uint32_t chunks = 0, max_len = 0;
+    for (int e = 0; e < rows; ++e) {
+        chunks += (table[e].width + kAttnSlots - 1) / kAttnSlots;
+        if (table[e].kv_len > max_len) max_len = table[e].kv_len;
+    }
+    L.attn_chunks = chunks;
+    L.scores = align256(L.part + (size_t)chunks * kPartFloats * 4);
+    L.score_stride = ((uint64_t)max_len + 63) & ~uint64_t(63);
+    L.total = align256(L.scores + (size_t)rows * L.score_stride * 4);
+    return L;
+}
+
+// ---- device facts and the tensor-map encoder --------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int num_sms() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+int get_encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode ? DS_OK : fail(DS_ECUDA, "cuTensorMapEncodeTiled is unavailable");
+}
+
+// 2D bf16 row-major [rows, 128] with a {64, box_rows} box and 128-byte swizzle.
+int encode_rows128(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows, const char* what) {
+    const cuuint64_t dims[2] = {128, rows};
+    const cuuint64_t strides[1] = {256};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(DS_ECUDA, "tensor map for %s failed (CUresult %d)", what, (int)r);
+    return DS_OK;
+}
+
+// ---- validation ----------------------------------------------------------------
+enum Needs : unsigned { kNeedKeys = 1, kNeedKv = 2, kUniqueQ = 4, kDisjointOut = 8 };
+
+int check_table(int rows, const ds_row_t* table) {
+    if (rows < 1 || rows > DS_ROWS_MAX) return fail(DS_EINVAL, "rows must be 1..=%d, got %d", DS_ROWS_MAX, rows);
+    if (!table) return fail(DS_EINVAL, "row table is NULL");
+    for (int e = 0; e < rows; ++e) {
+        const ds_row_t& r = table[e];
+        if (r.kv_len == 0 || r.width == 0) return fail(DS_EINVAL, "row %d: kv_len and width must be nonzero", e);
+        if (r.width > DS_TOPK) return fail(DS_EINVAL, "row %d: width %u exceeds %d", e, r.width, DS_TOPK);
+        if ((uint64_t)r.index_offset + r.width > 0xFFFFFFFFull)
+            return fail(DS_ESIZE, "row %d: index range exceeds u32", e);
+        if ((uint64_t)r.q_row * DS_HEADS * DS_DIM > 0xFFFFFFFFFFull)
+            return fail(DS_ESIZE, "row %d: q_row %u is out of range", e, r.q_row);
+    }
+    return DS_OK;
+}
+
+int check_set(const ds_row_set_t* set, unsigned needs) {
+    if (!set) return fail(DS_EINVAL, "row set is NULL");
+    int rc = check_table(set->rows, set->table);
+    if (rc) return rc;
+    const int rows = set->rows;
+    for (int e = 0; e < rows; ++e) {
+        if (needs & kNeedKeys) {
+            if (!set->index_keys || !set->index_keys[e]) return fail(DS_EINVAL, "row %d: indexer keys are NULL", e);
+            if (!aligned16(set->index_keys[e])) return fail(DS_EALIGN, "row %d: indexer keys not 16-B aligned", e);
+        }
+        if (needs & kNeedKv) {
+            if (!set->kv || !set->kv[e]) return fail(DS_EINVAL, "row %d: kv cache is NULL", e);
+            if (!aligned16(set->kv[e])) return fail(DS_EALIGN, "row %d: kv cache not 16-B aligned", e);
+        }
+        if (needs & kUniqueQ)
+            for (int o = 0; o < e; ++o)
+                if (set->table[o].q_row == set->table[e].q_row)
+                    return fail(DS_EINVAL, "row %d: q_row %u is used twice", e, set->table[e].q_row);
+        if (needs & kDisjointOut)
+            for (int o = 0; o < e; ++o) {
+                const uint64_t a0 = set->table[e].index_offset, a1 = a0 + set->table[e].width;
+                const uint64_t b0 = set->table[o].index_offset, b1 = b0 + set->table[o].width;
+                if (a0 < b1 && b0 < a1) return fail(DS_EINVAL, "index outputs of rows %d and %d overlap", o, e);
+            }
+    }
+    return DS_OK;
+}
+
+int check_workspace(const ds_row_set_t* set, void* ws, size_t bytes, const Layout& L) {
+    (void)set;
+    if (!ws) return fail(DS_EINVAL, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(ws) & 255) return fail(DS_EALIGN, "workspace must be 256-byte aligned");
+    if (bytes < L.total) return fail(DS_ESIZE, "workspace holds %zu bytes, needs %zu", bytes, L.total);
+    return DS_OK;
+}
+
+uint32_t max_q_row(const ds_row_set_t* set) {
+    uint32_t m = 0;
+    for (int e = 0; e < set->rows; ++e) m = set->table[e].q_row > m ? set->table[e].q_row : m;
+    return m;
+}
+
+// ---- stage launchers ---------------------------------------------------------------
+int run_indexer(const ds_row_set_t* set, const ds_bf16* q_index, const float* w_index, float* scores,
+                uint64_t stride, uint32_t* hist, uint32_t* status, cudaStream_t stream) {
+    int rc = get_encoder();
+    if (rc) return rc;
+    IndexerParams p;  // ~1.3 KB with the tensor maps; built per call on the host
+    std::memset(&p, 0, sizeof(p));
+    const uint32_t tile = indexer_tile_keys();
+    uint32_t tiles = 0;
+    for (int e = 0; e < set->rows; ++e) {
+        const ds_row_t& r = set->table[e];
+        p.kv_len[e] = r.kv_len;
+        p.q_row[e] = r.q_row;
+        p.tile_begin[e] = tiles;
+        tiles += (r.kv_len + tile - 1) / tile;
+        rc = encode_rows128(&p.kmap[e], set->index_keys[e], r.kv_len, 128, "indexer keys");
+        if (rc) return rc;
+    }
+    rc = encode_rows128(&p.qmap, q_index, (uint64_t)(max_q_row(set) + 1) * DS_INDEX_HEADS, 64, "indexer q");
+    if (rc) return rc;
+    p.w = w_index;
+    p.scores = scores;
+    p.hist = hist;
+    p.status = status;
+    p.score_stride = stride;
+    p.rows = (uint32_t)set->rows;
+    p.total_tiles = tiles;
+    const int sms = num_sms();
+    if (sms <= 0) return fail(DS_ECUDA, "no CUDA device");
+    cudaError_t err = launch_indexer(p, sms, stream);
+    return err == cudaSuccess ? DS_OK : cuda_fail(err, "indexer launch");
+}
+
+int run_topk(const ds_row_set_t* set, const float* scores, uint64_t stride, int32_t* out, const uint32_t* out_offset,
+             uint8_t* ws, const Layout& L, bool with_hist, cudaStream_t stream) {
+    TopkParams p;
+    std::memset(&p, 0, sizeof(p));
+    const uint32_t chunk = topk_chunk();
+    uint32_t chunks = 0;
+    for (int e = 0; e < set->rows; ++e) {
+        p.kv_len[e] = set->table[e].kv_len;
+        p.width[e] = set->table[e].width;
+        p.out_offset[e] = out_offset[e];
+        p.chunk_begin[e] = chunks;
+        chunks += (set->table[e].kv_len + chunk - 1) / chunk;
+    }
+    p.scores = scores;
+    p.score_stride = stride;
+    p.out = out;
+    p.hist = reinterpret_cast<uint32_t*>(ws + L.hist);
+    p.ctl = reinterpret_cast<uint32_t*>(ws + L.ctl);
+    p.cand = reinterpret_cast<uint64_t*>(ws + L.cand);
+    p.status = reinterpret_cast<uint32_t*>(ws + L.status);
+    p.rows = (uint32_t)set->rows;
+    p.total_chunks = chunks;
+    cudaError_t err = cudaSuccess;
+    if (with_hist) {
+        err = launch_topk_hist(p, stream);
+        if (err != cudaSuccess) return cuda_fail(err, "top-k histogram launch");
+    }
+    err = launch_topk_select(p, stream);
+    return err == cudaSuccess ? DS_OK : cuda_fail(err, "top-k select launch");
+}
+
+int run_attention(const ds_row_set_t* set, const ds_bf16* q_attn, const float* sinks, size_t sinks_row_stride,
+                  const int32_t* indices, const uint32_t* index_offset, float scale, ds_bf16* out,
+                  uint32_t* invalid, uint8_t* ws, const Layout& L, cudaStream_t stream) {
+    AttnParams p;
+    std::memset(&p, 0, sizeof(p));
+    uint32_t chunks = 0;
+    for (int e = 0; e < set->rows; ++e) {
+        const ds_row_t& r = set->table[e];
+        p.kv[e] = reinterpret_cast<const __nv_bfloat16*>(set->kv[e]);
+        p.kv_len[e] = r.kv_len;
+        p.width[e] = r.width;
+        p.index_offset[e] = index_offset[e];
+        p.q_row[e] = r.q_row;
+        p.chunk_begin[e] = chunks;
+        chunks += (r.width + kAttnSlots - 1) / kAttnSlots;
+    }
+    p.q = reinterpret_cast<const __nv_bfloat16*>(q_attn);
+    p.sinks = sinks;
+    p.sinks_row_stride = sinks_row_stride;
+    p.indices = indices;
+    p.part = reinterpret_cast<float*>(ws + L.part);
+    p.flags = reinterpret_cast<uint32_t*>(ws + L.flags);
+    p.out = reinterpret_cast<__nv_bfloat16*>(out);
+    p.invalid = invalid;
+    p.status = reinterpret_cast<uint32_t*>(ws + L.status);
+    p.scale = scale;
+    p.rows = (uint32_t)set->rows;
+    p.total_chunks = chunks;
+    cudaError_t err = launch_attention(p, stream);
+    return err == cudaSuccess ? DS_OK : cuda_fail(err, "attention launch");
+}
+
+int check_attn_args(const ds_bf16* q_attn, const float* sinks, size_t sinks_row_stride, float scale, ds_bf16* out) {
+    if (!q_attn || !sinks || !out) return fail(DS_EINVAL, "q_attn, sinks and out must be non-NULL");
+    if (!aligned16(q_attn) || !aligned16(out)) return fail(DS_EALIGN, "q_attn and out must be 16-B aligned");
+    if (sinks_row_stride != 0 && sinks_row_stride < DS_HEADS)
+        return fail(DS_EINVAL, "sinks_row_stride must be 0 or >= %d, got %zu", DS_HEADS, sinks_row_stride);
+    if (!(scale > 0.0f) || !(scale < __builtin_huge_valf())) return fail(DS_EINVAL, "scale must be finite and positive");
+    return DS_OK;
+}
+
+int check_indexer_args(const ds_bf16* q_index, const float* w_index) {
+    if (!q_index || !w_index) return fail(DS_EINVAL, "q_index and w_index must be non-NULL");
+    if (!aligned16(q_index)) return fail(DS_EALIGN, "q_index must be 16-B aligned");
+    return DS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ds_rows_workspace_bytes(int rows, const ds_row_t* table) {
+    if (check_table(rows, table)) return 0;
+    return make_layout(rows, table).total;
+}
+
+int ds_rows_indexer_score(const ds_row_set_t* set, const ds_bf16* q_index, const float* w_index, float* scores,
+                          size_t score_stride, void* stream) {
+    int rc = check_set(set, kNeedKeys);
+    if (rc) return rc;
+    rc = check_indexer_args(q_index, w_index);
+    if (rc) return rc;
+    if (!scores) return fail(DS_EINVAL, "scores is NULL");
+    for (int e = 0; e < set->rows; ++e)
+        if (score_stride < set->table[e].kv_len)
+            return fail(DS_EINVAL, "score_stride %zu is shorter than row %d (kv_len %u)", score_stride, e,
+                        set->table[e].kv_len);
+    return run_indexer(set, q_index, w_index, scores, score_stride, nullptr, nullptr, (cudaStream_t)stream);
+}
+
+int ds_rows_topk(const ds_row_set_t* set, const float* scores, size_t score_stride, int32_t* indices,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_set(set, kDisjointOut);
+    if (rc) return rc;
+    if (!scores || !indices) return fail(DS_EINVAL, "scores and indices must be non-NULL");
+    for (int e = 0; e < set->rows; ++e)
+        if (score_stride < set->table[e].kv_len)
+            return fail(DS_EINVAL, "score_stride %zu is shorter than row %d (kv_len %u)", score_stride, e,
+                        set->table[e].kv_len);
+    const Layout L = make_layout(set->rows, set->table);
+    rc = check_workspace(set, workspace, workspace_bytes, L);
+    if (rc) return rc;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t err = cudaMemsetAsync(ws, 0, L.ctl_end, s);
+    if (err != cudaSuccess) return cuda_fail(err, "workspace clear");
+    uint32_t off[DS_ROWS_MAX];
+    for (int e = 0; e < set->rows; ++e) off[e] = set->table[e].index_offset;
+    return run_topk(set, scores, score_stride, indices, off, ws, L, true, s);
+}
+
+int ds_rows_sparse_attn(const ds_row_set_t* set, const ds_bf16* q_attn, const float* sinks,
+                        size_t sinks_row_stride, const int32_t* indices, float scale, ds_bf16* out,
+                        uint32_t* invalid, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_set(set, kNeedKv | kUniqueQ);
+    if (rc) return rc;
+    rc = check_attn_args(q_attn, sinks, sinks_row_stride, scale, out);
+    if (rc) return rc;
+    if (!indices) return fail(DS_EINVAL, "indices is NULL");
+    const Layout L = make_layout(set->rows, set->table);
+    rc = check_workspace(set, workspace, workspace_bytes, L);
+    if (rc) return rc;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t err = cudaMemsetAsync(ws, 0, L.ctl_end, s);
+    if (err != cudaSuccess) return cuda_fail(err, "workspace clear");
+    uint32_t off[DS_ROWS_MAX];
+    for (int e = 0; e < set->rows; ++e) off[e] = set->table[e].index_offset;
+    return run_attention(set, q_attn, sinks, sinks_row_stride, indices, off, scale, out, invalid, ws, L, s);
+}
+
+int ds_rows_decode(const ds_row_set_t* set, const ds_bf16* q_index, const float* w_index, const ds_bf16* q_attn,
+                   const float* sinks, size_t sinks_row_stride, float scale, ds_bf16* out, int32_t* indices,
+                   uint32_t* invalid, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_set(set, kNeedKeys | kNeedKv | kUniqueQ | (indices ? kDisjointOut : 0u));
+    if (rc) return rc;
+    rc = check_indexer_args(q_index, w_index);
+    if (rc) return rc;
+    rc = check_attn_args(q_attn, sinks, sinks_row_stride, scale, out);
+    if (rc) return rc;
+    const Layout L = make_layout(set->rows, set->table);
+    rc = check_workspace(set, workspace, workspace_bytes, L);
+    if (rc) return rc;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t err = cudaMemsetAsync(ws, 0, L.ctl_end, s);
+    if (err != cudaSuccess) return cuda_fail(err, "workspace clear");
+    float* scores = reinterpret_cast<float*>(ws + L.scores);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
+    uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
+    rc = run_indexer(set, q_index, w_index, scores, L.score_stride, hist, status, s);
+    if (rc) return rc;
+    int32_t* idx = indices;
+    uint32_t off[DS_ROWS_MAX];
+    for (int e = 0; e < set->rows; ++e) off[e] = indices ? set->table[e].index_offset : (uint32_t)(e * DS_TOPK);
+    if (!idx) idx = reinterpret_cast<int32_t*>(ws + L.topk);
+    rc = run_topk(set, scores, L.score_stride, idx, off, ws, L, false, s);
+    if (rc) return rc;
+    return run_attention(set, q_attn, sinks, sinks_row_stride, idx, off, scale, out, invalid, ws, L, s);
+}
+
+const char* ds_rows_last_error(void) { return g_error.c_str(); }
+
+const char* ds_rows_version(void) { return "dsrows 0.1.0 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,78 @@
+// Launch tables and launchers of the dsrows kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "dsrows.h"
+
+namespace dsrows {
+
+// Indexer score: one TMA tensor map per row's key cache, one for the queries.
+struct IndexerParams {
+    CUtensorMap kmap[DS_ROWS_MAX];  // bf16 [kv_len, 128], box {64, 128}, 128-B swizzle
+    CUtensorMap qmap;               // bf16 [Q*64, 128], box {64, 64}, 128-B swizzle
+    const float* w;                 // [Q, 64]
+    float* scores;                  // entry e at e * score_stride
+    uint32_t* hist;                 // optional [8][2048] score-key histogram
+    uint32_t* status;               // device status word
+    uint64_t score_stride;
+    uint32_t rows;
+    uint32_t total_tiles;
+    uint32_t kv_len[DS_ROWS_MAX];
+    uint32_t q_row[DS_ROWS_MAX];
+    uint32_t tile_begin[DS_ROWS_MAX];
+};
+
+// Top-k: histogram, candidate collection and the per-row finish.
+struct TopkParams {
+    const float* scores;
+    uint64_t score_stride;
+    int32_t* out;          // indices; entry e at out_offset[e]
+    uint32_t* hist;        // [8][2048]
+    uint32_t* ctl;         // [8][16]
+    uint64_t* cand;        // [8][kCandCap]
+    uint32_t* status;
+    uint32_t rows;
+    uint32_t total_chunks;
+    uint32_t kv_len[DS_ROWS_MAX];
+    uint32_t width[DS_ROWS_MAX];
+    uint32_t out_offset[DS_ROWS_MAX];
+    uint32_t chunk_begin[DS_ROWS_MAX];
+};
+
+// Sparse attention: per-row KV pointers and the split of each row's slots.
+struct AttnParams {
+    const __nv_bfloat16* kv[DS_ROWS_MAX];
+    const __nv_bfloat16* q;       // [Q, 64, 512]
+    const float* sinks;
+    uint64_t sinks_row_stride;
+    const int32_t* indices;
+    float* part;                  // partials
+    uint32_t* flags;              // [8][64] head-invalid bits (+ row bits at [8*64 + e])
+    __nv_bfloat16* out;           // [Q, 64, 512]
+    uint32_t* invalid;            // optional [Q, 64]
+    uint32_t* status;
+    float scale;
+    uint32_t rows;
+    uint32_t total_chunks;
+    uint32_t kv_len[DS_ROWS_MAX];
+    uint32_t width[DS_ROWS_MAX];
+    uint32_t index_offset[DS_ROWS_MAX];
+    uint32_t q_row[DS_ROWS_MAX];
+    uint32_t chunk_begin[DS_ROWS_MAX];  // first attention chunk of each row
+};
+
+size_t indexer_smem_bytes();
+uint32_t indexer_tile_keys();
+cudaError_t launch_indexer(const IndexerParams& p, int num_sms, cudaStream_t stream);
+
+uint32_t topk_chunk();  // scores per histogram / collection CTA
+cudaError_t launch_topk_hist(const TopkParams& p, cudaStream_t stream);
+cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t stream);
+
+cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
+
+}  // namespace dsrows

@@ -1,0 +1,173 @@
+/*
+ * dsrows: one decode step of DeepSeek-style sparse attention over up to eight
+ * independent rows (requests), each with its own caches and its own length,
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the DeepSeek-V4 joint-decode kernels of the mlx-native
+ * crate: `src/shaders/deepseek_rows.metal` (sections "Lightning indexer score
+ * and deterministic top-512" and "Sparse attention (selected shared-KV rows
+ * with learned sinks)") and their dispatch in `src/ops/deepseek_rows.rs`
+ * (`dispatch_deepseek_indexer_rows`, `dispatch_deepseek_sparse_attention_rows`,
+ * row structs `DeepSeekIndexerRow` / `DeepSeekSparseAttentionRow`).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor pointers are DEVICE pointers, owned by the caller, which also
+ *   guarantees their sizes (stated per argument). The library allocates no
+ *   memory and never synchronises the host; every entry point only enqueues
+ *   work on `stream` (a cudaStream_t; NULL is the legacy default stream).
+ * - bf16 tensors are passed as `ds_bf16` (uint16_t bit patterns).
+ * - Arguments are validated on the host before anything is enqueued. On a
+ *   bad argument the call enqueues nothing, returns a negative `DS_E*` code
+ *   and sets a message readable with ds_rows_last_error() (per host thread).
+ *   A CUDA launch failure returns DS_ECUDA.
+ * - Bad DATA (NaN/Inf inputs, an out-of-range index) is not a call error: it
+ *   zeroes the affected attention heads ("fail closed") and is reported in
+ *   the optional `invalid` output.
+ * - Row `r` of a joint call is bitwise equal to a call with only row `r`: all
+ *   tiling, split counts and reduction orders depend on that row's kv_len and
+ *   width alone.
+ * - Calls that share a workspace or an output must not overlap in time
+ *   (order them on one stream).
+ */
+#ifndef DSROWS_H
+#define DSROWS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DS_ROWS_MAX 8     /* rows per call (binding slots per cache family) */
+#define DS_INDEX_HEADS 64 /* indexer query heads */
+#define DS_INDEX_DIM 128  /* indexer key / query width */
+#define DS_TOPK 512       /* most selected KV rows per row */
+#define DS_HEADS 64       /* attention heads */
+#define DS_DIM 512        /* shared-KV row width (K and V) */
+
+/* Status codes. */
+#define DS_OK 0
+#define DS_EINVAL (-1) /* a bad argument (message says which) */
+#define DS_ESIZE (-2)  /* workspace too small, or a size overflows 32 bits */
+#define DS_EALIGN (-3) /* a pointer is not aligned as required */
+#define DS_ECUDA (-4)  /* a CUDA call failed while enqueueing */
+
+typedef uint16_t ds_bf16;
+
+/*
+ * One row of a call (`DeepSeekSparseAttentionRow` plus the indexer's fields).
+ *   kv_len       keys / KV rows in the row's caches (> 0).
+ *   width        selected slots of the row, 1..512. The decode step uses
+ *                min(512, kv_len); the top-k stage writes exactly `width`
+ *                indices, -1 in slots past the row's finite scores.
+ *   index_offset element offset of the row's `width` int32 indices in the
+ *                indices buffer.
+ *   q_row        row of the [*, 64, 128] / [*, 64, 512] queries, the [*, 64]
+ *                head weights, per-row sinks, outputs and invalid flags.
+ */
+typedef struct {
+    uint32_t kv_len;
+    uint32_t width;
+    uint32_t index_offset;
+    uint32_t q_row;
+} ds_row_t;
+
+/*
+ * The rows of a call: `rows` entries of `table` (host memory), and per entry
+ * a device pointer to its caches (host arrays of `rows` pointers):
+ *   index_keys[e]  bf16 [kv_len, 128] row-major indexer keys   (16-B aligned)
+ *   kv[e]          bf16 [kv_len, 512] row-major shared K/V rows (16-B aligned)
+ * A call reads only the cache family it needs; the other may be NULL.
+ */
+typedef struct {
+    int rows;
+    const ds_row_t* table;
+    const ds_bf16* const* index_keys;
+    const ds_bf16* const* kv;
+} ds_row_set_t;
+
+/*
+ * Workspace bytes that every entry point below needs for this row table
+ * (the largest need over the entry points). 0 when the table is invalid
+ * (see ds_rows_last_error). The workspace must be 256-byte aligned; its
+ * contents need no initialisation and are scratch between calls.
+ */
+size_t ds_rows_workspace_bytes(int rows, const ds_row_t* table);
+
+/*
+ * (1) Lightning-indexer score (`deepseek_indexer_score_mma_rows_bf16`):
+ *   scores[e * score_stride + j] =
+ *       sum_{h<64} w_index[q_row, h] * max(0, sum_{d<128} q_index[q_row, h, d] * K_e[j, d])
+ * for j < kv_len of entry e; a non-finite score is stored as -inf. Every key
+ * is valid (no causal cut).
+ *   q_index     bf16 [Q, 64, 128]                              (16-B aligned)
+ *   w_index     fp32 [Q, 64]
+ *   scores      fp32, entry e at e * score_stride; score_stride >= max kv_len.
+ *               Elements j >= kv_len of a row are not written.
+ */
+int ds_rows_indexer_score(const ds_row_set_t* set, const ds_bf16* q_index, const float* w_index,
+                          float* scores, size_t score_stride, void* stream);
+
+/*
+ * (2) Deterministic top-k (`deepseek_indexer_topk_block/merge/finalize_rows_i32`):
+ * for each entry e, the first `width` indices j < kv_len ordered best first by
+ * (score descending, then lower index), over the finite scores only; slots past
+ * the number of finite scores hold -1. -0.0 and +0.0 tie.
+ *   scores      fp32, entry e at e * score_stride (as ds_rows_indexer_score).
+ *   indices     int32, entry e writes [index_offset, index_offset + width);
+ *               these ranges must not overlap.
+ *   workspace   at least ds_rows_workspace_bytes(...) bytes.
+ */
+int ds_rows_topk(const ds_row_set_t* set, const float* scores, size_t score_stride,
+                 int32_t* indices, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * (3)+(4) Gather and sink-softmax sparse attention
+ * (`deepseek_sparse_attention_score_rows_bf16` + `..._reduce_rows_bf16`):
+ * for each entry e and head h, over the slots t < width with index
+ * i_t = indices[index_offset + t]:
+ *   i_t == -1 is skipped; i_t < -1 or i_t >= kv_len zeroes every head of e;
+ *   l_t = scale * q_attn[q_row, h, :] . KV_e[i_t, :]
+ *   m = max(sink_h, max_t l_t), den = exp(sink_h - m) + sum_t exp(l_t - m)
+ *   out[q_row, h, :] = bf16( sum_t exp(l_t - m) * KV_e[i_t, :] / den )
+ * The sink has no value row. A non-finite sink, q element or selected KV
+ * element, an overflowed logit or den <= 0 zeroes the head (fail closed).
+ *   q_attn      bf16 [Q, 64, 512]                              (16-B aligned)
+ *   sinks       fp32; head h of entry e at sinks[q_row * sinks_row_stride + h];
+ *               sinks_row_stride 0 shares one [64] vector, else >= 64.
+ *   indices     int32 (as written by ds_rows_topk).
+ *   scale       finite and > 0 (1/sqrt(512) for the DeepSeek shapes).
+ *   out         bf16 [Q, 64, 512]; q_row must be unique across the entries.
+ *   invalid     optional uint32 [Q, 64]: 1 where the head was zeroed, else 0.
+ *   workspace   at least ds_rows_workspace_bytes(...) bytes.
+ */
+int ds_rows_sparse_attn(const ds_row_set_t* set, const ds_bf16* q_attn, const float* sinks,
+                        size_t sinks_row_stride, const int32_t* indices, float scale,
+                        ds_bf16* out, uint32_t* invalid, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/*
+ * The whole decode step: (1) indexer score -> (2) top-`width` -> (3)+(4)
+ * gather and sink attention, on one stream. Scores and candidate lists stay
+ * in the workspace. Arguments as in the stages above; `indices` is optional
+ * (NULL keeps them in the workspace) and, when given, receives the selected
+ * indices at each entry's index_offset (ranges must not overlap).
+ */
+int ds_rows_decode(const ds_row_set_t* set, const ds_bf16* q_index, const float* w_index,
+                   const ds_bf16* q_attn, const float* sinks, size_t sinks_row_stride,
+                   float scale, ds_bf16* out, int32_t* indices, uint32_t* invalid,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Message of the last failed call on this host thread ("" if none). */
+const char* ds_rows_last_error(void);
+
+/* Library version string. */
+const char* ds_rows_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSROWS_H */

@@ -1,0 +1,168 @@
+"""Host-side checks of the C-ABI library: it builds, loads, exports every
+declared symbol and rejects bad arguments before enqueueing anything.
+
+No GPU is needed: every call here fails validation on the host, so no CUDA
+call is reached (the one exception is guarded to run only without a GPU).
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import deepseek_sparse_attention_ragged_gb300 as ds
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsrows.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ds.build()
+    return ds.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(ds_rows_[a-z_0-9]+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("ds_rows_indexer_score", "ds_rows_topk", "ds_rows_sparse_attn", "ds_rows_decode",
+              "ds_rows_workspace_bytes", "ds_rows_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_version(lib):
+    assert "sm_103a" in ds.ds_rows_version()
+
+
+# ---------------------------------------------------------------------------
+# raw C-ABI validation (fake, aligned pointers: validation fails first)
+# ---------------------------------------------------------------------------
+
+FAKE = 0x7F0000000000  # 256-aligned, never dereferenced
+
+
+def _set(rows, keys=True, kv=True, n=None):
+    tab, cnt = ds._table(rows)
+    n = cnt if n is None else n
+    ptrs = (ctypes.c_void_p * max(1, cnt))(*[FAKE + 4096 * i for i in range(cnt)])
+    rs = ds._RowSet(n, ctypes.cast(tab, ctypes.POINTER(ds.Row)),
+                    ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p)) if keys else None,
+                    ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p)) if kv else None)
+    return rs, (tab, ptrs)
+
+
+def _err(lib):
+    return lib.ds_rows_last_error().decode()
+
+
+def _attn(lib, rows, scale=0.04, stride=0, ws_bytes=1 << 30, q=FAKE, kv=True, ws=FAKE):
+    rs, keep = _set(rows, kv=kv)
+    return lib.ds_rows_sparse_attn(ctypes.byref(rs), q, FAKE, stride, FAKE, ctypes.c_float(scale), FAKE, None,
+                                   ws, ws_bytes, None)
+
+
+def test_rows_count(lib):
+    assert lib.ds_rows_workspace_bytes(0, None) == 0
+    rows9 = [(10, 10, 16 * i, i) for i in range(9)]
+    tab, n = ds._table(rows9)
+    assert lib.ds_rows_workspace_bytes(9, tab) == 0
+    assert "rows must be 1..=8" in _err(lib)
+    assert _attn(lib, rows9) == -1
+
+
+@pytest.mark.parametrize("row,msg", [
+    ((0, 1, 0, 0), "nonzero"), ((5, 0, 0, 0), "nonzero"), ((600, 513, 0, 0), "exceeds 512"),
+    ((5, 5, 0xFFFFFFFE, 0), "exceeds u32"),
+])
+def test_bad_row(lib, row, msg):
+    assert _attn(lib, [row]) in (-1, -2)
+    assert msg in _err(lib)
+
+
+def test_scale(lib):
+    for s in (0.0, -1.0, float("inf"), float("nan")):
+        assert _attn(lib, [(8, 8, 0, 0)], scale=s) == -1
+        assert "scale" in _err(lib)
+
+
+def test_duplicate_q_row(lib):
+    assert _attn(lib, [(8, 8, 0, 3), (9, 9, 8, 3)]) == -1
+    assert "used twice" in _err(lib)
+
+
+def test_sinks_stride(lib):
+    assert _attn(lib, [(8, 8, 0, 0)], stride=7) == -1
+    assert "sinks_row_stride" in _err(lib)
+
+
+def test_workspace_checks(lib):
+    rows = [(100, 100, 0, 0)]
+    need = ds.ds_rows_workspace_bytes(rows)
+    assert _attn(lib, rows, ws_bytes=need - 1) == -2
+    assert "workspace holds" in _err(lib)
+    assert _attn(lib, rows, ws=FAKE + 16) == -3
+    assert _attn(lib, rows, ws=0) == -1
+
+
+def test_alignment(lib):
+    assert _attn(lib, [(8, 8, 0, 0)], q=FAKE + 2) == -3
+    assert "16-B aligned" in _err(lib)
+
+
+def test_missing_cache(lib):
+    assert _attn(lib, [(8, 8, 0, 0)], kv=False) == -1
+    assert "kv cache is NULL" in _err(lib)
+
+
+def test_topk_overlapping_outputs(lib):
+    rs, keep = _set([(600, 512, 0, 0), (600, 512, 100, 1)])
+    rc = lib.ds_rows_topk(ctypes.byref(rs), FAKE, 600, FAKE, FAKE, 1 << 30, None)
+    assert rc == -1 and "overlap" in _err(lib)
+
+
+def test_score_stride(lib):
+    rs, keep = _set([(600, 512, 0, 0)])
+    rc = lib.ds_rows_indexer_score(ctypes.byref(rs), FAKE, FAKE, FAKE, 599, None)
+    assert rc == -1 and "score_stride" in _err(lib)
+
+
+def test_decode_checks_everything(lib):
+    rs, keep = _set([(600, 512, 0, 0)], keys=False)
+    rc = lib.ds_rows_decode(ctypes.byref(rs), FAKE, FAKE, FAKE, FAKE, 0, ctypes.c_float(0.04), FAKE, None, None,
+                            FAKE, 1 << 30, None)
+    assert rc == -1 and "indexer keys are NULL" in _err(lib)
+
+
+def test_workspace_bytes_grows_with_rows(lib):
+    a = ds.ds_rows_workspace_bytes([(131072, 512, 0, 0)])
+    b = ds.ds_rows_workspace_bytes([(131072, 512, 512 * i, i) for i in range(8)])
+    assert 0 < a < b
+    assert b % 256 == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="launch-failure path is checked without a device only")
+def test_cuda_failure_is_reported_without_device(lib):
+    """With no CUDA device, a call that passes validation fails at its first
+    CUDA call and reports DS_ECUDA (the launch-error path)."""
+    rows = [(64, 64, 0, 0)]
+    assert _attn(lib, rows, ws_bytes=ds.ds_rows_workspace_bytes(rows)) == -4
+    assert "failed" in _err(lib)
+
+
+def test_python_binding_checks_tensors():
+    with pytest.raises(TypeError):
+        ds._require(torch.zeros(4, dtype=torch.float32), "x", torch.bfloat16, 4)
+    with pytest.raises(ValueError):
+        ds._require(torch.zeros(4, dtype=torch.bfloat16), "x", torch.bfloat16, 4)  # not CUDA

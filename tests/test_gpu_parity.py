@@ -1,0 +1,337 @@
+"""GPU parity: every stage and the fused decode step against the CPU oracle,
+through the C-ABI, on the five benchmark workloads and stand-alone stage inputs.
+"""
+
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import deepseek_sparse_attention_ragged_gb300 as ds
+import oracle
+import workloads
+from workloads.device import bf16_tensor, to_device
+
+from parity import (check_out, check_scores, check_topk, check_topk_consistent, score_bound)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    ds.build()
+    ds.load()
+
+
+@functools.lru_cache(maxsize=None)
+def cfg(i):
+    return workloads.config(i)
+
+
+@functools.lru_cache(maxsize=None)
+def cfg_dev(i):
+    return to_device(cfg(i), "cuda")
+
+
+@functools.lru_cache(maxsize=None)
+def cfg_ref(i):
+    return oracle.decode(cfg(i))
+
+
+def _row_inputs(wl, e):
+    r = wl.rows[e]
+    q = oracle.bf16_to_f64(wl.q_index[r.q_row])
+    w = wl.w_index[r.q_row].astype(np.float64)
+    keys = oracle.bf16_to_f64(wl.keys[e])
+    return q, w, keys
+
+
+def run_decode(dev, rows=None, indices=True, invalid=True, stream=None):
+    rows = dev.rows if rows is None else rows
+    nq = max(r.q_row for r in dev.rows) + 1
+    out = torch.full((nq, 64, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    n_idx = max(r.index_offset + r.width for r in dev.rows)
+    idx = torch.full((n_idx,), -7, dtype=torch.int32, device="cuda") if indices else None
+    inv = torch.full((nq, 64), 7, dtype=torch.int32, device="cuda") if invalid else None
+    keys = [dev.keys[dev.rows.index(r)] for r in rows]
+    kv = [dev.kv[dev.rows.index(r)] for r in rows]
+    ds.ds_rows_decode(rows, dev.q_index, dev.w_index, keys, dev.q_attn, kv, dev.sinks, dev.sinks_row_stride,
+                      dev.scale, out, indices=idx, invalid=inv, stream=stream)
+    torch.cuda.synchronize()
+    return out, idx, inv
+
+
+# ---------------------------------------------------------------------------
+# (1) indexer scores
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("i", [0, 1, 2, 3, 4])
+def test_indexer_scores(i):
+    wl, dev = cfg(i), cfg_dev(i)
+    stride = max(r.kv_len for r in wl.rows)
+    scores = torch.full((wl.num_rows, stride), float("nan"), dtype=torch.float32, device="cuda")
+    ds.ds_rows_indexer_score(dev.rows, dev.q_index, dev.w_index, dev.keys, scores, stride)
+    torch.cuda.synchronize()
+    got = scores.cpu().numpy()
+    for e, r in enumerate(wl.rows):
+        q, w, keys = _row_inputs(wl, e)
+        ref = cfg_ref(i)[e]["scores"]
+        check_scores(got[e, : r.kv_len], ref, score_bound(q, w, keys), exact=wl.integer_valued,
+                     what=f"cfg{i} row{e}")
+        assert np.isnan(got[e, r.kv_len:]).all(), "wrote past kv_len"
+
+
+def test_indexer_identical_keys_identical_scores():
+    """Exact duplicate keys at different tile positions give bitwise equal scores."""
+    wl = cfg(4)
+    dev = cfg_dev(4)
+    e = 7  # kv_len 262144, 64 prototypes
+    r = wl.rows[e]
+    scores = torch.empty((1, r.kv_len), dtype=torch.float32, device="cuda")
+    one = [workloads.Row(r.kv_len, r.width, 0, r.q_row)]
+    ds.ds_rows_indexer_score(one, dev.q_index, dev.w_index, [dev.keys[e]], scores, r.kv_len)
+    got = scores.cpu().numpy()[0]
+    keys = wl.keys[e]
+    _, first, inverse = np.unique(keys, axis=0, return_index=True, return_inverse=True)
+    np.testing.assert_array_equal(got, got[first][inverse.ravel()])
+
+
+# ---------------------------------------------------------------------------
+# (2) top-k on generated scores (bit-exact: fp32 inputs, exact comparisons)
+# ---------------------------------------------------------------------------
+
+TOPK_CASES = {
+    "normal": dict(lens=[1, 17, 511, 512, 513, 8191, 8193, 40000], kw={}),
+    "ties": dict(lens=[300, 1000, 9000, 70000], kw=dict(ties=True)),
+    "nonfinite": dict(lens=[20, 600, 9000, 33000], kw=dict(nonfinite=True)),
+    "zeros": dict(lens=[513, 5000, 16385], kw=dict(signed_zeros=True, ties=True)),
+    "long": dict(lens=[262144, 131072, 3], kw={}),
+}
+
+
+@pytest.mark.parametrize("case", sorted(TOPK_CASES))
+def test_topk_exact(case):
+    spec = TOPK_CASES[case]
+    lens = spec["lens"]
+    rows = [workloads.Row(L, min(512, L), 512 * e, e) for e, L in enumerate(lens)]
+    rows_s = workloads.random_scores(31 + len(case), lens, **spec["kw"])
+    stride = max(lens)
+    host = np.full((len(lens), stride), np.nan, np.float32)
+    for e, s in enumerate(rows_s):
+        host[e, : len(s)] = s
+    scores = torch.from_numpy(host).cuda()
+    idx = torch.full((512 * len(lens),), -7, dtype=torch.int32, device="cuda")
+    ws = ds.workspace(rows)
+    ds.ds_rows_topk(rows, scores, stride, idx, ws)
+    torch.cuda.synchronize()
+    got = idx.cpu().numpy()
+    for e, r in enumerate(rows):
+        ref = oracle.topk(rows_s[e].astype(np.float64), r.width)
+        np.testing.assert_array_equal(got[r.index_offset: r.index_offset + r.width], ref, err_msg=f"row {e}")
+
+
+def test_topk_equal_scores_slow_path():
+    """All-equal scores on a row longer than the candidate list: the threshold bin
+    overflows, the row is refined from its full score array, and the lowest
+    indices win."""
+    lens = [40000, 70000]
+    rows = [workloads.Row(L, 512, 512 * e, e) for e, L in enumerate(lens)]
+    host = np.full((2, 70000), 1.5, np.float32)
+    host[1, 12345] = 2.0
+    host[1, 50000:50010] = np.nan
+    scores = torch.from_numpy(host).cuda()
+    idx = torch.full((1024,), -7, dtype=torch.int32, device="cuda")
+    ds.ds_rows_topk(rows, scores, 70000, idx, ds.workspace(rows))
+    got = idx.cpu().numpy()
+    np.testing.assert_array_equal(got[:512], np.arange(512))
+    np.testing.assert_array_equal(got[512:], oracle.topk(host[1].astype(np.float64), 512))
+
+
+def test_topk_fewer_finite_than_width():
+    L = 700
+    s = np.full(L, -np.inf, np.float32)
+    s[[5, 600, 33]] = [1.0, 3.0, 1.0]
+    rows = [workloads.Row(L, 512, 0, 0)]
+    idx = torch.full((512,), -7, dtype=torch.int32, device="cuda")
+    ds.ds_rows_topk(rows, torch.from_numpy(s).cuda(), L, idx, ds.workspace(rows))
+    got = idx.cpu().numpy()
+    assert got[:3].tolist() == [600, 5, 33]
+    assert np.all(got[3:] == -1)
+
+
+# ---------------------------------------------------------------------------
+# (3)+(4) attention on generated indices
+# ---------------------------------------------------------------------------
+
+ATTN_CASES = {
+    "unique": dict(sentinel_frac=0.0),
+    "sentinels": dict(sentinel_frac=0.3),
+    "duplicates": dict(unique=False),
+    "bad_rows": dict(sentinel_frac=0.1, bad_rows=(1,)),
+}
+
+
+@pytest.mark.parametrize("case", sorted(ATTN_CASES))
+def test_sparse_attn(case):
+    wl = workloads.make_workload("attn", 41, [600, 5000, 33, 1], per_row_sinks=True)
+    rows = [workloads.Row(r.kv_len, w, r.index_offset, r.q_row) for r, w in zip(wl.rows, [512, 300, 33, 1])]
+    dev = to_device(wl)
+    idx_h = workloads.random_indices(43, rows, **ATTN_CASES[case])
+    idx = torch.from_numpy(idx_h).cuda()
+    out = torch.full((4, 64, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    inv = torch.full((4, 64), 7, dtype=torch.int32, device="cuda")
+    ds.ds_rows_sparse_attn(rows, dev.q_attn, dev.sinks, 64, idx, dev.scale, out, dev.kv, invalid=inv)
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy()
+    ginv = inv.cpu().numpy()
+    for e, r in enumerate(rows):
+        sel = idx_h[r.index_offset: r.index_offset + r.width]
+        ref, rinv = oracle.sparse_attention_rows(oracle.bf16_to_f64(wl.q_attn[r.q_row]),
+                                                 oracle._LazyRows(wl.kv[e], r.kv_len), sel,
+                                                 wl.sinks[r.q_row], wl.scale)
+        np.testing.assert_array_equal(ginv[r.q_row], rinv.astype(np.int32), err_msg=f"row {e} flags")
+        check_out(got[r.q_row], ref, what=f"{case} row {e}")
+
+
+def test_sparse_attn_shared_sinks_and_dense_closed_form():
+    """width == kv_len with every row selected and sink -3e38 (exp underflows):
+    dense softmax attention; sinks shared (stride 0)."""
+    L = 96
+    wl = workloads.make_workload("dense", 44, [L], per_row_sinks=False)
+    dev = to_device(wl)
+    rows = [workloads.Row(L, L, 0, 0)]
+    idx = torch.arange(L, dtype=torch.int32, device="cuda")
+    sinks = torch.full((64,), -3.0e38, dtype=torch.float32, device="cuda")
+    out = torch.empty((1, 64, 512), dtype=torch.bfloat16, device="cuda")
+    ds.ds_rows_sparse_attn(rows, dev.q_attn, sinks, 0, idx, dev.scale, out, dev.kv)
+    q = oracle.bf16_to_f64(wl.q_attn[0])
+    kv = oracle.bf16_to_f64(wl.kv[0])
+    logits = wl.scale * q @ kv.T
+    p = np.exp(logits - logits.max(axis=1, keepdims=True))
+    dense = (p / p.sum(axis=1, keepdims=True)) @ kv
+    check_out(out.float().cpu().numpy()[0], dense, what="dense")
+
+
+# ---------------------------------------------------------------------------
+# the fused decode step
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("i", [0, 1, 2, 3, 4])
+def test_decode(i):
+    wl, dev = cfg(i), cfg_dev(i)
+    out, idx, inv = run_decode(dev)
+    got = out.float().cpu().numpy()
+    gidx = idx.cpu().numpy()
+    ginv = inv.cpu().numpy()
+    swaps = 0
+    for e, r in enumerate(wl.rows):
+        ref = cfg_ref(i)[e]
+        q, w, keys = _row_inputs(wl, e)
+        sel = gidx[r.index_offset: r.index_offset + r.width]
+        swaps += check_topk(sel, ref["indices"], ref["scores"], r.width, exact=wl.integer_valued,
+                            T=score_bound(q, w, keys), what=f"cfg{i} row{e}")
+        if set(sel.tolist()) == set(ref["indices"].tolist()):
+            expect, rinv = ref["out"], ref["invalid"]
+        else:
+            # A near-tie swap (allowed above): the attention of the selected set,
+            # already validated against the oracle's scores, is the expected value.
+            expect, rinv = oracle.sparse_attention_rows(oracle.bf16_to_f64(wl.q_attn[r.q_row]),
+                                                        oracle._LazyRows(wl.kv[e], r.kv_len), sel,
+                                                        wl.row_sinks(e), wl.scale)
+        np.testing.assert_array_equal(ginv[r.q_row], rinv.astype(np.int32))
+        check_out(got[r.q_row], expect, what=f"cfg{i} row{e}")
+    print(f"cfg{i}: near-tie swaps {swaps}")
+
+
+@pytest.mark.parametrize("i", [0, 1, 2, 3, 4])
+def test_joint_equals_single_row(i):
+    """Row r of a joint launch is bitwise equal to a launch of row r alone."""
+    dev = cfg_dev(i)
+    out, idx, _ = run_decode(dev)
+    for e, r in enumerate(dev.rows):
+        o1, i1, _ = run_decode(dev, rows=[r])
+        assert torch.equal(o1[r.q_row].view(torch.int16), out[r.q_row].view(torch.int16)), f"row {e} out"
+        assert torch.equal(i1[r.index_offset: r.index_offset + r.width],
+                           idx[r.index_offset: r.index_offset + r.width]), f"row {e} indices"
+
+
+def test_decode_stages_agree():
+    """decode == indexer_score -> topk -> sparse_attn, bitwise, and the top-k is
+    exactly the top-width of the GPU's own scores."""
+    wl, dev = cfg(2), cfg_dev(2)
+    out, idx, _ = run_decode(dev)
+    stride = max(r.kv_len for r in wl.rows)
+    scores = torch.empty((wl.num_rows, stride), dtype=torch.float32, device="cuda")
+    ds.ds_rows_indexer_score(dev.rows, dev.q_index, dev.w_index, dev.keys, scores, stride)
+    idx2 = torch.full_like(idx, -7)
+    ds.ds_rows_topk(dev.rows, scores, stride, idx2, ds.workspace(dev.rows))
+    out2 = torch.full_like(out, float("nan"))
+    ds.ds_rows_sparse_attn(dev.rows, dev.q_attn, dev.sinks, dev.sinks_row_stride, idx2, dev.scale, out2, dev.kv)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx2)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    s = scores.cpu().numpy()
+    for e, r in enumerate(wl.rows):
+        check_topk_consistent(idx2.cpu().numpy()[r.index_offset: r.index_offset + r.width], s[e, : r.kv_len],
+                              r.width)
+
+
+def test_decode_repeatable_and_on_side_stream():
+    dev = cfg_dev(0)
+    a, ia, _ = run_decode(dev)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        b, ib, _ = run_decode(dev, stream=s)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(ia, ib)
+
+
+def test_decode_without_optional_outputs():
+    dev = cfg_dev(0)
+    a, ia, _ = run_decode(dev)
+    b, _, _ = run_decode(dev, indices=False, invalid=False)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# ---------------------------------------------------------------------------
+# fail-closed data
+# ---------------------------------------------------------------------------
+
+def test_fail_closed_decode():
+    wl = workloads.make_workload("fail", 51, [700, 900, 300], per_row_sinks=True)
+    wl.q_attn[0, 5, 17] = 0x7FC0                       # NaN in row 0, head 5
+    wl.sinks[1, 9] = np.inf                            # row 1 head 9 sink
+    dev = to_device(wl)
+    out, idx, inv = run_decode(dev)
+    ginv = inv.cpu().numpy()
+    got = out.float().cpu().numpy()
+    ref = oracle.decode(wl)
+    for e, r in enumerate(wl.rows):
+        np.testing.assert_array_equal(ginv[r.q_row], ref[e]["invalid"].astype(np.int32))
+        check_out(got[r.q_row], ref[e]["out"], what=f"row {e}")
+    assert ginv[0, 5] == 1 and np.all(got[0, 5] == 0)
+    assert ginv[1, 9] == 1 and np.all(got[1, 9] == 0)
+    assert ginv[2].sum() == 0
+
+
+def test_fail_closed_kv_and_keys():
+    """A non-finite KV element on a selected row zeroes every head of the row;
+    a non-finite indexer key is never selected."""
+    wl = workloads.make_workload("fail2", 52, [800, 800], per_row_sinks=True)
+    ref0 = oracle.decode(wl)
+    j = int(ref0[0]["indices"][3])
+    wl.kv[0][j, 100] = 0x7F80                          # +Inf
+    best = int(ref0[1]["indices"][0])
+    wl.keys[1][best, 7] = 0x7FC0                       # NaN key: excluded from top-k
+    dev = to_device(wl)
+    out, idx, inv = run_decode(dev)
+    ref = oracle.decode(wl)
+    assert best not in ref[1]["indices"].tolist()
+    gidx = idx.cpu().numpy()
+    assert best not in gidx[512:1024].tolist()
+    assert np.all(inv.cpu().numpy()[0] == 1)
+    assert np.all(out[0].float().cpu().numpy() == 0)
+    check_out(out[1].float().cpu().numpy(), ref[1]["out"], what="row 1")
