@@ -175,7 +175,7 @@ uint32_t max_q_row(const ds_row_set_t* set) {
 
 // ---- stage launchers ---------------------------------------------------------------
 int run_indexer(const ds_row_set_t* set, const ds_bf16* q_index, const float* w_index, float* scores,
-                uint64_t stride, uint32_t* hist, uint32_t* status, cudaStream_t stream) {
+                uint64_t stride, uint32_t* hist, uint32_t* status, cudaStream_t stream, bool pdl) {
     int rc = get_encoder();
     if (rc) return rc;
     IndexerParams p;  // ~1.3 KB with the tensor maps; built per call on the host
@@ -202,7 +202,7 @@ int run_indexer(const ds_row_set_t* set, const ds_bf16* q_index, const float* w_
     p.total_tiles = tiles;
     const int sms = num_sms();
     if (sms <= 0) return fail(DS_ECUDA, "no CUDA device");
-    cudaError_t err = launch_indexer(p, sms, stream);
+    cudaError_t err = launch_indexer(p, sms, stream, pdl);
     return err == cudaSuccess ? DS_OK : cuda_fail(err, "indexer launch");
 }
 
@@ -230,10 +230,10 @@ int run_topk(const ds_row_set_t* set, const float* scores, uint64_t stride, int3
     p.total_chunks = chunks;
     cudaError_t err = cudaSuccess;
     if (with_hist) {
-        err = launch_topk_hist(p, stream);
+        err = launch_topk_hist(p, stream, true);
         if (err != cudaSuccess) return cuda_fail(err, "top-k histogram launch");
     }
-    err = launch_topk_select(p, stream);
+    err = launch_topk_select(p, stream, true);
     return err == cudaSuccess ? DS_OK : cuda_fail(err, "top-k select launch");
 }
 
@@ -265,7 +265,7 @@ int run_attention(const ds_row_set_t* set, const ds_bf16* q_attn, const float* s
     p.scale = scale;
     p.rows = (uint32_t)set->rows;
     p.total_chunks = chunks;
-    cudaError_t err = launch_attention(p, stream);
+    cudaError_t err = launch_attention(p, stream, true);
     return err == cudaSuccess ? DS_OK : cuda_fail(err, "attention launch");
 }
 
@@ -304,7 +304,7 @@ int ds_rows_indexer_score(const ds_row_set_t* set, const ds_bf16* q_index, const
         if (score_stride < set->table[e].kv_len)
             return fail(DS_EINVAL, "score_stride %zu is shorter than row %d (kv_len %u)", score_stride, e,
                         set->table[e].kv_len);
-    return run_indexer(set, q_index, w_index, scores, score_stride, nullptr, nullptr, (cudaStream_t)stream);
+    return run_indexer(set, q_index, w_index, scores, score_stride, nullptr, nullptr, (cudaStream_t)stream, false);
 }
 
 int ds_rows_topk(const ds_row_set_t* set, const float* scores, size_t score_stride, int32_t* indices,
@@ -321,7 +321,7 @@ int ds_rows_topk(const ds_row_set_t* set, const float* scores, size_t score_stri
     if (rc) return rc;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t err = cudaMemsetAsync(ws, 0, L.ctl_end, s);
+    cudaError_t err = launch_clear(reinterpret_cast<uint32_t*>(ws), (uint32_t)(L.ctl_end / 4), s);
     if (err != cudaSuccess) return cuda_fail(err, "workspace clear");
     uint32_t off[DS_ROWS_MAX];
     for (int e = 0; e < set->rows; ++e) off[e] = set->table[e].index_offset;
@@ -341,7 +341,7 @@ int ds_rows_sparse_attn(const ds_row_set_t* set, const ds_bf16* q_attn, const fl
     if (rc) return rc;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t err = cudaMemsetAsync(ws, 0, L.ctl_end, s);
+    cudaError_t err = launch_clear(reinterpret_cast<uint32_t*>(ws), (uint32_t)(L.ctl_end / 4), s);
     if (err != cudaSuccess) return cuda_fail(err, "workspace clear");
     uint32_t off[DS_ROWS_MAX];
     for (int e = 0; e < set->rows; ++e) off[e] = set->table[e].index_offset;
@@ -362,12 +362,12 @@ int ds_rows_decode(const ds_row_set_t* set, const ds_bf16* q_index, const float*
     if (rc) return rc;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t err = cudaMemsetAsync(ws, 0, L.ctl_end, s);
+    cudaError_t err = launch_clear(reinterpret_cast<uint32_t*>(ws), (uint32_t)(L.ctl_end / 4), s);
     if (err != cudaSuccess) return cuda_fail(err, "workspace clear");
     float* scores = reinterpret_cast<float*>(ws + L.scores);
     uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
     uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
-    rc = run_indexer(set, q_index, w_index, scores, L.score_stride, hist, status, s);
+    rc = run_indexer(set, q_index, w_index, scores, L.score_stride, hist, status, s, true);
     if (rc) return rc;
     int32_t* idx = indices;
     uint32_t off[DS_ROWS_MAX];

@@ -108,12 +108,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_kernel(const AttnPar
     const int L = (int)p.kv_len[e];
     const __nv_bfloat16* kv = p.kv[e];
 
+    pdl_trigger();
+    // The query is an input of the call: fetch it while the previous kernel finishes.
+    const __nv_bfloat16* q = p.q + (size_t)p.q_row[e] * kHeads * kDim;
+    for (int k = t; k < kHeads * (kDim / 8); k += kThreads) {
+        const int row = k >> 6, col = (k & 63) * 8;
+        cp_async16(q_s + row * kQStride + col, q + (size_t)row * kDim + col);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    pdl_wait();  // the indices come from the previous kernel
+
     // Selected indices of this chunk: -1 for sentinels, bad indices and slots past the width.
     if (t < kSlots) {
         const uint32_t slot = c * kSlots + t;
         int i = -1;
         if (slot < W) {
-            const int v = p.indices[p.index_offset[e] + slot];
+            const int v = __ldcg(p.indices + p.index_offset[e] + slot);
             if (v < -1 || v >= L) atomicOr(&p.flags[kRowsMax * kHeads + e], 1u);
             else i = v;
         }
@@ -121,12 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_kernel(const AttnPar
     }
     __syncthreads();
 
-    // Gather: the row's query (64 x 1 KiB) and the chunk's selected KV rows.
-    const __nv_bfloat16* q = p.q + (size_t)p.q_row[e] * kHeads * kDim;
-    for (int k = t; k < kHeads * (kDim / 8); k += kThreads) {
-        const int row = k >> 6, col = (k & 63) * 8;
-        cp_async16(q_s + row * kQStride + col, q + (size_t)row * kDim + col);
-    }
+    // Gather the chunk's selected KV rows (1 KiB each, once for all heads).
     for (int k = t; k < kSlots * (kDim / 8); k += kThreads) {
         const int row = k >> 6, col = (k & 63) * 8;
         const int i = idx_s[row];
@@ -234,7 +239,9 @@ constexpr int kCombineFeatures = 16;
 constexpr int kCombineBlocks = kDim / kCombineFeatures;  // 32 per row
 
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
-    __shared__ float fac[kHeads][kAttnChunksMax];
+    __shared__ float mc_s[kAttnChunksMax][kHeads];
+    __shared__ float lc_s[kAttnChunksMax][kHeads];
+    __shared__ float fac[kHeads][kAttnChunksMax + 1];
     __shared__ float inv_den[kHeads];
     __shared__ uint32_t bad[kHeads];
     const int e = blockIdx.x / kCombineBlocks;
@@ -243,43 +250,58 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
     const uint32_t W = p.width[e];
     const int nchunks = (int)((W + kSlots - 1) / kSlots);
     const float* part0 = p.part + (size_t)p.chunk_begin[e] * kPartFloats;
-    const bool row_bad = p.flags[kRowsMax * kHeads + e] != 0;
+    pdl_trigger();
+    pdl_wait();  // partials and flags come from the partial kernel
 
+    // Issue every load of this thread before using any.
+    const int h = t >> 2;
+    const int f = fb * kCombineFeatures + (t & 3) * 4;
+    float4 v[kAttnChunksMax];
+#pragma unroll
+    for (int c = 0; c < kAttnChunksMax; ++c)
+        if (c < nchunks)
+            v[c] = __ldcg(reinterpret_cast<const float4*>(part0 + (size_t)c * kPartFloats + 2 * kHeads +
+                                                          (size_t)h * kDim + f));
+    for (int i = t; i < nchunks * kHeads; i += 256) {
+        const int c = i / kHeads, hh = i % kHeads;
+        mc_s[c][hh] = __ldcg(part0 + (size_t)c * kPartFloats + hh);
+        lc_s[c][hh] = __ldcg(part0 + (size_t)c * kPartFloats + kHeads + hh);
+    }
+    __syncthreads();
     if (t < kHeads) {
-        const int h = t;
-        const float sink = p.sinks[(size_t)p.q_row[e] * p.sinks_row_stride + h];
-        uint32_t inv = row_bad || p.flags[e * kHeads + h] != 0 || !finite_f(sink);
+        const bool row_bad = __ldcg(p.flags + kRowsMax * kHeads + e) != 0;
+        const float sink = p.sinks[(size_t)p.q_row[e] * p.sinks_row_stride + t];
+        uint32_t inv = row_bad || __ldcg(p.flags + e * kHeads + t) != 0 || !finite_f(sink);
         float m = sink;
-        for (int c = 0; c < nchunks; ++c) m = fmaxf(m, part0[(size_t)c * kPartFloats + h]);
+        for (int c = 0; c < nchunks; ++c) m = fmaxf(m, mc_s[c][t]);
         float den = finite_f(sink) ? expf(sink - m) : 0.0f;
         for (int c = 0; c < nchunks; ++c) {
-            const float mc = part0[(size_t)c * kPartFloats + h];
-            const float f = mc == -INFINITY ? 0.0f : expf(mc - m);
-            fac[h][c] = f;
-            den += part0[(size_t)c * kPartFloats + kHeads + h] * f;
+            const float mc = mc_s[c][t];
+            const float fc = mc == -INFINITY ? 0.0f : expf(mc - m);
+            fac[t][c] = fc;
+            den = fmaf(lc_s[c][t], fc, den);
         }
         if (!finite_f(den) || !(den > 0.0f) || !finite_f(m)) inv = 1;
-        inv_den[h] = 1.0f / den;
-        bad[h] = inv;
-        if (p.invalid && fb == 0) p.invalid[(size_t)p.q_row[e] * kHeads + h] = inv;
+        inv_den[t] = 1.0f / den;
+        bad[t] = inv;
+        if (p.invalid && fb == 0) p.invalid[(size_t)p.q_row[e] * kHeads + t] = inv;
     }
     __syncthreads();
 
-    const int h = t >> 2;
-    const int f = fb * kCombineFeatures + (t & 3) * 4;
     float4 acc = make_float4(0, 0, 0, 0);
-    for (int c = 0; c < nchunks; ++c) {
-        const float4 v =
-            *reinterpret_cast<const float4*>(part0 + (size_t)c * kPartFloats + 2 * kHeads + (size_t)h * kDim + f);
-        const float w = fac[h][c];
-        acc.x = fmaf(v.x, w, acc.x);
-        acc.y = fmaf(v.y, w, acc.y);
-        acc.z = fmaf(v.z, w, acc.z);
-        acc.w = fmaf(v.w, w, acc.w);
+#pragma unroll
+    for (int c = 0; c < kAttnChunksMax; ++c) {
+        if (c < nchunks) {
+            const float w = fac[h][c];
+            acc.x = fmaf(v[c].x, w, acc.x);
+            acc.y = fmaf(v[c].y, w, acc.y);
+            acc.z = fmaf(v[c].z, w, acc.z);
+            acc.w = fmaf(v[c].w, w, acc.w);
+        }
     }
-    const float s = inv_den[h];
+    const float sc = inv_den[h];
     const bool zero = bad[h] != 0;
-    float r[4] = {acc.x * s, acc.y * s, acc.z * s, acc.w * s};
+    const float r[4] = {acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc};
     __nv_bfloat16 o[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) o[i] = __float2bfloat16_rn(!zero && finite_f(r[i]) ? r[i] : 0.0f);
@@ -287,7 +309,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
     *reinterpret_cast<uint2*>(out) = *reinterpret_cast<const uint2*>(o);
 }
 
-cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream) {
+cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream, bool pdl) {
     static bool configured = false;
     if (!configured) {
         cudaError_t err = cudaFuncSetAttribute(attn_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -296,11 +318,10 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream) {
         configured = true;
     }
     if (p.total_chunks == 0) return cudaSuccess;
-    attn_partial_kernel<<<p.total_chunks, kThreads, kSmemBytes, stream>>>(p);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_kernel(attn_partial_kernel, dim3(p.total_chunks), dim3(kThreads), kSmemBytes, stream,
+                                    pdl, p);
     if (err != cudaSuccess) return err;
-    attn_combine_kernel<<<p.rows * kCombineBlocks, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(attn_combine_kernel, dim3(p.rows * kCombineBlocks), dim3(256), 0, stream, true, p);
 }
 
 }  // namespace dsrows

@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_score_kernel(const __grid
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = bar->tmem_base;
+    pdl_trigger();
 
     if (warp == 0) {
         // ---- TMA producer ----------------------------------------------------
@@ -214,6 +215,9 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_score_kernel(const __grid
         const int quarter = warp & 3;          // TMEM lanes [32*quarter, 32*quarter+32)
         const int ep_tid = threadIdx.x - 64;   // 0..127
         const bool want_hist = p.hist != nullptr;
+        // The histogram may still be being cleared by the previous kernel (PDL):
+        // the producer and MMA warps start streaming, the epilogue waits here.
+        pdl_wait();
         int cur = -1;
         uint32_t it = 0;
         for (uint32_t g = g_begin; g < g_end; ++g, ++it) {
@@ -276,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_score_kernel(const __grid
 
 size_t indexer_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_indexer(const IndexerParams& p, int num_sms, cudaStream_t stream) {
+cudaError_t launch_indexer(const IndexerParams& p, int num_sms, cudaStream_t stream, bool pdl) {
     static bool configured = false;
     if (!configured) {
         cudaError_t err = cudaFuncSetAttribute(indexer_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -286,8 +290,7 @@ cudaError_t launch_indexer(const IndexerParams& p, int num_sms, cudaStream_t str
     }
     if (p.total_tiles == 0) return cudaSuccess;
     const uint32_t grid = p.total_tiles < (uint32_t)num_sms ? p.total_tiles : (uint32_t)num_sms;
-    indexer_score_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(indexer_score_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, pdl, p);
 }
 
 uint32_t indexer_tile_keys() { return kTileKeys; }

@@ -67,12 +67,16 @@ struct AttnParams {
 
 size_t indexer_smem_bytes();
 uint32_t indexer_tile_keys();
-cudaError_t launch_indexer(const IndexerParams& p, int num_sms, cudaStream_t stream);
+cudaError_t launch_indexer(const IndexerParams& p, int num_sms, cudaStream_t stream, bool pdl);
 
 uint32_t topk_chunk();  // scores per histogram / collection CTA
-cudaError_t launch_topk_hist(const TopkParams& p, cudaStream_t stream);
-cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t stream);
+cudaError_t launch_topk_hist(const TopkParams& p, cudaStream_t stream, bool pdl);
+cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t stream, bool pdl);
 
-cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
+// Zero `words` 32-bit words (the workspace control region); an ordinary launch.
+cudaError_t launch_clear(uint32_t* p, uint32_t words, cudaStream_t stream);
+
+// Partial kernel (PDL on the previous kernel when `pdl`), then the combine kernel (PDL).
+cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream, bool pdl);
 
 }  // namespace dsrows

@@ -18,8 +18,8 @@
 //   3. the last CTA of a row to finish (an atomic arrival counter; nothing
 //      waits) refines the threshold digit by digit (11/11/10 key bits, then
 //      the index bits, stopping as soon as a bin is taken whole), keeps the
-//      `width` winners and ranks them by counting (rank = number of larger
-//      composites), then writes them best first.
+//      `width` winners, sorts them with a 512-wide bitonic network (warp
+//      shuffles for partners closer than 32) and writes them best first.
 // A row whose threshold bin alone overflows the candidate list falls back to
 // the same refinement over the row's full score array.
 
@@ -103,13 +103,24 @@ __device__ BinPick pick_bin(const uint32_t* h, uint32_t need, uint32_t* scratch)
     return r;
 }
 
-// Element sources for the refinement: the candidate list, or a full score row.
+
+// Element sources for the refinement: candidates in shared or global memory, or a full score row.
+struct SmemCandSource {
+    const uint64_t* c;  // composites
+    uint32_t n;
+    __device__ __forceinline__ uint32_t size() const { return n; }
+    __device__ __forceinline__ bool get(uint32_t i, uint64_t& v) const {
+        v = c[i];
+        return true;
+    }
+};
+
 struct CandSource {
-    const uint64_t* cand;
+    const uint64_t* cand;  // key << 32 | index
     uint32_t n;
     __device__ __forceinline__ uint32_t size() const { return n; }
     __device__ __forceinline__ bool get(uint32_t i, uint64_t& c) const {
-        const uint64_t v = cand[i];
+        const uint64_t v = __ldcg(cand + i);
         c = composite((uint32_t)(v >> 32), (uint32_t)v);
         return true;
     }
@@ -120,26 +131,54 @@ struct RowSource {
     uint32_t n;
     __device__ __forceinline__ uint32_t size() const { return n; }
     __device__ __forceinline__ bool get(uint32_t i, uint64_t& c) const {
-        const float x = s[i];
+        const float x = __ldcg(s + i);
         if (!finite_f(x)) return false;
         c = composite(score_key(x), i);
         return true;
     }
 };
 
+constexpr int kSmemCand = 4096;  // candidates the finishing CTA stages in shared memory
+
 struct FinishSmem {
     uint32_t h[kHistBins];
     uint32_t scratch[32];
+    uint64_t cand[kSmemCand];
     uint64_t sel[kTopK];
     uint32_t nsel;
 };
 
-// Refine from the level-0 pick, select the winners, rank and write them.
+// Sort the 512 composites of sm.sel in descending order; thread t ends with element t.
+// Bitonic network: partners closer than 32 exchange by warp shuffle, the rest through shared memory.
+__device__ __forceinline__ uint64_t bitonic_desc_512(FinishSmem& sm) {
+    const int t = threadIdx.x;
+    uint64_t x = sm.sel[t];
+    for (int k = 2; k <= kTopK; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            uint64_t y;
+            if (j >= 32) {
+                __syncthreads();
+                sm.sel[t] = x;
+                __syncthreads();
+                y = sm.sel[t ^ j];
+            } else {
+                y = __shfl_xor_sync(kFull, x, j);
+            }
+            const bool desc = (t & k) == 0;
+            const bool lower = (t & j) == 0;
+            const uint64_t hi = x > y ? x : y, lo = x > y ? y : x;
+            x = (lower == desc) ? hi : lo;
+        }
+    }
+    return x;
+}
+
+// Refine from the level-0 pick, select the winners, sort and write them best first.
 template <class Src>
 __device__ void finish_row(const Src& src, const BinPick& l0, uint32_t width, int32_t* out, FinishSmem& sm,
                            uint32_t* status) {
-    const int t = threadIdx.x;
-    bool take_all = l0.total <= width;
+    const int t = threadIdx.x, lane = t & 31;
+    const bool take_all = l0.total <= width;
     int level = 0;
     uint64_t prefix = (uint64_t)(l0.bin < 0 ? 0 : l0.bin);
     uint32_t need = take_all ? 0 : width - l0.gt;
@@ -159,7 +198,6 @@ __device__ void finish_row(const Src& src, const BinPick& l0, uint32_t width, in
         const BinPick pk = pick_bin(sm.h, need, sm.scratch);
         if (pk.bin < 0) {  // inconsistent counts: keep what is certain
             if (t == 0) atomicOr(status, kStatusCandOverflow);
-            done = true;
             break;
         }
         need -= pk.gt;
@@ -170,27 +208,27 @@ __device__ void finish_row(const Src& src, const BinPick& l0, uint32_t width, in
     const int shift = kLevels[level].shift;
 
     if (t == 0) sm.nsel = 0;
+    sm.sel[t] = 0;  // below every finite element's composite
     __syncthreads();
     const uint32_t n = src.size();
-    for (uint32_t i = t; i < n; i += kThreads) {
-        uint64_t c;
-        if (!src.get(i, c)) continue;
-        if (take_all || (c >> shift) >= prefix) {
-            const uint32_t pos = atomicAdd(&sm.nsel, 1u);
-            if (pos < (uint32_t)kTopK) sm.sel[pos] = c;
+    for (uint32_t base = 0; base < n; base += kThreads) {
+        const uint32_t i = base + t;
+        uint64_t c = 0;
+        const bool take = i < n && src.get(i, c) && (take_all || (c >> shift) >= prefix);
+        const uint32_t m = __ballot_sync(kFull, take);
+        if (m) {
+            uint32_t pos = 0;
+            if (lane == 0) pos = atomicAdd(&sm.nsel, (uint32_t)__popc(m));
+            pos = __shfl_sync(kFull, pos, 0) + __popc(m & ((1u << lane) - 1u));
+            if (take && pos < (uint32_t)kTopK) sm.sel[pos] = c;
         }
     }
     __syncthreads();
-    const uint32_t nsel = sm.nsel < width ? sm.nsel : width;
-    if (sm.nsel > width && t == 0) atomicOr(status, kStatusCandOverflow);
-    // Rank by counting: rank = number of larger composites (all distinct).
-    for (uint32_t k = t; k < nsel; k += kThreads) {
-        const uint64_t c = sm.sel[k];
-        uint32_t rank = 0;
-        for (uint32_t u = 0; u < nsel; ++u) rank += sm.sel[u] > c ? 1u : 0u;
-        if (rank < width) out[rank] = (int32_t)(~(uint32_t)c);
-    }
-    for (uint32_t k = nsel + t; k < width; k += kThreads) out[k] = -1;
+    const uint32_t got = sm.nsel;
+    const uint32_t nsel = got < width ? got : width;
+    if (got > width && t == 0) atomicOr(status, kStatusCandOverflow);
+    const uint64_t x = bitonic_desc_512(sm);
+    if ((uint32_t)t < width) out[t] = (uint32_t)t < nsel ? (int32_t)(~(uint32_t)x) : -1;
 }
 
 }  // namespace
@@ -198,6 +236,8 @@ __device__ void finish_row(const Src& src, const BinPick& l0, uint32_t width, in
 // Level-0 histogram of one chunk of a row's scores (stand-alone top-k).
 __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const TopkParams p) {
     __shared__ uint32_t h[kHistBins];
+    pdl_trigger();
+    pdl_wait();  // the histogram is being cleared by the previous kernel
     const int e = entry_of_chunk(p, blockIdx.x);
     const uint32_t c = blockIdx.x - p.chunk_begin[e];
     const uint32_t L = p.kv_len[e];
@@ -206,10 +246,15 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const TopkParams p)
     for (int i = threadIdx.x; i < kHistBins; i += kThreads) h[i] = 0;
     __syncthreads();
     const float* s = p.scores + (size_t)e * p.score_stride;
-    for (uint32_t j = begin + threadIdx.x; j < end; j += kThreads) {
-        const float x = s[j];
-        if (finite_f(x)) atomicAdd(&h[score_key(x) >> 21], 1u);
+    float v[kChunk / kThreads];
+#pragma unroll
+    for (int i = 0; i < kChunk / kThreads; ++i) {
+        const uint32_t j = begin + threadIdx.x + i * kThreads;
+        v[i] = j < end ? s[j] : __int_as_float(0x7FC00000);
     }
+#pragma unroll
+    for (int i = 0; i < kChunk / kThreads; ++i)
+        if (finite_f(v[i])) atomicAdd(&h[score_key(v[i]) >> 21], 1u);
     __syncthreads();
     for (int i = threadIdx.x; i < kHistBins; i += kThreads)
         if (h[i]) atomicAdd(&p.hist[(size_t)e * kHistBins + i], h[i]);
@@ -229,8 +274,27 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const TopkParams 
     uint64_t* cand = p.cand + (size_t)e * kCandCap;
     const float* s = p.scores + (size_t)e * p.score_stride;
     const int t = threadIdx.x, lane = t & 31;
+    pdl_trigger();
+    pdl_wait();  // scores and histogram come from the previous kernel
 
-    for (int i = t; i < kHistBins; i += kThreads) sm.h[i] = hist[i];
+    // Issue this thread's 16 score loads before anything waits on them.
+    constexpr int kPer = kChunk / kThreads;  // 16
+    const uint32_t begin = c * kChunk;
+    const uint32_t end = min(L, begin + kChunk);
+    const bool vec = (reinterpret_cast<uintptr_t>(s) & 15) == 0;
+    float v[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer / 4; ++i) {
+        const uint32_t j = begin + 4 * t + 4 * kThreads * i;
+        if (vec && j + 3 < end) {
+            const float4 q = __ldcg(reinterpret_cast<const float4*>(s + j));
+            v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
+        } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[4 * i + u] = j + u < end ? __ldcg(s + j + u) : __int_as_float(0x7FC00000);
+        }
+    }
+    for (int i = t; i < kHistBins; i += kThreads) sm.h[i] = __ldcg(hist + i);
     __syncthreads();
     const BinPick l0 = pick_bin(sm.h, width, sm.scratch);
     const bool take_all = l0.total <= width;
@@ -239,29 +303,26 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const TopkParams 
     const bool fast = n_cand <= (uint32_t)kCandCap;
 
     if (fast) {
-        const uint32_t begin = c * kChunk;
-        const uint32_t end = min(L, begin + kChunk);
-        for (uint32_t base = begin; base < end; base += kThreads) {
-            const uint32_t j = base + t;
-            bool take = false;
-            uint32_t key = 0;
-            if (j < end) {
-                const float x = s[j];
-                if (finite_f(x)) {
-                    key = score_key(x);
-                    take = (key >> 21) >= b0;
-                }
-            }
-            const uint32_t m = __ballot_sync(kFull, take);
-            if (m) {
-                const int leader = __ffs(m) - 1;
-                uint32_t pos = 0;
-                if (lane == leader) pos = atomicAdd(&ctl[0], (uint32_t)__popc(m));
-                pos = __shfl_sync(kFull, pos, leader);
-                if (take) {
-                    const uint32_t at = pos + __popc(m & ((1u << lane) - 1u));
-                    if (at < (uint32_t)kCandCap) cand[at] = ((uint64_t)key << 32) | j;
-                }
+        uint32_t take = 0;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) take |= (finite_f(v[i]) && (score_key(v[i]) >> 21) >= b0) ? (1u << i) : 0u;
+        const uint32_t cnt = __popc(take);
+        uint32_t incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const uint32_t total = __shfl_sync(kFull, incl, 31);
+        uint32_t base = 0;
+        if (lane == 31 && total) base = atomicAdd(&ctl[0], total);
+        uint32_t at = __shfl_sync(kFull, base, 31) + incl - cnt;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            if (take & (1u << i)) {
+                const uint32_t j = begin + 4 * t + 4 * kThreads * (i >> 2) + (i & 3);
+                if (at < (uint32_t)kCandCap) cand[at] = ((uint64_t)score_key(v[i]) << 32) | j;
+                ++at;
             }
         }
     }
@@ -276,30 +337,45 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(const TopkParams 
 
     int32_t* out = p.out + p.out_offset[e];
     if (fast) {
-        const uint32_t got = *(volatile uint32_t*)&ctl[0];
+        const uint32_t got = __ldcg(&ctl[0]);
         if (got != n_cand && t == 0) atomicOr(p.status, kStatusCandOverflow);
-        CandSource src{cand, got < (uint32_t)kCandCap ? got : (uint32_t)kCandCap};
+        const uint32_t n = got < (uint32_t)kCandCap ? got : (uint32_t)kCandCap;
         BinPick l0f = l0;
         l0f.bin = (int)b0;
-        finish_row(src, l0f, width, out, sm, p.status);
+        if (n <= (uint32_t)kSmemCand) {
+            for (uint32_t i = t; i < n; i += kThreads) {
+                const uint64_t x = __ldcg(cand + i);
+                sm.cand[i] = composite((uint32_t)(x >> 32), (uint32_t)x);
+            }
+            __syncthreads();
+            finish_row(SmemCandSource{sm.cand, n}, l0f, width, out, sm, p.status);
+        } else {
+            finish_row(CandSource{cand, n}, l0f, width, out, sm, p.status);
+        }
     } else {
-        RowSource src{s, L};
-        finish_row(src, l0, width, out, sm, p.status);
+        finish_row(RowSource{s, L}, l0, width, out, sm, p.status);
     }
 }
 
 uint32_t topk_chunk() { return kChunk; }
 
-cudaError_t launch_topk_hist(const TopkParams& p, cudaStream_t stream) {
+cudaError_t launch_topk_hist(const TopkParams& p, cudaStream_t stream, bool pdl) {
     if (p.total_chunks == 0) return cudaSuccess;
-    topk_hist_kernel<<<p.total_chunks, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(topk_hist_kernel, dim3(p.total_chunks), dim3(kThreads), 0, stream, pdl, p);
 }
 
-cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t stream) {
+cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t stream, bool pdl) {
     if (p.total_chunks == 0) return cudaSuccess;
-    topk_select_kernel<<<p.total_chunks, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(topk_select_kernel, dim3(p.total_chunks), dim3(kThreads), 0, stream, pdl, p);
+}
+
+__global__ void __launch_bounds__(1024) clear_kernel(uint32_t* __restrict__ p, uint32_t words) {
+    pdl_trigger();
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < words; i += gridDim.x * blockDim.x) p[i] = 0;
+}
+
+cudaError_t launch_clear(uint32_t* p, uint32_t words, cudaStream_t stream) {
+    return launch_kernel(clear_kernel, dim3(4), dim3(1024), 0, stream, false, p, words);
 }
 
 }  // namespace dsrows
