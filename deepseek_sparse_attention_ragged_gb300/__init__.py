@@ -22,7 +22,7 @@ from . import build as _build
 
 __all__ = [
     "DsRowsError", "Row", "load", "build", "library_path",
-    "ds_rows_workspace_bytes", "workspace", "ds_rows_indexer_score", "ds_rows_topk",
+    "ds_rows_workspace_bytes", "workspace", "ds_rows_indexer_score", "ds_rows_topk", "ds_rows_topk_static",
     "ds_rows_sparse_attn", "ds_rows_decode", "ds_rows_version",
     "ROWS_MAX", "INDEX_HEADS", "INDEX_DIM", "TOP_K", "HEADS", "DIM",
 ]
@@ -87,6 +87,8 @@ def load():
     lib.ds_rows_indexer_score.restype = i32
     lib.ds_rows_topk.argtypes = [rs, vp, sz, vp, vp, sz, vp]
     lib.ds_rows_topk.restype = i32
+    lib.ds_rows_topk_static.argtypes = [rs, vp, sz, vp, vp]
+    lib.ds_rows_topk_static.restype = i32
     lib.ds_rows_sparse_attn.argtypes = [rs, vp, vp, sz, vp, ctypes.c_float, vp, u32p, vp, sz, vp]
     lib.ds_rows_sparse_attn.restype = i32
     lib.ds_rows_decode.argtypes = [rs, vp, vp, vp, vp, sz, ctypes.c_float, vp, vp, u32p, vp, sz, vp]
@@ -231,6 +233,20 @@ def ds_rows_topk(rows, scores, score_stride, indices, workspace_t, stream=None):
     rs, keep = _rowset(tab, n)
     _check(lib, lib.ds_rows_topk(ctypes.byref(rs), _ptr(scores), int(score_stride), _ptr(indices),
                                  _ptr(workspace_t), workspace_t.numel(), _stream(stream)))
+
+
+def ds_rows_topk_static(rows, scores, score_stride, indices, stream=None):
+    """ds_rows_topk without a workspace: for callers that cannot allocate device
+    memory when they run this stage. The library keeps the scratch in one fixed
+    array per device; calls that overlap on the GPU must not share a device."""
+    lib = load()
+    rl = _rows_list(rows)
+    _require(scores, "scores", torch.float32, (len(rl) - 1) * score_stride + max(r[0] for r in rl))
+    _require(indices, "indices", torch.int32, max(r[2] + r[1] for r in rl))
+    tab, n = _table(rl)
+    rs, keep = _rowset(tab, n)
+    _check(lib, lib.ds_rows_topk_static(ctypes.byref(rs), _ptr(scores), int(score_stride), _ptr(indices),
+                                        _stream(stream)))
 
 
 def _attn_checks(rl, q_attn, sinks, sinks_row_stride, out, kv, invalid):

@@ -286,6 +286,52 @@ int check_indexer_args(const ds_bf16* q_index, const float* w_index) {
 
 }  // namespace
 
+// ---- top-k with scratch held by the library ------------------------------------
+// Some callers cannot allocate device memory at the point where they call the
+// top-k stage (a CUDA-graph or real-time caller that forbids allocation, or an
+// embedder whose allocator is not reachable from the calling code). For them
+// ds_rows_topk_static keeps the stage's scratch (status word, histogram,
+// per-row counters, candidate lists) in this one file-scope device array,
+// sized for DS_ROWS_MAX rows; every GPU that loads the library holds it until
+// the process exits.
+namespace {
+
+constexpr size_t kStaticHist = 256;
+constexpr size_t kStaticCtl = kStaticHist + (size_t)kRowsMax * kHistBins * 4;
+constexpr size_t kStaticCand = align256(kStaticCtl + (size_t)kRowsMax * kCtlWords * 4);
+constexpr size_t kStaticBytes = kStaticCand + (size_t)kRowsMax * kCandCap * 8;
+static_assert(kStaticBytes == DS_TOPK_STATIC_SCRATCH_BYTES, "header size must match the scratch layout");
+
+}  // namespace
+
+static __device__ __align__(256) uint8_t g_topk_scratch[kStaticBytes];
+
+namespace {
+
+std::mutex g_scratch_mu;
+uint8_t* g_scratch_ptr[64] = {};
+
+// The scratch's device address on the current device, looked up once per
+// device. In host code `g_topk_scratch` names a host-side stand-in, never
+// the device memory, so only this address may be passed to a kernel.
+int topk_scratch(uint8_t** out) {
+    int dev = -1;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(DS_ECUDA, "device %d is out of range", dev);
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* addr = nullptr;
+        err = cudaGetSymbolAddress(&addr, g_topk_scratch);
+        if (err != cudaSuccess) return cuda_fail(err, "cudaGetSymbolAddress of the top-k scratch");
+        g_scratch_ptr[dev] = static_cast<uint8_t*>(addr);
+    }
+    *out = g_scratch_ptr[dev];
+    return DS_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 size_t ds_rows_workspace_bytes(int rows, const ds_row_t* table) {
@@ -376,6 +422,35 @@ int ds_rows_decode(const ds_row_set_t* set, const ds_bf16* q_index, const float*
     rc = run_topk(set, scores, L.score_stride, idx, off, ws, L, false, s);
     if (rc) return rc;
     return run_attention(set, q_attn, sinks, sinks_row_stride, idx, off, scale, out, invalid, ws, L, s);
+}
+
+int ds_rows_topk_static(const ds_row_set_t* set, const float* scores, size_t score_stride, int32_t* indices,
+                        void* stream) {
+    int rc = check_set(set, kDisjointOut);
+    if (rc) return rc;
+    if (!scores || !indices) return fail(DS_EINVAL, "scores and indices must be non-NULL");
+    for (int e = 0; e < set->rows; ++e)
+        if (score_stride < set->table[e].kv_len)
+            return fail(DS_EINVAL, "score_stride %zu is shorter than row %d (kv_len %u)", score_stride, e,
+                        set->table[e].kv_len);
+    const size_t need = kStaticCand + (size_t)set->rows * kCandCap * 8;
+    if (need > kStaticBytes)
+        return fail(DS_ESIZE, "top-k needs %zu bytes of scratch, the library holds %zu", need, kStaticBytes);
+    uint8_t* ws = nullptr;
+    rc = topk_scratch(&ws);
+    if (rc) return rc;
+    Layout L{};
+    L.hist = kStaticHist;
+    L.ctl = kStaticCtl;
+    L.cand = kStaticCand;
+    cudaStream_t s = (cudaStream_t)stream;
+    // The array keeps the previous call's contents: zero the status word,
+    // histogram and counters (the candidate lists need no clearing).
+    cudaError_t err = launch_clear(reinterpret_cast<uint32_t*>(ws), (uint32_t)(kStaticCand / 4), s);
+    if (err != cudaSuccess) return cuda_fail(err, "scratch clear");
+    uint32_t off[DS_ROWS_MAX];
+    for (int e = 0; e < set->rows; ++e) off[e] = set->table[e].index_offset;
+    return run_topk(set, scores, score_stride, indices, off, ws, L, true, s);
 }
 
 const char* ds_rows_last_error(void) { return g_error.c_str(); }

@@ -124,6 +124,31 @@ int ds_rows_topk(const ds_row_set_t* set, const float* scores, size_t score_stri
                  int32_t* indices, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Top-k without a workspace. There is no counterpart on the prior-art pages:
+ * this entry point exists for callers that cannot allocate device memory when
+ * they run the top-k stage, for example code running under a CUDA graph or a
+ * real-time loop that forbids allocation, or an embedding whose device
+ * allocator is not reachable from the calling code. It computes exactly what
+ * ds_rows_topk computes (same arguments, bitwise the same indices) but keeps
+ * its scratch in one fixed array inside the library instead of a
+ * caller-provided workspace, and allocates nothing.
+ *   - Size: the array holds DS_TOPK_STATIC_SCRATCH_BYTES bytes (about 1.1 MB),
+ *     enough for DS_ROWS_MAX rows of any kv_len; every GPU that loads the
+ *     library keeps it until the process exits. A table needing more is
+ *     rejected with DS_ESIZE (more than DS_ROWS_MAX rows is DS_EINVAL).
+ *   - Set-up: the first call on each device looks up the array's device
+ *     address (with that device current). Make that first call before any
+ *     stream capture.
+ *   - Sharing: every call on a device uses the same array, which keeps the
+ *     previous call's contents; each call clears what must start at zero.
+ *     Calls that overlap on the GPU (different streams, no ordering between
+ *     them) race on the array and give wrong results: order them.
+ */
+#define DS_TOPK_STATIC_SCRATCH_BYTES 1114880
+int ds_rows_topk_static(const ds_row_set_t* set, const float* scores, size_t score_stride,
+                        int32_t* indices, void* stream);
+
+/*
  * (3)+(4) Gather and sink-softmax sparse attention
  * (`deepseek_sparse_attention_score_rows_bf16` + `..._reduce_rows_bf16`):
  * for each entry e and head h, over the slots t < width with index

@@ -1,0 +1,62 @@
+"""The workspace-free top-k entry point, checked against the ordinary one.
+
+ds_rows_topk_static exists for callers that cannot allocate device memory when
+they run the top-k stage (allocation-free graph or real-time code, or code that
+cannot reach the device allocator). It keeps its scratch in one array inside
+the library, so this test calls it twice in a row, on different scores, to show
+that each call starts from a clean state, and compares every result with
+ds_rows_topk through the C-ABI. The indices are integers: they must be equal.
+
+This file sorts last so that a run stopping at the first failure has already
+run every other test.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import deepseek_sparse_attention_ragged_gb300 as ds
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    ds.build()
+    ds.load()
+
+
+def _scores(seed, lens, **kw):
+    rows_s = workloads.random_scores(seed, lens, **kw)
+    stride = max(lens)
+    host = np.full((len(lens), stride), np.nan, np.float32)
+    for e, s in enumerate(rows_s):
+        host[e, : len(s)] = s
+    return torch.from_numpy(host).cuda(), stride
+
+
+def test_static_scratch_topk_matches_workspace_topk_twice():
+    lens = [131072, 40000, 513, 1, 9000, 70000, 2048, 300]
+    rows = [workloads.Row(L, min(512, L), 512 * e, e) for e, L in enumerate(lens)]
+    ws = ds.workspace(rows)
+    for call, kw in enumerate([dict(), dict(ties=True, nonfinite=True)]):
+        scores, stride = _scores(71 + call, lens, **kw)
+        want = torch.full((512 * len(lens),), -7, dtype=torch.int32, device="cuda")
+        got = torch.full_like(want, -9)
+        ds.ds_rows_topk(rows, scores, stride, want, ws)
+        ds.ds_rows_topk_static(rows, scores, stride, got)
+        torch.cuda.synchronize()
+        for r in rows:
+            sl = slice(r.index_offset, r.index_offset + r.width)
+            assert torch.equal(got[sl], want[sl]), f"call {call}, row kv_len {r.kv_len}"
+
+
+def test_static_scratch_topk_rejects_too_many_rows():
+    rows = [workloads.Row(16, 16, 16 * e, e) for e in range(9)]
+    scores = torch.zeros((9, 16), dtype=torch.float32, device="cuda")
+    idx = torch.zeros((9 * 16,), dtype=torch.int32, device="cuda")
+    with pytest.raises(ds.DsRowsError, match="rows must be 1..=8"):
+        ds.ds_rows_topk_static(rows, scores, 16, idx)
