@@ -45,8 +45,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 // ---- workspace layout ------------------------------------------------------
 struct Layout {
     size_t status = 0;  // u32 status word at offset 0
-    size_t hist, ctl, flags, ctl_end;
-    size_t cand, topk, part, scores, total;
+    size_t hist, flags, ctl_end;
+    size_t topk, part, scores, total;
     uint32_t attn_chunks;
     uint64_t score_stride;  // floats per row of the decode scores
 };
@@ -54,11 +54,9 @@ struct Layout {
 Layout make_layout(int rows, const ds_row_t* table) {
     Layout L;
     L.hist = 256;
-    L.ctl = align256(L.hist + (size_t)kRowsMax * kHistBins * 4);
-    L.flags = align256(L.ctl + (size_t)kRowsMax * kCtlWords * 4);
+    L.flags = align256(L.hist + (size_t)kRowsMax * kHistBins * 4);
     L.ctl_end = align256(L.flags + ((size_t)kRowsMax * kHeads + kRowsMax) * 4);
-    L.cand = L.ctl_end;
-    L.topk = align256(L.cand + (size_t)rows * kCandCap * 8);
+    L.topk = L.ctl_end;
     L.part = align256(L.topk + (size_t)kRowsMax * kTopK * 4);
     uint32_t chunks = 0, max_len = 0;
     for (int e = 0; e < rows; ++e) {
@@ -66,7 +64,7 @@ Layout make_layout(int rows, const ds_row_t* table) {
         if (table[e].kv_len > max_len) max_len = table[e].kv_len;
     }
     L.attn_chunks = chunks;
-    L.scores = align256(L.part + (size_t)chunks * kPartFloats * 4);
+    L.scores = align256(L.part + 2 * (size_t)chunks * kPartFloats * 4);  // two head halves
     L.score_stride = ((uint64_t)max_len + 63) & ~uint64_t(63);
     L.total = align256(L.scores + (size_t)rows * L.score_stride * 4);
     return L;
@@ -223,8 +221,6 @@ int run_topk(const ds_row_set_t* set, const float* scores, uint64_t stride, int3
     p.score_stride = stride;
     p.out = out;
     p.hist = reinterpret_cast<uint32_t*>(ws + L.hist);
-    p.ctl = reinterpret_cast<uint32_t*>(ws + L.ctl);
-    p.cand = reinterpret_cast<uint64_t*>(ws + L.cand);
     p.status = reinterpret_cast<uint32_t*>(ws + L.status);
     p.rows = (uint32_t)set->rows;
     p.total_chunks = chunks;
@@ -290,16 +286,14 @@ int check_indexer_args(const ds_bf16* q_index, const float* w_index) {
 // Some callers cannot allocate device memory at the point where they call the
 // top-k stage (a CUDA-graph or real-time caller that forbids allocation, or an
 // embedder whose allocator is not reachable from the calling code). For them
-// ds_rows_topk_static keeps the stage's scratch (status word, histogram,
-// per-row counters, candidate lists) in this one file-scope device array,
-// sized for DS_ROWS_MAX rows; every GPU that loads the library holds it until
-// the process exits.
+// ds_rows_topk_static keeps the stage's scratch (status word and the per-row
+// score histograms) in this one file-scope device array, sized for
+// DS_ROWS_MAX rows; every GPU that loads the library holds it until the
+// process exits.
 namespace {
 
 constexpr size_t kStaticHist = 256;
-constexpr size_t kStaticCtl = kStaticHist + (size_t)kRowsMax * kHistBins * 4;
-constexpr size_t kStaticCand = align256(kStaticCtl + (size_t)kRowsMax * kCtlWords * 4);
-constexpr size_t kStaticBytes = kStaticCand + (size_t)kRowsMax * kCandCap * 8;
+constexpr size_t kStaticBytes = kStaticHist + (size_t)kRowsMax * kHistBins * 4;
 static_assert(kStaticBytes == DS_TOPK_STATIC_SCRATCH_BYTES, "header size must match the scratch layout");
 
 }  // namespace
@@ -433,7 +427,7 @@ int ds_rows_topk_static(const ds_row_set_t* set, const float* scores, size_t sco
         if (score_stride < set->table[e].kv_len)
             return fail(DS_EINVAL, "score_stride %zu is shorter than row %d (kv_len %u)", score_stride, e,
                         set->table[e].kv_len);
-    const size_t need = kStaticCand + (size_t)set->rows * kCandCap * 8;
+    const size_t need = kStaticHist + (size_t)set->rows * kHistBins * 4;
     if (need > kStaticBytes)
         return fail(DS_ESIZE, "top-k needs %zu bytes of scratch, the library holds %zu", need, kStaticBytes);
     uint8_t* ws = nullptr;
@@ -441,12 +435,10 @@ int ds_rows_topk_static(const ds_row_set_t* set, const float* scores, size_t sco
     if (rc) return rc;
     Layout L{};
     L.hist = kStaticHist;
-    L.ctl = kStaticCtl;
-    L.cand = kStaticCand;
     cudaStream_t s = (cudaStream_t)stream;
-    // The array keeps the previous call's contents: zero the status word,
-    // histogram and counters (the candidate lists need no clearing).
-    cudaError_t err = launch_clear(reinterpret_cast<uint32_t*>(ws), (uint32_t)(kStaticCand / 4), s);
+    // The array keeps the previous call's contents: zero the status word and
+    // the histograms before they are rebuilt.
+    cudaError_t err = launch_clear(reinterpret_cast<uint32_t*>(ws), (uint32_t)(kStaticBytes / 4), s);
     if (err != cudaSuccess) return cuda_fail(err, "scratch clear");
     uint32_t off[DS_ROWS_MAX];
     for (int e = 0; e < set->rows; ++e) off[e] = set->table[e].index_offset;

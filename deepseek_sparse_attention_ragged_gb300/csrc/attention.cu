@@ -6,13 +6,14 @@
 //   l_t = scale * q_h . KV[i_t],  m = max(sink_h, max l_t),
 //   den = exp(sink_h - m) + sum exp(l_t - m),  out_h = sum exp(l_t - m) KV[i_t] / den.
 //
-// GB300 design. A row's `width` slots are split into chunks of 32; one CTA per
-// (row, chunk) gathers its 32 KV rows (1 KiB each, 16-byte cp.async, read once
-// for all 64 heads), computes the 64x32 logits S = Q G^T and the 64x512
-// partial P G on tensor cores (mma.sync m16n8k16 bf16, fp32 accumulate), with
-// a chunk-local softmax (m_c, l_c). P enters the second product as a bf16
-// hi + lo pair, which keeps ~16 bits of each weight. A second kernel combines
-// the chunks of a row in chunk order with the sink:
+// GB300 design. A row's `width` slots are split into chunks of 64; one CTA per
+// (row, half of the 64 heads, chunk) gathers its 64 KV rows (1 KiB each,
+// 16-byte cp.async, read once for the CTA's 32 heads), computes the 32x64
+// logits S = Q G^T and the 32x512 partial P G on tensor cores (mma.sync
+// m16n8k16 bf16, fp32 accumulate), with a chunk-local softmax (m_c, l_c)
+// whose warp reductions run for four heads side by side. P enters the second
+// product as a bf16 hi + lo pair, which keeps ~16 bits of each weight. A
+// second kernel combines the chunks of a (row, half) in chunk order with the sink:
 //   m = max(sink, m_c), den = exp(sink - m) + sum_c l_c exp(m_c - m),
 //   out = sum_c acc_c exp(m_c - m) / den,
 // so every reduction order depends on the row's width alone.
@@ -30,27 +31,29 @@ namespace dsrows {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kSlots = kAttnSlots;  // 32
-constexpr int kQStride = kDim + 8;  // bf16 per smem row: 1040 B, conflict-free ldmatrix
-constexpr int kPStride = kSlots + 8;
+constexpr int kSlots = kAttnSlots;        // 64 selected slots per CTA
+constexpr int kHalf = kHeads / 2;         // 32 heads per CTA
+constexpr int kQStride = kDim + 8;        // bf16 per smem row: 1040 B, conflict-free ldmatrix
+constexpr int kPStride = kSlots + 8;      // 144 B rows, conflict-free ldmatrix
 constexpr int kLgStride = kSlots + 1;
 
 struct SmemLayout {
     static constexpr size_t q = 0;
-    static constexpr size_t g = q + (size_t)kHeads * kQStride * 2;
+    static constexpr size_t g = q + (size_t)kHalf * kQStride * 2;
     static constexpr size_t p_hi = g + (size_t)kSlots * kQStride * 2;
-    static constexpr size_t p_lo = p_hi + (size_t)kHeads * kPStride * 2;
-    static constexpr size_t lg = p_lo + (size_t)kHeads * kPStride * 2;
-    static constexpr size_t idx = lg + (size_t)kHeads * kLgStride * 4;
+    static constexpr size_t p_lo = p_hi + (size_t)kHalf * kPStride * 2;
+    static constexpr size_t lg = p_lo + (size_t)kHalf * kPStride * 2;
+    static constexpr size_t idx = lg + (size_t)kHalf * kLgStride * 4;
     static constexpr size_t total = idx + kSlots * 4;
 };
 constexpr size_t kSmemBytes = SmemLayout::total;
 
-__device__ __forceinline__ int entry_of_chunk(const AttnParams& p, uint32_t c) {
+// CTA b -> (entry, head half, chunk): entry e owns CTAs [2 chunk_begin[e], 2 chunk_begin[e+1]).
+__device__ __forceinline__ int entry_of_cta(const AttnParams& p, uint32_t b) {
     int e = 0;
 #pragma unroll
     for (int i = 1; i < kRowsMax; ++i)
-        if (i < (int)p.rows && c >= p.chunk_begin[i]) e = i;
+        if (i < (int)p.rows && b >= 2 * p.chunk_begin[i]) e = i;
     return e;
 }
 
@@ -79,19 +82,10 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    return v;
-}
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    return v;
-}
-
 }  // namespace
 
+// One CTA per (row, head half, 64-slot chunk): blockIdx = 2 * chunk_begin[e] + 2 * c + half... laid out as
+// [entry][half][chunk] so a row's two halves are adjacent ranges.
 __global__ void __launch_bounds__(kThreads, 1) attn_partial_kernel(const AttnParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __nv_bfloat16* q_s = reinterpret_cast<__nv_bfloat16*>(smem + SmemLayout::q);
@@ -102,16 +96,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_kernel(const AttnPar
     int* idx_s = reinterpret_cast<int*>(smem + SmemLayout::idx);
 
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const int e = entry_of_chunk(p, blockIdx.x);
-    const uint32_t c = blockIdx.x - p.chunk_begin[e];
+    const int e = entry_of_cta(p, blockIdx.x);
     const uint32_t W = p.width[e];
+    const uint32_t nchunks = (W + kSlots - 1) / kSlots;
+    const uint32_t local = blockIdx.x - 2 * p.chunk_begin[e];
+    const int half = (int)(local / nchunks);
+    const uint32_t c = local % nchunks;
+    const int head0 = half * kHalf;
     const int L = (int)p.kv_len[e];
     const __nv_bfloat16* kv = p.kv[e];
 
     pdl_trigger();
     // The query is an input of the call: fetch it while the previous kernel finishes.
-    const __nv_bfloat16* q = p.q + (size_t)p.q_row[e] * kHeads * kDim;
-    for (int k = t; k < kHeads * (kDim / 8); k += kThreads) {
+    const __nv_bfloat16* q = p.q + ((size_t)p.q_row[e] * kHeads + head0) * kDim;
+    for (int k = t; k < kHalf * (kDim / 8); k += kThreads) {
         const int row = k >> 6, col = (k & 63) * 8;
         cp_async16(q_s + row * kQStride + col, q + (size_t)row * kDim + col);
     }
@@ -131,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_kernel(const AttnPar
     }
     __syncthreads();
 
-    // Gather the chunk's selected KV rows (1 KiB each, once for all heads).
+    // Gather the chunk's selected KV rows (1 KiB each, once for the CTA's 32 heads).
     for (int k = t; k < kSlots * (kDim / 8); k += kThreads) {
         const int row = k >> 6, col = (k & 63) * 8;
         const int i = idx_s[row];
@@ -143,13 +141,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_kernel(const AttnPar
     __syncthreads();
 
     // ---- S = Q G^T : warp -> 16 heads x 16 slots ----------------------------
-    const int mt = warp >> 1;       // head tile (16 heads)
+    const int mt = warp >> 2;  // head tile (16 heads)
     {
-        const int nh = warp & 1;    // slot half (16 slots)
+        const int nq = warp & 3;  // slot quarter (16 slots)
         float acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
         const uint32_t a_addr = smem_u32(q_s + (16 * mt + (lane & 15)) * kQStride + (lane >> 4) * 8);
         const uint32_t b_addr =
-            smem_u32(g_s + (16 * nh + (lane >> 4) * 8 + (lane & 7)) * kQStride + ((lane >> 3) & 1) * 8);
+            smem_u32(g_s + (16 * nq + (lane >> 4) * 8 + (lane & 7)) * kQStride + ((lane >> 3) & 1) * 8);
 #pragma unroll 8
         for (int k0 = 0; k0 < kDim; k0 += 16) {
             uint32_t a[4], b[4];
@@ -161,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_kernel(const AttnPar
         const int h0 = 16 * mt + (lane >> 2);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            const int s0 = 16 * nh + nt * 8 + 2 * (lane & 3);
+            const int s0 = 16 * nq + nt * 8 + 2 * (lane & 3);
             lg_s[h0 * kLgStride + s0] = acc[nt][0] * p.scale;
             lg_s[h0 * kLgStride + s0 + 1] = acc[nt][1] * p.scale;
             lg_s[(h0 + 8) * kLgStride + s0] = acc[nt][2] * p.scale;
@@ -170,108 +168,135 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_kernel(const AttnPar
     }
     __syncthreads();
 
-    // ---- chunk softmax: warp -> 8 heads, lane -> slot -----------------------
+    // ---- chunk softmax: warp -> 4 heads (reduced side by side), lane -> 2 slots
     float* part = p.part + (size_t)blockIdx.x * kPartFloats;
     {
-        const bool live = idx_s[lane] >= 0;
-        for (int hh = 0; hh < 8; ++hh) {
-            const int h = warp * 8 + hh;
-            const float l = lg_s[h * kLgStride + lane];
-            const bool ok = live && finite_f(l);
-            if (__any_sync(0xFFFFFFFFu, live && !ok) && lane == 0) atomicOr(&p.flags[e * kHeads + h], 1u);
-            const float m = warp_max(ok ? l : -INFINITY);
-            const float w = ok ? expf(l - m) : 0.0f;
-            const float sum = warp_sum(w);
-            const __nv_bfloat16 hi = __float2bfloat16_rn(w);
-            const __nv_bfloat16 lo = __float2bfloat16_rn(w - __bfloat162float(hi));
-            ph_s[h * kPStride + lane] = hi;
-            pl_s[h * kPStride + lane] = lo;
+        constexpr int kH = kHalf / 8;  // 4 heads per warp
+        const bool live0 = idx_s[lane] >= 0, live1 = idx_s[lane + 32] >= 0;
+        float l0[kH], l1[kH], m[kH], w0[kH], w1[kH], sum[kH];
+        bool bad[kH];
+#pragma unroll
+        for (int i = 0; i < kH; ++i) {
+            const int h = warp * kH + i;
+            l0[i] = lg_s[h * kLgStride + lane];
+            l1[i] = lg_s[h * kLgStride + lane + 32];
+            const bool ok0 = live0 && finite_f(l0[i]), ok1 = live1 && finite_f(l1[i]);
+            bad[i] = (live0 && !ok0) || (live1 && !ok1);
+            if (!ok0) l0[i] = -INFINITY;
+            if (!ok1) l1[i] = -INFINITY;
+            m[i] = fmaxf(l0[i], l1[i]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int i = 0; i < kH; ++i) m[i] = fmaxf(m[i], __shfl_xor_sync(0xFFFFFFFFu, m[i], o));
+#pragma unroll
+        for (int i = 0; i < kH; ++i) {
+            w0[i] = l0[i] == -INFINITY ? 0.0f : expf(l0[i] - m[i]);
+            w1[i] = l1[i] == -INFINITY ? 0.0f : expf(l1[i] - m[i]);
+            sum[i] = w0[i] + w1[i];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int i = 0; i < kH; ++i) sum[i] += __shfl_xor_sync(0xFFFFFFFFu, sum[i], o);
+#pragma unroll
+        for (int i = 0; i < kH; ++i) {
+            const int h = warp * kH + i;
+            if (__any_sync(0xFFFFFFFFu, bad[i]) && lane == 0) atomicOr(&p.flags[e * kHeads + head0 + h], 1u);
+            const __nv_bfloat16 hi0 = __float2bfloat16_rn(w0[i]), hi1 = __float2bfloat16_rn(w1[i]);
+            ph_s[h * kPStride + lane] = hi0;
+            ph_s[h * kPStride + lane + 32] = hi1;
+            pl_s[h * kPStride + lane] = __float2bfloat16_rn(w0[i] - __bfloat162float(hi0));
+            pl_s[h * kPStride + lane + 32] = __float2bfloat16_rn(w1[i] - __bfloat162float(hi1));
             if (lane == 0) {
-                part[h] = m;
-                part[kHeads + h] = sum;
+                part[h] = m[i];
+                part[kHalf + h] = sum[i];
             }
         }
     }
     __syncthreads();
 
-    // ---- acc = P G : warp -> 16 heads x 256 features ------------------------
+    // ---- acc = P G : warp -> 16 heads x 128 features ------------------------
     {
-        const int fh = warp & 1;
-        float acc[32][4];
+        const int fq = warp & 3;
+        float acc[16][4];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
-        uint32_t ah[2][4], al[2][4];
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-            const int off = (16 * mt + (lane & 15)) * kPStride + 16 * ks + (lane >> 4) * 8;
-            ldsm_x4(smem_u32(ph_s + off), ah[ks][0], ah[ks][1], ah[ks][2], ah[ks][3]);
-            ldsm_x4(smem_u32(pl_s + off), al[ks][0], al[ks][1], al[ks][2], al[ks][3]);
-        }
+        for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
         // ldmatrix.trans lane address: row (slot) = k0 + (mi % 2) * 8 + lane % 8, col = n0 + (mi / 2) * 8.
         const int mi = lane >> 3;
         const uint32_t b_base =
-            smem_u32(g_s + ((mi & 1) * 8 + (lane & 7)) * kQStride + fh * 256 + (mi >> 1) * 8);
+            smem_u32(g_s + ((mi & 1) * 8 + (lane & 7)) * kQStride + fq * 128 + (mi >> 1) * 8);
 #pragma unroll
-        for (int pr = 0; pr < 16; ++pr) {
+        for (int ks = 0; ks < kSlots / 16; ++ks) {
+            uint32_t ah[4], al[4];
+            const int off = (16 * mt + (lane & 15)) * kPStride + 16 * ks + (lane >> 4) * 8;
+            ldsm_x4(smem_u32(ph_s + off), ah[0], ah[1], ah[2], ah[3]);
+            ldsm_x4(smem_u32(pl_s + off), al[0], al[1], al[2], al[3]);
 #pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
+            for (int pr = 0; pr < 8; ++pr) {
                 uint32_t b[4];
                 ldsm_x4_t(b_base + (16 * ks * kQStride + 16 * pr) * 2, b[0], b[1], b[2], b[3]);
-                mma_bf16(acc[2 * pr], ah[ks], b[0], b[1]);
-                mma_bf16(acc[2 * pr], al[ks], b[0], b[1]);
-                mma_bf16(acc[2 * pr + 1], ah[ks], b[2], b[3]);
-                mma_bf16(acc[2 * pr + 1], al[ks], b[2], b[3]);
+                mma_bf16(acc[2 * pr], ah, b[0], b[1]);
+                mma_bf16(acc[2 * pr], al, b[0], b[1]);
+                mma_bf16(acc[2 * pr + 1], ah, b[2], b[3]);
+                mma_bf16(acc[2 * pr + 1], al, b[2], b[3]);
             }
         }
-        float* pacc = part + 2 * kHeads;
+        float* pacc = part + 2 * kHalf;
         const int h0 = 16 * mt + (lane >> 2);
 #pragma unroll
-        for (int nt = 0; nt < 32; ++nt) {
-            const int f = fh * 256 + nt * 8 + 2 * (lane & 3);
+        for (int nt = 0; nt < 16; ++nt) {
+            const int f = fq * 128 + nt * 8 + 2 * (lane & 3);
             *reinterpret_cast<float2*>(pacc + (size_t)h0 * kDim + f) = make_float2(acc[nt][0], acc[nt][1]);
             *reinterpret_cast<float2*>(pacc + (size_t)(h0 + 8) * kDim + f) = make_float2(acc[nt][2], acc[nt][3]);
         }
     }
 }
 
-// Combine the chunks of a row: CTA = (row, 16 features), thread = (head, 4 features).
-constexpr int kCombineFeatures = 16;
-constexpr int kCombineBlocks = kDim / kCombineFeatures;  // 32 per row
+// Combine the chunks of a (row, head half): CTA = (row, half, 64 features), thread = (head, 8 features).
+constexpr int kCombineFeatures = 64;
+constexpr int kCombineBlocks = kDim / kCombineFeatures;  // 8 per (row, half)
 
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
-    __shared__ float mc_s[kAttnChunksMax][kHeads];
-    __shared__ float lc_s[kAttnChunksMax][kHeads];
-    __shared__ float fac[kHeads][kAttnChunksMax + 1];
-    __shared__ float inv_den[kHeads];
-    __shared__ uint32_t bad[kHeads];
-    const int e = blockIdx.x / kCombineBlocks;
+    __shared__ float mc_s[kAttnChunksMax][kHalf];
+    __shared__ float lc_s[kAttnChunksMax][kHalf];
+    __shared__ float fac[kHalf][kAttnChunksMax + 1];
+    __shared__ float inv_den[kHalf];
+    __shared__ uint32_t bad[kHalf];
+    const int e = blockIdx.x / (2 * kCombineBlocks);
+    const int half = (blockIdx.x / kCombineBlocks) & 1;
     const int fb = blockIdx.x % kCombineBlocks;
+    const int head0 = half * kHalf;
     const int t = threadIdx.x;
     const uint32_t W = p.width[e];
     const int nchunks = (int)((W + kSlots - 1) / kSlots);
-    const float* part0 = p.part + (size_t)p.chunk_begin[e] * kPartFloats;
+    const float* part0 = p.part + ((size_t)2 * p.chunk_begin[e] + (size_t)half * nchunks) * kPartFloats;
     pdl_trigger();
     pdl_wait();  // partials and flags come from the partial kernel
 
     // Issue every load of this thread before using any.
-    const int h = t >> 2;
-    const int f = fb * kCombineFeatures + (t & 3) * 4;
-    float4 v[kAttnChunksMax];
+    const int h = t >> 3;
+    const int f = fb * kCombineFeatures + (t & 7) * 8;
+    float4 v[kAttnChunksMax][2];
 #pragma unroll
     for (int c = 0; c < kAttnChunksMax; ++c)
-        if (c < nchunks)
-            v[c] = __ldcg(reinterpret_cast<const float4*>(part0 + (size_t)c * kPartFloats + 2 * kHeads +
-                                                          (size_t)h * kDim + f));
-    for (int i = t; i < nchunks * kHeads; i += 256) {
-        const int c = i / kHeads, hh = i % kHeads;
+        if (c < nchunks) {
+            const float* src = part0 + (size_t)c * kPartFloats + 2 * kHalf + (size_t)h * kDim + f;
+            v[c][0] = __ldcg(reinterpret_cast<const float4*>(src));
+            v[c][1] = __ldcg(reinterpret_cast<const float4*>(src + 4));
+        }
+    if (t < nchunks * kHalf) {
+        const int c = t / kHalf, hh = t % kHalf;
         mc_s[c][hh] = __ldcg(part0 + (size_t)c * kPartFloats + hh);
-        lc_s[c][hh] = __ldcg(part0 + (size_t)c * kPartFloats + kHeads + hh);
+        lc_s[c][hh] = __ldcg(part0 + (size_t)c * kPartFloats + kHalf + hh);
     }
     __syncthreads();
-    if (t < kHeads) {
+    if (t < kHalf) {
+        const int hd = head0 + t;
         const bool row_bad = __ldcg(p.flags + kRowsMax * kHeads + e) != 0;
-        const float sink = p.sinks[(size_t)p.q_row[e] * p.sinks_row_stride + t];
-        uint32_t inv = row_bad || __ldcg(p.flags + e * kHeads + t) != 0 || !finite_f(sink);
+        const float sink = p.sinks[(size_t)p.q_row[e] * p.sinks_row_stride + hd];
+        uint32_t inv = row_bad || __ldcg(p.flags + e * kHeads + hd) != 0 || !finite_f(sink);
         float m = sink;
         for (int c = 0; c < nchunks; ++c) m = fmaxf(m, mc_s[c][t]);
         float den = finite_f(sink) ? expf(sink - m) : 0.0f;
@@ -284,29 +309,31 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnParams p) {
         if (!finite_f(den) || !(den > 0.0f) || !finite_f(m)) inv = 1;
         inv_den[t] = 1.0f / den;
         bad[t] = inv;
-        if (p.invalid && fb == 0) p.invalid[(size_t)p.q_row[e] * kHeads + t] = inv;
+        if (p.invalid && fb == 0) p.invalid[(size_t)p.q_row[e] * kHeads + hd] = inv;
     }
     __syncthreads();
 
-    float4 acc = make_float4(0, 0, 0, 0);
+    float r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
     for (int c = 0; c < kAttnChunksMax; ++c) {
         if (c < nchunks) {
             const float w = fac[h][c];
-            acc.x = fmaf(v[c].x, w, acc.x);
-            acc.y = fmaf(v[c].y, w, acc.y);
-            acc.z = fmaf(v[c].z, w, acc.z);
-            acc.w = fmaf(v[c].w, w, acc.w);
+            r[0] = fmaf(v[c][0].x, w, r[0]); r[1] = fmaf(v[c][0].y, w, r[1]);
+            r[2] = fmaf(v[c][0].z, w, r[2]); r[3] = fmaf(v[c][0].w, w, r[3]);
+            r[4] = fmaf(v[c][1].x, w, r[4]); r[5] = fmaf(v[c][1].y, w, r[5]);
+            r[6] = fmaf(v[c][1].z, w, r[6]); r[7] = fmaf(v[c][1].w, w, r[7]);
         }
     }
     const float sc = inv_den[h];
     const bool zero = bad[h] != 0;
-    const float r[4] = {acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc};
-    __nv_bfloat16 o[4];
+    __align__(16) __nv_bfloat16 o[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) o[i] = __float2bfloat16_rn(!zero && finite_f(r[i]) ? r[i] : 0.0f);
-    __nv_bfloat16* out = p.out + ((size_t)p.q_row[e] * kHeads + h) * kDim + f;
-    *reinterpret_cast<uint2*>(out) = *reinterpret_cast<const uint2*>(o);
+    for (int i = 0; i < 8; ++i) {
+        const float x = r[i] * sc;
+        o[i] = __float2bfloat16_rn(!zero && finite_f(x) ? x : 0.0f);
+    }
+    __nv_bfloat16* out = p.out + ((size_t)p.q_row[e] * kHeads + head0 + h) * kDim + f;
+    *reinterpret_cast<uint4*>(out) = *reinterpret_cast<const uint4*>(o);
 }
 
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream, bool pdl) {
@@ -318,10 +345,10 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream, bool pdl)
         configured = true;
     }
     if (p.total_chunks == 0) return cudaSuccess;
-    cudaError_t err = launch_kernel(attn_partial_kernel, dim3(p.total_chunks), dim3(kThreads), kSmemBytes, stream,
-                                    pdl, p);
+    cudaError_t err = launch_kernel(attn_partial_kernel, dim3(2 * p.total_chunks), dim3(kThreads), kSmemBytes,
+                                    stream, pdl, p);
     if (err != cudaSuccess) return err;
-    return launch_kernel(attn_combine_kernel, dim3(p.rows * kCombineBlocks), dim3(256), 0, stream, true, p);
+    return launch_kernel(attn_combine_kernel, dim3(p.rows * 2 * kCombineBlocks), dim3(256), 0, stream, true, p);
 }
 
 }  // namespace dsrows

@@ -31,19 +31,15 @@ constexpr uint64_t kWaitBudgetNs = 2000000000ull;
 // ---------------------------------------------------------------------------
 //   [0, 256)                 control: u32 status, u32 pad...
 //   hist   [8][2048] u32     level-0 histogram of score keys per entry
-//   ctl    [8][16]  u32      per-entry counters (candidates, arrivals)
 //   flags  [8][64]  u32      per-entry, per-head attention invalid bits
-//   cand   [8][kCandCap] u64 top-k candidates (key << 32 | index)
 //   topk   [8][512] i32      selected indices (decode without an indices output)
 //   part   [chunks][...]     attention partials
 //   scores [8][stride] f32   indexer scores (decode only)
 constexpr int kHistBins = 2048;
-constexpr int kCtlWords = 16;
-constexpr int kCandCap = 16384;
-constexpr int kAttnSlots = 32;                       // selected slots per attention CTA
-constexpr int kAttnChunksMax = kTopK / kAttnSlots;   // 16
-// One attention partial: m[64], l[64], acc[64][512] (fp32).
-constexpr size_t kPartFloats = 64 + 64 + (size_t)kHeads * kDim;
+constexpr int kAttnSlots = 64;                       // selected slots per attention CTA
+constexpr int kAttnChunksMax = kTopK / kAttnSlots;   // 8
+// One attention partial (a chunk of one head half): m[32], l[32], acc[32][512] (fp32).
+constexpr size_t kPartFloats = 32 + 32 + (size_t)(kHeads / 2) * kDim;
 
 // ---------------------------------------------------------------------------
 // PTX helpers (device)

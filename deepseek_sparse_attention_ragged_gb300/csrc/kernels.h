@@ -26,14 +26,12 @@ struct IndexerParams {
     uint32_t tile_begin[DS_ROWS_MAX];
 };
 
-// Top-k: histogram, candidate collection and the per-row finish.
+// Top-k: level-0 histogram, then one 8-CTA cluster per row for the selection.
 struct TopkParams {
     const float* scores;
     uint64_t score_stride;
     int32_t* out;          // indices; entry e at out_offset[e]
-    uint32_t* hist;        // [8][2048]
-    uint32_t* ctl;         // [8][16]
-    uint64_t* cand;        // [8][kCandCap]
+    uint32_t* hist;        // [8][2048] level 0 (top 11 key bits), zero before it is built
     uint32_t* status;
     uint32_t rows;
     uint32_t total_chunks;

@@ -9,22 +9,28 @@
 //   c = key << 32 | ~index,
 // which is distinct per element, so "the best `width`" is the set of the
 // `width` largest composites, a pure function of the scores. The selection is
-// a radix select:
+// a radix select that keeps each row on chip:
 //   1. a 2048-bin histogram of the top 11 key bits per row (fused into the
 //      indexer epilogue in the decode step, or the histogram kernel here);
-//   2. one pass of CTAs over each row: from the histogram every CTA finds the
-//      bin of the width-th best score and appends the elements at or above it
-//      to a per-row candidate list (typically width + a few hundred);
-//   3. the last CTA of a row to finish (an atomic arrival counter; nothing
-//      waits) refines the threshold digit by digit (11/11/10 key bits, then
-//      the index bits, stopping as soon as a bin is taken whole), keeps the
-//      `width` winners, sorts them with a 512-wide bitonic network (warp
-//      shuffles for partners closer than 32) and writes them best first.
-// A row whose threshold bin alone overflows the candidate list falls back to
-// the same refinement over the row's full score array.
+//   2. one 8-CTA thread-block cluster per row: every CTA picks the bin of the
+//      width-th best score from the histogram, streams its slice of the row
+//      once, and appends the elements at or above that bin (typically width +
+//      a few hundred) into the leader CTA's shared memory through distributed
+//      shared memory;
+//   3. after one cluster barrier the leader refines the threshold digit by
+//      digit over its candidates (11/11/10 key bits, then the index bits,
+//      stopping as soon as a bin is taken whole), keeps the `width` winners
+//      and sorts them: 16 warp-level 32-element shuffle sorts, then four
+//      merge rounds by binary search.
+// A row whose threshold bin overflows the leader's candidate space is refined
+// by the leader from the row's full score array (correct, slower).
+
+#include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "kernels.h"
+
+namespace cg = cooperative_groups;
 
 namespace dsrows {
 
@@ -104,24 +110,13 @@ __device__ BinPick pick_bin(const uint32_t* h, uint32_t need, uint32_t* scratch)
 }
 
 
-// Element sources for the refinement: candidates in shared or global memory, or a full score row.
+// Element sources for the refinement: candidates in shared memory, or a full score row.
 struct SmemCandSource {
     const uint64_t* c;  // composites
     uint32_t n;
     __device__ __forceinline__ uint32_t size() const { return n; }
     __device__ __forceinline__ bool get(uint32_t i, uint64_t& v) const {
         v = c[i];
-        return true;
-    }
-};
-
-struct CandSource {
-    const uint64_t* cand;  // key << 32 | index
-    uint32_t n;
-    __device__ __forceinline__ uint32_t size() const { return n; }
-    __device__ __forceinline__ bool get(uint32_t i, uint64_t& c) const {
-        const uint64_t v = __ldcg(cand + i);
-        c = composite((uint32_t)(v >> 32), (uint32_t)v);
         return true;
     }
 };
@@ -138,52 +133,100 @@ struct RowSource {
     }
 };
 
-constexpr int kSmemCand = 4096;  // candidates the finishing CTA stages in shared memory
+constexpr int kCluster = 8;        // CTAs per row in the select kernel
+constexpr int kLeaderCap = 8192;   // candidates the leader CTA holds in shared memory
 
-struct FinishSmem {
-    uint32_t h[kHistBins];
+struct SelectSmem {
+    uint32_t h[kHistBins];   // level-0 histogram (each CTA), then refinement levels (leader)
     uint32_t scratch[32];
-    uint64_t cand[kSmemCand];
+    uint64_t cand[kLeaderCap];
     uint64_t sel[kTopK];
+    uint32_t ncand;
     uint32_t nsel;
 };
 
-// Sort the 512 composites of sm.sel in descending order; thread t ends with element t.
-// Bitonic network: partners closer than 32 exchange by warp shuffle, the rest through shared memory.
-__device__ __forceinline__ uint64_t bitonic_desc_512(FinishSmem& sm) {
-    const int t = threadIdx.x;
+// Where the refinement stands: the last digit level fixed, the composite
+// prefix through that level, and how many elements of that prefix are needed.
+struct Refine {
+    bool take_all;  // fewer finite scores than the width: keep them all
+    int level;
+    uint64_t prefix;
+    uint32_t need;
+    bool done;      // the prefix's whole bin is taken
+};
+
+__device__ __forceinline__ Refine refine_from_level0(const BinPick& l0, uint32_t width) {
+    Refine r;
+    r.take_all = l0.total <= width;
+    r.level = 0;
+    r.prefix = (uint64_t)(l0.bin < 0 ? 0 : l0.bin);
+    r.need = r.take_all ? 0 : width - l0.gt;
+    r.done = r.take_all || l0.eq == r.need;
+    return r;
+}
+
+// Sort the 512 distinct composites of sm.sel descending and write the winners.
+// Each warp sorts its 32 elements with a shuffle bitonic network; then four
+// merge rounds pair the sorted runs (32 -> 64 -> 128 -> 256 -> 512): an
+// element's place in the merged run is its place in its own run plus the
+// number of larger elements in the partner run (a binary search).
+__device__ __forceinline__ void sort_and_write(SelectSmem& sm, uint32_t nsel, uint32_t width, int32_t* out) {
+    const int t = threadIdx.x, lane = t & 31;
     uint64_t x = sm.sel[t];
-    for (int k = 2; k <= kTopK; k <<= 1) {
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
         for (int j = k >> 1; j > 0; j >>= 1) {
-            uint64_t y;
-            if (j >= 32) {
-                __syncthreads();
-                sm.sel[t] = x;
-                __syncthreads();
-                y = sm.sel[t ^ j];
-            } else {
-                y = __shfl_xor_sync(kFull, x, j);
-            }
-            const bool desc = (t & k) == 0;
-            const bool lower = (t & j) == 0;
+            const uint64_t y = __shfl_xor_sync(kFull, x, j);
+            const bool desc = (lane & k) == 0;
+            const bool lower = (lane & j) == 0;
             const uint64_t hi = x > y ? x : y, lo = x > y ? y : x;
             x = (lower == desc) ? hi : lo;
         }
     }
-    return x;
+    uint32_t pos = lane;  // position inside the current run
+    uint64_t* buf = sm.sel;
+#pragma unroll
+    for (int run = 32; run < kTopK; run <<= 1) {
+        __syncthreads();
+        buf[t] = x;
+        __syncthreads();
+        const uint32_t base = (uint32_t)t & ~(uint32_t)(2 * run - 1);  // start of the merged pair
+        const bool first = ((uint32_t)t & run) == 0;
+        const uint64_t* partner = buf + base + (first ? run : 0);
+        // Elements of the partner run (descending) that go before x: the larger
+        // ones, and for the second run of the pair also the equal ones (only the
+        // zero padding repeats), so that equal values keep distinct places.
+        uint32_t c = 0;
+#pragma unroll
+        for (int step = kTopK; step > 0; step >>= 1) {
+            if (step <= run && c + step <= (uint32_t)run) {
+                const uint64_t y = partner[c + step - 1];
+                if (y > x || (!first && y == x)) c += step;
+            }
+        }
+        pos += c;
+        __syncthreads();
+        buf[base + pos] = x;  // write into the merged order
+        __syncthreads();
+        x = buf[t];
+        pos = (uint32_t)t - (uint32_t)t / (2 * run) * (2 * run);  // t mod (2 run)
+    }
+    // Now thread t holds the element of rank t; zeros (padding) sort last.
+    if ((uint32_t)t < width) out[t] = (uint32_t)t < nsel ? (int32_t)(~(uint32_t)x) : -1;
 }
 
-// Refine from the level-0 pick, select the winners, sort and write them best first.
+// Refine digit by digit, select the winners, sort and write them best first.
 template <class Src>
-__device__ void finish_row(const Src& src, const BinPick& l0, uint32_t width, int32_t* out, FinishSmem& sm,
+__device__ void finish_row(const Src& src, Refine st, uint32_t width, int32_t* out, SelectSmem& sm,
                            uint32_t* status) {
     const int t = threadIdx.x, lane = t & 31;
-    const bool take_all = l0.total <= width;
-    int level = 0;
-    uint64_t prefix = (uint64_t)(l0.bin < 0 ? 0 : l0.bin);
-    uint32_t need = take_all ? 0 : width - l0.gt;
-    bool done = take_all || l0.eq == need;
-    for (int lv = 1; lv < 6 && !done; ++lv) {
+    const bool take_all = st.take_all;
+    int level = st.level;
+    uint64_t prefix = st.prefix;
+    uint32_t need = st.need;
+    bool done = st.done;
+    for (int lv = level + 1; lv < 6 && !done; ++lv) {
         const LevelSpec up = kLevels[lv - 1];
         const LevelSpec cur = kLevels[lv];
         const uint32_t mask = (1u << cur.bits) - 1;
@@ -227,8 +270,7 @@ __device__ void finish_row(const Src& src, const BinPick& l0, uint32_t width, in
     const uint32_t got = sm.nsel;
     const uint32_t nsel = got < width ? got : width;
     if (got > width && t == 0) atomicOr(status, kStatusCandOverflow);
-    const uint64_t x = bitonic_desc_512(sm);
-    if ((uint32_t)t < width) out[t] = (uint32_t)t < nsel ? (int32_t)(~(uint32_t)x) : -1;
+    sort_and_write(sm, nsel, width, out);
 }
 
 }  // namespace
@@ -260,100 +302,110 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const TopkParams p)
         if (h[i]) atomicAdd(&p.hist[(size_t)e * kHistBins + i], h[i]);
 }
 
-// Candidate collection for one chunk; the row's last CTA finishes the row.
-__global__ void __launch_bounds__(kThreads) topk_select_kernel(const TopkParams p) {
-    __shared__ FinishSmem sm;
-    __shared__ uint32_t is_last;
-    const int e = entry_of_chunk(p, blockIdx.x);
-    const uint32_t c = blockIdx.x - p.chunk_begin[e];
+// One 8-CTA cluster per row. Every CTA takes the level-0 threshold bin from
+// the row's histogram, streams its slice of the scores once, and appends the
+// candidates (finite, top 11 key bits >= that bin) and the level-1 histogram
+// of the bin straight into the leader CTA's shared memory; after one cluster
+// barrier the leader refines, sorts and writes the row.
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
+    topk_select_kernel(const TopkParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    SelectSmem& sm = *reinterpret_cast<SelectSmem*>(smem_raw);
+    cg::cluster_group cluster = cg::this_cluster();
+    const uint32_t rank = cluster.block_rank();
+    const int e = blockIdx.x / kCluster;
     const uint32_t L = p.kv_len[e];
     const uint32_t width = p.width[e];
-    const uint32_t nchunks = (L + kChunk - 1) / kChunk;
-    const uint32_t* hist = p.hist + (size_t)e * kHistBins;
-    uint32_t* ctl = p.ctl + (size_t)e * kCtlWords;
-    uint64_t* cand = p.cand + (size_t)e * kCandCap;
     const float* s = p.scores + (size_t)e * p.score_stride;
     const int t = threadIdx.x, lane = t & 31;
-    pdl_trigger();
-    pdl_wait();  // scores and histogram come from the previous kernel
+    SelectSmem& leader = *cluster.map_shared_rank(&sm, 0);
 
-    // Issue this thread's 16 score loads before anything waits on them.
-    constexpr int kPer = kChunk / kThreads;  // 16
-    const uint32_t begin = c * kChunk;
-    const uint32_t end = min(L, begin + kChunk);
+    if (t == 0) sm.ncand = 0;
+    pdl_trigger();
+    cluster.sync();  // the leader's counters are zero before anyone appends
+    pdl_wait();      // scores and histogram come from the previous kernel
+
+    // This CTA's slice: a multiple of 2048 scores (512 threads x float4).
+    const uint32_t per = (((L + kCluster - 1) / kCluster) + 2047) & ~2047u;
+    const uint32_t begin = min(L, rank * per);
+    const uint32_t end = min(L, begin + per);
     const bool vec = (reinterpret_cast<uintptr_t>(s) & 15) == 0;
-    float v[kPer];
+    constexpr int kBatch = 8;  // float4 loads in flight per thread
+    float v[kBatch * 4];
+    auto load_batch = [&](uint32_t base) {
 #pragma unroll
-    for (int i = 0; i < kPer / 4; ++i) {
-        const uint32_t j = begin + 4 * t + 4 * kThreads * i;
-        if (vec && j + 3 < end) {
-            const float4 q = __ldcg(reinterpret_cast<const float4*>(s + j));
-            v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
-        } else {
+        for (int i = 0; i < kBatch; ++i) {
+            const uint32_t j = base + 4 * t + 4 * kThreads * i;
+            if (vec && j + 3 < end) {
+                const float4 q = __ldcg(reinterpret_cast<const float4*>(s + j));
+                v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
+            } else {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) v[4 * i + u] = j + u < end ? __ldcg(s + j + u) : __int_as_float(0x7FC00000);
+                for (int u = 0; u < 4; ++u)
+                    v[4 * i + u] = j + u < end ? __ldcg(s + j + u) : __int_as_float(0x7FC00000);
+            }
         }
+    };
+    load_batch(begin);  // in flight while the threshold is picked
+    {
+        uint32_t hv[kHistBins / kThreads];
+#pragma unroll
+        for (int i = 0; i < kHistBins / kThreads; ++i) hv[i] = __ldcg(p.hist + (size_t)e * kHistBins + t + i * kThreads);
+#pragma unroll
+        for (int i = 0; i < kHistBins / kThreads; ++i) sm.h[t + i * kThreads] = hv[i];
     }
-    for (int i = t; i < kHistBins; i += kThreads) sm.h[i] = __ldcg(hist + i);
     __syncthreads();
     const BinPick l0 = pick_bin(sm.h, width, sm.scratch);
     const bool take_all = l0.total <= width;
     const uint32_t n_cand = take_all ? l0.total : l0.gt + l0.eq;
     const uint32_t b0 = take_all ? 0u : (uint32_t)l0.bin;
-    const bool fast = n_cand <= (uint32_t)kCandCap;
+    const bool fast = n_cand <= (uint32_t)kLeaderCap;
 
     if (fast) {
-        uint32_t take = 0;
+        for (uint32_t base = begin; base < end; base += kBatch * 4 * kThreads) {
+            if (base != begin) load_batch(base);
+            uint32_t take = 0;
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) take |= (finite_f(v[i]) && (score_key(v[i]) >> 21) >= b0) ? (1u << i) : 0u;
-        const uint32_t cnt = __popc(take);
-        uint32_t incl = cnt;
+            for (int i = 0; i < kBatch * 4; ++i) {
+                const bool fin = finite_f(v[i]);
+                const uint32_t key = fin ? score_key(v[i]) : 0u;
+                take |= (fin && (key >> 21) >= b0) ? (1u << i) : 0u;
+            }
+            const uint32_t cnt = __popc(take);
+            uint32_t incl = cnt;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += y;
-        }
-        const uint32_t total = __shfl_sync(kFull, incl, 31);
-        uint32_t base = 0;
-        if (lane == 31 && total) base = atomicAdd(&ctl[0], total);
-        uint32_t at = __shfl_sync(kFull, base, 31) + incl - cnt;
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const uint32_t total = __shfl_sync(kFull, incl, 31);
+            uint32_t at = 0;
+            if (lane == 31 && total) at = atomicAdd(&leader.ncand, total);
+            at = __shfl_sync(kFull, at, 31) + incl - cnt;
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-            if (take & (1u << i)) {
-                const uint32_t j = begin + 4 * t + 4 * kThreads * (i >> 2) + (i & 3);
-                if (at < (uint32_t)kCandCap) cand[at] = ((uint64_t)score_key(v[i]) << 32) | j;
-                ++at;
+            for (int i = 0; i < kBatch * 4; ++i) {
+                if (take & (1u << i)) {
+                    const uint32_t j = base + 4 * t + 4 * kThreads * (i >> 2) + (i & 3);
+                    if (at < (uint32_t)kLeaderCap) leader.cand[at] = composite(score_key(v[i]), j);
+                    ++at;
+                }
             }
         }
     }
-
-    // Arrival: the last CTA of the row sees every other CTA's candidates.
-    __threadfence();
-    __syncthreads();
-    if (t == 0) is_last = (atomicAdd(&ctl[1], 1u) == nchunks - 1) ? 1u : 0u;
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
+    cluster.sync();  // every append into the leader is visible to it
+    if (rank != 0) return;
 
     int32_t* out = p.out + p.out_offset[e];
     if (fast) {
-        const uint32_t got = __ldcg(&ctl[0]);
+        const uint32_t got = sm.ncand;
         if (got != n_cand && t == 0) atomicOr(p.status, kStatusCandOverflow);
-        const uint32_t n = got < (uint32_t)kCandCap ? got : (uint32_t)kCandCap;
         BinPick l0f = l0;
         l0f.bin = (int)b0;
-        if (n <= (uint32_t)kSmemCand) {
-            for (uint32_t i = t; i < n; i += kThreads) {
-                const uint64_t x = __ldcg(cand + i);
-                sm.cand[i] = composite((uint32_t)(x >> 32), (uint32_t)x);
-            }
-            __syncthreads();
-            finish_row(SmemCandSource{sm.cand, n}, l0f, width, out, sm, p.status);
-        } else {
-            finish_row(CandSource{cand, n}, l0f, width, out, sm, p.status);
-        }
+        const Refine st = refine_from_level0(l0f, width);
+        finish_row(SmemCandSource{sm.cand, got < (uint32_t)kLeaderCap ? got : (uint32_t)kLeaderCap}, st, width,
+                   out, sm, p.status);
     } else {
-        finish_row(RowSource{s, L}, l0, width, out, sm, p.status);
+        finish_row(RowSource{s, L}, refine_from_level0(l0, width), width, out, sm, p.status);
     }
 }
 
@@ -365,8 +417,15 @@ cudaError_t launch_topk_hist(const TopkParams& p, cudaStream_t stream, bool pdl)
 }
 
 cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t stream, bool pdl) {
-    if (p.total_chunks == 0) return cudaSuccess;
-    return launch_kernel(topk_select_kernel, dim3(p.total_chunks), dim3(kThreads), 0, stream, pdl, p);
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t err = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)sizeof(SelectSmem));
+        if (err != cudaSuccess) return err;
+        configured = true;
+    }
+    return launch_kernel(topk_select_kernel, dim3(p.rows * kCluster), dim3(kThreads), sizeof(SelectSmem), stream,
+                         pdl, p);
 }
 
 __global__ void __launch_bounds__(1024) clear_kernel(uint32_t* __restrict__ p, uint32_t words) {
@@ -375,7 +434,7 @@ __global__ void __launch_bounds__(1024) clear_kernel(uint32_t* __restrict__ p, u
 }
 
 cudaError_t launch_clear(uint32_t* p, uint32_t words, cudaStream_t stream) {
-    return launch_kernel(clear_kernel, dim3(4), dim3(1024), 0, stream, false, p, words);
+    return launch_kernel(clear_kernel, dim3(16), dim3(1024), 0, stream, false, p, words);
 }
 
 }  // namespace dsrows

@@ -132,7 +132,7 @@ int ds_rows_topk(const ds_row_set_t* set, const float* scores, size_t score_stri
  * ds_rows_topk computes (same arguments, bitwise the same indices) but keeps
  * its scratch in one fixed array inside the library instead of a
  * caller-provided workspace, and allocates nothing.
- *   - Size: the array holds DS_TOPK_STATIC_SCRATCH_BYTES bytes (about 1.1 MB),
+ *   - Size: the array holds DS_TOPK_STATIC_SCRATCH_BYTES bytes (about 64 KiB),
  *     enough for DS_ROWS_MAX rows of any kv_len; every GPU that loads the
  *     library keeps it until the process exits. A table needing more is
  *     rejected with DS_ESIZE (more than DS_ROWS_MAX rows is DS_EINVAL).
@@ -144,7 +144,7 @@ int ds_rows_topk(const ds_row_set_t* set, const float* scores, size_t score_stri
  *     Calls that overlap on the GPU (different streams, no ordering between
  *     them) race on the array and give wrong results: order them.
  */
-#define DS_TOPK_STATIC_SCRATCH_BYTES 1114880
+#define DS_TOPK_STATIC_SCRATCH_BYTES 65792
 int ds_rows_topk_static(const ds_row_set_t* set, const float* scores, size_t score_stride,
                         int32_t* indices, void* stream);
 

@@ -219,6 +219,22 @@ def config_kv_lens(i: int) -> List[int]:
     raise ValueError(f"no config {i}")
 
 
+def draw_queries(wl: Workload, seed: int):
+    """Another set of queries for the same caches, drawn with the workload's recipe:
+    (q_index uint16 [Q,64,128], w_index float32 [Q,64], q_attn uint16 [Q,64,512])."""
+    rng = np.random.default_rng(seed)
+    Q = wl.q_index.shape[0]
+    if wl.integer_valued:
+        qI = _int_bf16(rng, (Q, HEADS, INDEX_DIM))
+        wI = rng.integers(-3, 3, endpoint=True, size=(Q, HEADS)).astype(np.float32)
+        qA = _int_bf16(rng, (Q, HEADS, KV_DIM))
+    else:
+        qI = _normal_bf16(rng, (Q, HEADS, INDEX_DIM))
+        wI = rng.standard_normal(size=(Q, HEADS), dtype=np.float32) / np.float32(8.0)
+        qA = _normal_bf16(rng, (Q, HEADS, KV_DIM))
+    return qI, wI, qA
+
+
 # ---------------------------------------------------------------------------
 # Stand-alone stage inputs (scores for the top-k stage, indices for attention)
 # ---------------------------------------------------------------------------
