@@ -205,7 +205,7 @@ int run_indexer(const ds_row_set_t* set, const ds_bf16* q_index, const float* w_
 }
 
 int run_topk(const ds_row_set_t* set, const float* scores, uint64_t stride, int32_t* out, const uint32_t* out_offset,
-             uint8_t* ws, const Layout& L, bool with_hist, cudaStream_t stream) {
+             uint8_t* ws, const Layout& L, bool with_hist, bool by_index, cudaStream_t stream) {
     TopkParams p;
     std::memset(&p, 0, sizeof(p));
     const uint32_t chunk = topk_chunk();
@@ -223,6 +223,7 @@ int run_topk(const ds_row_set_t* set, const float* scores, uint64_t stride, int3
     p.hist = reinterpret_cast<uint32_t*>(ws + L.hist);
     p.status = reinterpret_cast<uint32_t*>(ws + L.status);
     p.rows = (uint32_t)set->rows;
+    p.order_by_index = by_index ? 1u : 0u;
     p.total_chunks = chunks;
     cudaError_t err = cudaSuccess;
     if (with_hist) {
@@ -235,7 +236,8 @@ int run_topk(const ds_row_set_t* set, const float* scores, uint64_t stride, int3
 
 int run_attention(const ds_row_set_t* set, const ds_bf16* q_attn, const float* sinks, size_t sinks_row_stride,
                   const int32_t* indices, const uint32_t* index_offset, float scale, ds_bf16* out,
-                  uint32_t* invalid, uint8_t* ws, const Layout& L, cudaStream_t stream) {
+                  uint32_t* invalid, uint8_t* ws, const Layout& L, cudaStream_t stream,
+                  const float* scores = nullptr, uint64_t score_stride = 0, int32_t* sorted_out = nullptr) {
     AttnParams p;
     std::memset(&p, 0, sizeof(p));
     uint32_t chunks = 0;
@@ -261,6 +263,10 @@ int run_attention(const ds_row_set_t* set, const ds_bf16* q_attn, const float* s
     p.scale = scale;
     p.rows = (uint32_t)set->rows;
     p.total_chunks = chunks;
+    p.scores = scores;
+    p.score_stride = score_stride;
+    p.sorted_out = sorted_out;
+    for (int e = 0; e < set->rows; ++e) p.sorted_offset[e] = set->table[e].index_offset;
     cudaError_t err = launch_attention(p, stream, true);
     return err == cudaSuccess ? DS_OK : cuda_fail(err, "attention launch");
 }
@@ -365,7 +371,7 @@ int ds_rows_topk(const ds_row_set_t* set, const float* scores, size_t score_stri
     if (err != cudaSuccess) return cuda_fail(err, "workspace clear");
     uint32_t off[DS_ROWS_MAX];
     for (int e = 0; e < set->rows; ++e) off[e] = set->table[e].index_offset;
-    return run_topk(set, scores, score_stride, indices, off, ws, L, true, s);
+    return run_topk(set, scores, score_stride, indices, off, ws, L, true, false, s);
 }
 
 int ds_rows_sparse_attn(const ds_row_set_t* set, const ds_bf16* q_attn, const float* sinks,
@@ -409,13 +415,17 @@ int ds_rows_decode(const ds_row_set_t* set, const ds_bf16* q_index, const float*
     uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
     rc = run_indexer(set, q_index, w_index, scores, L.score_stride, hist, status, s, true);
     if (rc) return rc;
-    int32_t* idx = indices;
+    // The selection goes to the workspace in ascending index order (the step's
+    // canonical order, no sort on the critical path); attention reads it there,
+    // and when the caller asks for indices, extra CTAs of the attention kernel
+    // write them best first.
+    int32_t* sel = reinterpret_cast<int32_t*>(ws + L.topk);
     uint32_t off[DS_ROWS_MAX];
-    for (int e = 0; e < set->rows; ++e) off[e] = indices ? set->table[e].index_offset : (uint32_t)(e * DS_TOPK);
-    if (!idx) idx = reinterpret_cast<int32_t*>(ws + L.topk);
-    rc = run_topk(set, scores, L.score_stride, idx, off, ws, L, false, s);
+    for (int e = 0; e < set->rows; ++e) off[e] = (uint32_t)(e * DS_TOPK);
+    rc = run_topk(set, scores, L.score_stride, sel, off, ws, L, false, true, s);
     if (rc) return rc;
-    return run_attention(set, q_attn, sinks, sinks_row_stride, idx, off, scale, out, invalid, ws, L, s);
+    return run_attention(set, q_attn, sinks, sinks_row_stride, sel, off, scale, out, invalid, ws, L, s, scores,
+                         L.score_stride, indices);
 }
 
 int ds_rows_topk_static(const ds_row_set_t* set, const float* scores, size_t score_stride, int32_t* indices,
@@ -442,7 +452,7 @@ int ds_rows_topk_static(const ds_row_set_t* set, const float* scores, size_t sco
     if (err != cudaSuccess) return cuda_fail(err, "scratch clear");
     uint32_t off[DS_ROWS_MAX];
     for (int e = 0; e < set->rows; ++e) off[e] = set->table[e].index_offset;
-    return run_topk(set, scores, score_stride, indices, off, ws, L, true, s);
+    return run_topk(set, scores, score_stride, indices, off, ws, L, true, false, s);
 }
 
 const char* ds_rows_last_error(void) { return g_error.c_str(); }

@@ -96,6 +96,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_partial_kernel(const AttnPar
     int* idx_s = reinterpret_cast<int*>(smem + SmemLayout::idx);
 
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    if (blockIdx.x >= 2 * p.total_chunks) {
+        // Best-first indices for the caller, off the critical path: this CTA
+        // orders row e's selection (ascending index) by (score desc, index asc).
+        const int e = (int)(blockIdx.x - 2 * p.total_chunks);
+        const uint32_t W = p.width[e];
+        pdl_trigger();
+        pdl_wait();  // the selection and the scores come from the previous kernels
+        const float* sc = p.scores + (size_t)e * p.score_stride;
+        uint64_t x[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const uint32_t slot = t + q * kThreads;
+            const int j = slot < W ? __ldcg(p.indices + p.index_offset[e] + slot) : -1;
+            x[q] = j >= 0 ? composite(score_key(__ldcg(sc + j)), (uint32_t)j) : 0ull;
+        }
+        sort512_desc<kThreads>(x, reinterpret_cast<uint64_t*>(smem));
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const uint32_t slot = t + q * kThreads;
+            if (slot < W) p.sorted_out[p.sorted_offset[e] + slot] = x[q] ? (int32_t)(~(uint32_t)x[q]) : -1;
+        }
+        return;
+    }
     const int e = entry_of_cta(p, blockIdx.x);
     const uint32_t W = p.width[e];
     const uint32_t nchunks = (W + kSlots - 1) / kSlots;
@@ -345,8 +368,9 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream, bool pdl)
         configured = true;
     }
     if (p.total_chunks == 0) return cudaSuccess;
-    cudaError_t err = launch_kernel(attn_partial_kernel, dim3(2 * p.total_chunks), dim3(kThreads), kSmemBytes,
-                                    stream, pdl, p);
+    const uint32_t sort_ctas = p.sorted_out ? p.rows : 0u;
+    cudaError_t err = launch_kernel(attn_partial_kernel, dim3(2 * p.total_chunks + sort_ctas), dim3(kThreads),
+                                    kSmemBytes, stream, pdl, p);
     if (err != cudaSuccess) return err;
     return launch_kernel(attn_combine_kernel, dim3(p.rows * 2 * kCombineBlocks), dim3(256), 0, stream, true, p);
 }

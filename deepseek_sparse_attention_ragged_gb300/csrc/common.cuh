@@ -32,7 +32,7 @@ constexpr uint64_t kWaitBudgetNs = 2000000000ull;
 //   [0, 256)                 control: u32 status, u32 pad...
 //   hist   [8][2048] u32     level-0 histogram of score keys per entry
 //   flags  [8][64]  u32      per-entry, per-head attention invalid bits
-//   topk   [8][512] i32      selected indices (decode without an indices output)
+//   topk   [8][512] i32      the decode's selection (ascending index order)
 //   part   [chunks][...]     attention partials
 //   scores [8][stride] f32   indexer scores (decode only)
 constexpr int kHistBins = 2048;
@@ -226,6 +226,72 @@ inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Sort 512 64-bit values in descending order with NT = 256 or 512 threads;
+// thread t holds the values of positions t + k NT in x[k]; `buf` is 512 words
+// of shared memory. Zero may repeat (padding); other values must be distinct.
+// Each warp sorts 32-value runs with a shuffle bitonic network; four merge
+// rounds then pair the sorted runs (32 -> 64 -> 128 -> 256 -> 512): a value's
+// place in the merged run is its place in its own run plus the partner run's
+// values that go before it (a binary search). On return x[k] is the value of
+// rank t + k NT.
+template <int NT>
+__device__ __forceinline__ void sort512_desc(uint64_t (&x)[512 / NT], uint64_t* buf) {
+    constexpr int PER = 512 / NT;
+    const int t = threadIdx.x, lane = t & 31;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+#pragma unroll
+        for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                const uint64_t y = __shfl_xor_sync(0xFFFFFFFFu, x[q], j);
+                const bool desc = (lane & k) == 0;
+                const bool lower = (lane & j) == 0;
+                const uint64_t hi = x[q] > y ? x[q] : y, lo = x[q] > y ? y : x[q];
+                x[q] = (lower == desc) ? hi : lo;
+            }
+        }
+    }
+    uint32_t pos[PER];
+#pragma unroll
+    for (int q = 0; q < PER; ++q) pos[q] = lane;  // place inside the current run
+#pragma unroll
+    for (int run = 32; run < 512; run <<= 1) {
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < PER; ++q) buf[t + q * NT] = x[q];
+        __syncthreads();
+        uint32_t dst[PER];
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+            const uint32_t p = (uint32_t)(t + q * NT);
+            const uint32_t base = p & ~(uint32_t)(2 * run - 1);
+            const bool first = (p & run) == 0;
+            const uint64_t* partner = buf + base + (first ? run : 0);
+            // Partner values that go before x: the larger ones, and for the second
+            // run of the pair also the equal ones, so equal values keep distinct places.
+            uint32_t c = 0;
+#pragma unroll
+            for (int step = 512; step > 0; step >>= 1) {
+                if (step <= run && c + step <= (uint32_t)run) {
+                    const uint64_t y = partner[c + step - 1];
+                    if (y > x[q] || (!first && y == x[q])) c += step;
+                }
+            }
+            dst[q] = base + pos[q] + c;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < PER; ++q) buf[dst[q]] = x[q];
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+            x[q] = buf[t + q * NT];
+            pos[q] = (uint32_t)(t + q * NT) & (uint32_t)(2 * run - 1);
+        }
+    }
+}
+
 // Order-preserving map of a finite fp32 score to u32 (larger score -> larger key);
 // -0.0 maps like +0.0 so that the two tie.
 __device__ __forceinline__ uint32_t score_key(float s) {
@@ -235,5 +301,10 @@ __device__ __forceinline__ uint32_t score_key(float s) {
 }
 
 __device__ __forceinline__ bool finite_f(float x) { return (__float_as_uint(x) & 0x7F800000u) != 0x7F800000u; }
+
+// The composite that orders (score desc, index asc) as one descending u64.
+__device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t index) {
+    return ((uint64_t)key << 32) | (uint64_t)(~index);
+}
 
 }  // namespace dsrows

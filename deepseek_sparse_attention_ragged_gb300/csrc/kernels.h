@@ -34,7 +34,8 @@ struct TopkParams {
     uint32_t* hist;        // [8][2048] level 0 (top 11 key bits), zero before it is built
     uint32_t* status;
     uint32_t rows;
-    uint32_t total_chunks;
+    uint32_t order_by_index;  // 0: best first; 1: ascending index (the decode's canonical order)
+    uint32_t total_chunks;    // histogram CTAs (chunks of topk_chunk() scores)
     uint32_t kv_len[DS_ROWS_MAX];
     uint32_t width[DS_ROWS_MAX];
     uint32_t out_offset[DS_ROWS_MAX];
@@ -61,6 +62,12 @@ struct AttnParams {
     uint32_t index_offset[DS_ROWS_MAX];
     uint32_t q_row[DS_ROWS_MAX];
     uint32_t chunk_begin[DS_ROWS_MAX];  // first attention chunk of each row
+    // Optional best-first copy of the indices (decode): one extra CTA per row
+    // sorts the row's selection by its scores into sorted_out.
+    const float* scores;
+    uint64_t score_stride;
+    int32_t* sorted_out;
+    uint32_t sorted_offset[DS_ROWS_MAX];
 };
 
 size_t indexer_smem_bytes();

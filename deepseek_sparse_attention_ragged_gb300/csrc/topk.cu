@@ -25,6 +25,7 @@
 // A row whose threshold bin overflows the leader's candidate space is refined
 // by the leader from the row's full score array (correct, slower).
 
+#include <cfloat>
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -53,10 +54,6 @@ __device__ __forceinline__ int entry_of_chunk(const TopkParams& p, uint32_t c) {
     for (int i = 1; i < kRowsMax; ++i)
         if (i < (int)p.rows && c >= p.chunk_begin[i]) e = i;
     return e;
-}
-
-__device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t index) {
-    return ((uint64_t)key << 32) | (uint64_t)(~index);
 }
 
 struct BinPick {
@@ -135,6 +132,7 @@ struct RowSource {
 
 constexpr int kCluster = 8;        // CTAs per row in the select kernel
 constexpr int kLeaderCap = 8192;   // candidates the leader CTA holds in shared memory
+constexpr int kBitmapWords = kLeaderCap * 2;  // the candidate space as a bitmap: rows up to 524288 keys
 
 struct SelectSmem {
     uint32_t h[kHistBins];   // level-0 histogram (each CTA), then refinement levels (leader)
@@ -165,61 +163,63 @@ __device__ __forceinline__ Refine refine_from_level0(const BinPick& l0, uint32_t
     return r;
 }
 
-// Sort the 512 distinct composites of sm.sel descending and write the winners.
-// Each warp sorts its 32 elements with a shuffle bitonic network; then four
-// merge rounds pair the sorted runs (32 -> 64 -> 128 -> 256 -> 512): an
-// element's place in the merged run is its place in its own run plus the
-// number of larger elements in the partner run (a binary search).
-__device__ __forceinline__ void sort_and_write(SelectSmem& sm, uint32_t nsel, uint32_t width, int32_t* out) {
-    const int t = threadIdx.x, lane = t & 31;
-    uint64_t x = sm.sel[t];
+// Write the nsel winners of sm.sel (composites) to out[0, width), then -1.
+// Best first: sorted by composite. Index order (ascending): through a bitmap of
+// the row's L positions in the candidate space when it fits, else sorted by index.
+__device__ __forceinline__ void write_winners(SelectSmem& sm, uint32_t nsel, uint32_t width, uint32_t L,
+                                              bool by_index, int32_t* out) {
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const uint32_t words = (L + 31) / 32;
+    if (!by_index || words > (uint32_t)kBitmapWords) {
+        const uint64_t c = sm.sel[t];
+        // Best first: the composite. Index order: its low word ~index, larger for a
+        // lower index (zero stays the padding). Either way ~(low word) is the index.
+        uint64_t x[1] = {by_index ? (uint64_t)(uint32_t)c : c};
+        sort512_desc<kThreads>(x, sm.sel);
+        if ((uint32_t)t < width) out[t] = (uint32_t)t < nsel ? (int32_t)(~(uint32_t)x[0]) : -1;
+        return;
+    }
+    uint32_t* bm = reinterpret_cast<uint32_t*>(sm.cand);  // the candidates are consumed
+    for (uint32_t w = t; w < words; w += kThreads) bm[w] = 0;
+    __syncthreads();
+    if ((uint32_t)t < nsel) {
+        const uint32_t j = ~(uint32_t)sm.sel[t];
+        atomicOr(&bm[j >> 5], 1u << (j & 31));
+    }
+    __syncthreads();
+    // Each thread owns a contiguous run of words; a block scan of the run
+    // popcounts gives every set bit its place.
+    const uint32_t per = (words + kThreads - 1) / kThreads;
+    const uint32_t w0 = min(words, t * per), w1 = min(words, w0 + per);
+    uint32_t cnt = 0;
+    for (uint32_t w = w0; w < w1; ++w) cnt += __popc(bm[w]);
+    uint32_t incl = cnt;
 #pragma unroll
-    for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            const uint64_t y = __shfl_xor_sync(kFull, x, j);
-            const bool desc = (lane & k) == 0;
-            const bool lower = (lane & j) == 0;
-            const uint64_t hi = x > y ? x : y, lo = x > y ? y : x;
-            x = (lower == desc) ? hi : lo;
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) sm.scratch[warp] = incl;
+    __syncthreads();
+    uint32_t before = 0;
+    for (int w = 0; w < warp; ++w) before += sm.scratch[w];
+    uint32_t at = before + incl - cnt;
+    for (uint32_t w = w0; w < w1; ++w) {
+        uint32_t bits = bm[w];
+        while (bits) {
+            const int b = __ffs(bits) - 1;
+            bits &= bits - 1;
+            if (at < width) out[at] = (int32_t)(32 * w + b);
+            ++at;
         }
     }
-    uint32_t pos = lane;  // position inside the current run
-    uint64_t* buf = sm.sel;
-#pragma unroll
-    for (int run = 32; run < kTopK; run <<= 1) {
-        __syncthreads();
-        buf[t] = x;
-        __syncthreads();
-        const uint32_t base = (uint32_t)t & ~(uint32_t)(2 * run - 1);  // start of the merged pair
-        const bool first = ((uint32_t)t & run) == 0;
-        const uint64_t* partner = buf + base + (first ? run : 0);
-        // Elements of the partner run (descending) that go before x: the larger
-        // ones, and for the second run of the pair also the equal ones (only the
-        // zero padding repeats), so that equal values keep distinct places.
-        uint32_t c = 0;
-#pragma unroll
-        for (int step = kTopK; step > 0; step >>= 1) {
-            if (step <= run && c + step <= (uint32_t)run) {
-                const uint64_t y = partner[c + step - 1];
-                if (y > x || (!first && y == x)) c += step;
-            }
-        }
-        pos += c;
-        __syncthreads();
-        buf[base + pos] = x;  // write into the merged order
-        __syncthreads();
-        x = buf[t];
-        pos = (uint32_t)t - (uint32_t)t / (2 * run) * (2 * run);  // t mod (2 run)
-    }
-    // Now thread t holds the element of rank t; zeros (padding) sort last.
-    if ((uint32_t)t < width) out[t] = (uint32_t)t < nsel ? (int32_t)(~(uint32_t)x) : -1;
+    for (uint32_t k = nsel + t; k < width; k += kThreads) out[k] = -1;
 }
 
 // Refine digit by digit, select the winners, sort and write them best first.
 template <class Src>
-__device__ void finish_row(const Src& src, Refine st, uint32_t width, int32_t* out, SelectSmem& sm,
-                           uint32_t* status) {
+__device__ void finish_row(const Src& src, Refine st, uint32_t width, uint32_t L, bool by_index, int32_t* out,
+                           SelectSmem& sm, uint32_t* status) {
     const int t = threadIdx.x, lane = t & 31;
     const bool take_all = st.take_all;
     int level = st.level;
@@ -270,7 +270,7 @@ __device__ void finish_row(const Src& src, Refine st, uint32_t width, int32_t* o
     const uint32_t got = sm.nsel;
     const uint32_t nsel = got < width ? got : width;
     if (got > width && t == 0) atomicOr(status, kStatusCandOverflow);
-    sort_and_write(sm, nsel, width, out);
+    write_winners(sm, nsel, width, L, by_index, out);
 }
 
 }  // namespace
@@ -362,15 +362,19 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     const bool fast = n_cand <= (uint32_t)kLeaderCap;
 
     if (fast) {
+        // The smallest score whose key falls in bin b0: for finite scores,
+        // key >= b0 << 21 is the same as score >= this value (-0.0 ties +0.0).
+        float thr = -FLT_MAX;
+        if (!take_all) {
+            const uint32_t k0 = b0 << 21;
+            const float f = __uint_as_float((k0 & 0x80000000u) ? (k0 & 0x7FFFFFFFu) : ~k0);
+            if (finite_f(f)) thr = f;
+        }
         for (uint32_t base = begin; base < end; base += kBatch * 4 * kThreads) {
             if (base != begin) load_batch(base);
             uint32_t take = 0;
 #pragma unroll
-            for (int i = 0; i < kBatch * 4; ++i) {
-                const bool fin = finite_f(v[i]);
-                const uint32_t key = fin ? score_key(v[i]) : 0u;
-                take |= (fin && (key >> 21) >= b0) ? (1u << i) : 0u;
-            }
+            for (int i = 0; i < kBatch * 4; ++i) take |= (v[i] >= thr && v[i] < INFINITY) ? (1u << i) : 0u;
             const uint32_t cnt = __popc(take);
             uint32_t incl = cnt;
 #pragma unroll
@@ -402,12 +406,14 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
         BinPick l0f = l0;
         l0f.bin = (int)b0;
         const Refine st = refine_from_level0(l0f, width);
-        finish_row(SmemCandSource{sm.cand, got < (uint32_t)kLeaderCap ? got : (uint32_t)kLeaderCap}, st, width,
-                   out, sm, p.status);
+        finish_row(SmemCandSource{sm.cand, got < (uint32_t)kLeaderCap ? got : (uint32_t)kLeaderCap}, st, width, L,
+                   p.order_by_index != 0, out, sm, p.status);
     } else {
-        finish_row(RowSource{s, L}, refine_from_level0(l0, width), width, out, sm, p.status);
+        finish_row(RowSource{s, L}, refine_from_level0(l0, width), width, L, p.order_by_index != 0, out, sm,
+                   p.status);
     }
 }
+
 
 uint32_t topk_chunk() { return kChunk; }
 

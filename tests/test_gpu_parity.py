@@ -259,8 +259,11 @@ def test_joint_equals_single_row(i):
 
 
 def test_decode_stages_agree():
-    """decode == indexer_score -> topk -> sparse_attn, bitwise, and the top-k is
-    exactly the top-width of the GPU's own scores."""
+    """decode == indexer_score -> topk -> sparse_attn, bitwise. The decode's
+    indices output equals ds_rows_topk's (best first); its attention takes the
+    selection in ascending index order (the step's canonical order), so the
+    stand-alone attention is given the same order. The top-k is exactly the
+    top-width of the GPU's own scores."""
     wl, dev = cfg(2), cfg_dev(2)
     out, idx, _ = run_decode(dev)
     stride = max(r.kv_len for r in wl.rows)
@@ -268,10 +271,18 @@ def test_decode_stages_agree():
     ds.ds_rows_indexer_score(dev.rows, dev.q_index, dev.w_index, dev.keys, scores, stride)
     idx2 = torch.full_like(idx, -7)
     ds.ds_rows_topk(dev.rows, scores, stride, idx2, ds.workspace(dev.rows))
-    out2 = torch.full_like(out, float("nan"))
-    ds.ds_rows_sparse_attn(dev.rows, dev.q_attn, dev.sinks, dev.sinks_row_stride, idx2, dev.scale, out2, dev.kv)
     torch.cuda.synchronize()
     assert torch.equal(idx, idx2)
+    by_index = idx2.cpu().numpy().copy()
+    for r in wl.rows:
+        seg = by_index[r.index_offset: r.index_offset + r.width]
+        live = np.sort(seg[seg >= 0])
+        seg[:] = -1
+        seg[: len(live)] = live
+    out2 = torch.full_like(out, float("nan"))
+    ds.ds_rows_sparse_attn(dev.rows, dev.q_attn, dev.sinks, dev.sinks_row_stride, torch.from_numpy(by_index).cuda(),
+                           dev.scale, out2, dev.kv)
+    torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
     s = scores.cpu().numpy()
     for e, r in enumerate(wl.rows):
