@@ -361,7 +361,7 @@ def main():
                          "bytes_per_launch": idx_bytes, "ms_per_launch": idx_ms},
             "e2e": {"value": world * R / (e2e_ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": 5 * args.steps,
+            "gpu_launches": 3 * args.steps,
             "clocks": clocks.summary(),
             "cpu_baseline": cb,
         }

@@ -236,8 +236,7 @@ int run_topk(const ds_row_set_t* set, const float* scores, uint64_t stride, int3
 
 int run_attention(const ds_row_set_t* set, const ds_bf16* q_attn, const float* sinks, size_t sinks_row_stride,
                   const int32_t* indices, const uint32_t* index_offset, float scale, ds_bf16* out,
-                  uint32_t* invalid, uint8_t* ws, const Layout& L, cudaStream_t stream,
-                  const float* scores = nullptr, uint64_t score_stride = 0, int32_t* sorted_out = nullptr) {
+                  uint32_t* invalid, uint8_t* ws, const Layout& L, cudaStream_t stream) {
     AttnParams p;
     std::memset(&p, 0, sizeof(p));
     uint32_t chunks = 0;
@@ -263,10 +262,6 @@ int run_attention(const ds_row_set_t* set, const ds_bf16* q_attn, const float* s
     p.scale = scale;
     p.rows = (uint32_t)set->rows;
     p.total_chunks = chunks;
-    p.scores = scores;
-    p.score_stride = score_stride;
-    p.sorted_out = sorted_out;
-    for (int e = 0; e < set->rows; ++e) p.sorted_offset[e] = set->table[e].index_offset;
     cudaError_t err = launch_attention(p, stream, true);
     return err == cudaSuccess ? DS_OK : cuda_fail(err, "attention launch");
 }
@@ -415,17 +410,38 @@ int ds_rows_decode(const ds_row_set_t* set, const ds_bf16* q_index, const float*
     uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
     rc = run_indexer(set, q_index, w_index, scores, L.score_stride, hist, status, s, true);
     if (rc) return rc;
-    // The selection goes to the workspace in ascending index order (the step's
-    // canonical order, no sort on the critical path); attention reads it there,
-    // and when the caller asks for indices, extra CTAs of the attention kernel
-    // write them best first.
-    int32_t* sel = reinterpret_cast<int32_t*>(ws + L.topk);
-    uint32_t off[DS_ROWS_MAX];
-    for (int e = 0; e < set->rows; ++e) off[e] = (uint32_t)(e * DS_TOPK);
-    rc = run_topk(set, scores, L.score_stride, sel, off, ws, L, false, true, s);
-    if (rc) return rc;
-    return run_attention(set, q_attn, sinks, sinks_row_stride, sel, off, scale, out, invalid, ws, L, s, scores,
-                         L.score_stride, indices);
+    // Selection and attention in one kernel: one 8-CTA cluster per row keeps the
+    // selection on chip and attends over it in best-first order, the order of
+    // the indices it writes for the caller.
+    TailParams tp;
+    std::memset(&tp, 0, sizeof(tp));
+    uint32_t chunks = 0;
+    for (int e = 0; e < set->rows; ++e) {
+        const ds_row_t& r = set->table[e];
+        tp.kv[e] = reinterpret_cast<const __nv_bfloat16*>(set->kv[e]);
+        tp.kv_len[e] = r.kv_len;
+        tp.width[e] = r.width;
+        tp.index_offset[e] = r.index_offset;
+        tp.q_row[e] = r.q_row;
+        tp.chunk_begin[e] = chunks;
+        chunks += (r.width + kAttnSlots - 1) / kAttnSlots;
+    }
+    tp.part = reinterpret_cast<float*>(ws + L.part);
+    tp.flags = reinterpret_cast<uint32_t*>(ws + L.flags);
+    tp.scores = scores;
+    tp.score_stride = L.score_stride;
+    tp.hist = hist;
+    tp.status = status;
+    tp.q = reinterpret_cast<const __nv_bfloat16*>(q_attn);
+    tp.sinks = sinks;
+    tp.sinks_row_stride = sinks_row_stride;
+    tp.out = reinterpret_cast<__nv_bfloat16*>(out);
+    tp.invalid = invalid;
+    tp.indices = indices;
+    tp.scale = scale;
+    tp.rows = (uint32_t)set->rows;
+    err = launch_decode_tail(tp, s, true);
+    return err == cudaSuccess ? DS_OK : cuda_fail(err, "decode select + attention launch");
 }
 
 int ds_rows_topk_static(const ds_row_set_t* set, const float* scores, size_t score_stride, int32_t* indices,

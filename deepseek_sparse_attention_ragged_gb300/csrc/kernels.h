@@ -62,12 +62,30 @@ struct AttnParams {
     uint32_t index_offset[DS_ROWS_MAX];
     uint32_t q_row[DS_ROWS_MAX];
     uint32_t chunk_begin[DS_ROWS_MAX];  // first attention chunk of each row
-    // Optional best-first copy of the indices (decode): one extra CTA per row
-    // sorts the row's selection by its scores into sorted_out.
-    const float* scores;
+};
+
+// The decode after the indexer: selection + attention, one 8-CTA cluster per row.
+struct TailParams {
+    const float* scores;          // indexer scores, entry e at e * score_stride
     uint64_t score_stride;
-    int32_t* sorted_out;
-    uint32_t sorted_offset[DS_ROWS_MAX];
+    const uint32_t* hist;         // [8][2048] level-0 histogram built by the indexer
+    uint32_t* status;
+    const __nv_bfloat16* kv[DS_ROWS_MAX];
+    const __nv_bfloat16* q;       // [Q, 64, 512]
+    const float* sinks;
+    uint64_t sinks_row_stride;
+    float* part;                  // chunk partials: m[64], l[64], acc[64][512] per chunk
+    uint32_t* flags;              // [8][64] head flags, zero on entry
+    __nv_bfloat16* out;           // [Q, 64, 512]
+    uint32_t* invalid;            // optional [Q, 64]
+    int32_t* indices;             // optional best-first selection, entry e at index_offset[e]
+    float scale;
+    uint32_t rows;
+    uint32_t kv_len[DS_ROWS_MAX];
+    uint32_t width[DS_ROWS_MAX];
+    uint32_t index_offset[DS_ROWS_MAX];
+    uint32_t q_row[DS_ROWS_MAX];
+    uint32_t chunk_begin[DS_ROWS_MAX];  // first 64-slot chunk of each row
 };
 
 size_t indexer_smem_bytes();
@@ -83,5 +101,8 @@ cudaError_t launch_clear(uint32_t* p, uint32_t words, cudaStream_t stream);
 
 // Partial kernel (PDL on the previous kernel when `pdl`), then the combine kernel (PDL).
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream, bool pdl);
+
+size_t decode_tail_smem_bytes();
+cudaError_t launch_decode_tail(const TailParams& p, cudaStream_t stream, bool pdl);
 
 }  // namespace dsrows
