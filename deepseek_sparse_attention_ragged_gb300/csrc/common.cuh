@@ -29,7 +29,7 @@ constexpr uint64_t kWaitBudgetNs = 2000000000ull;
 // ---------------------------------------------------------------------------
 // Workspace layout (bytes, all 256-aligned)
 // ---------------------------------------------------------------------------
-//   [0, 256)                 control: u32 status, u32 pad...
+//   [0, 256)                 control: u32 status, pad
 //   hist   [8][2048] u32     level-0 histogram of score keys per entry
 //   flags  [8][64]  u32      per-entry, per-head attention invalid bits
 //   topk   [8][512] i32      the decode's selection (ascending index order)

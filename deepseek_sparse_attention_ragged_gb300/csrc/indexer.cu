@@ -9,7 +9,8 @@
 // (M=128, N=64, K=128 as 8 steps of 16). Operands sit in shared memory in the
 // 128-byte-swizzled K-major layout written by TMA. The epilogue gives each
 // thread one key (one TMEM lane): it reads the key's 64 head dot products and
-// sums relu(x_h) * w_h in head order, so the score of a key depends only on
+// sums relu(x_h) * w_h as four interleaved partial sums (heads h = i mod 4,
+// each in head order) added pairwise, so the score of a key depends only on
 // the key's data and the query (bitwise, wherever the tile sits).
 //
 // Warp roles (192 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
@@ -251,9 +252,11 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_score_kernel(const __grid
             if (lane == 0) mbar_arrive(&bar->acc_empty[a]);
 
             const float* w = w_s + e * kIdxHeads;
-            float s = 0.0f;
+            // Four independent chains: a quarter of the dependent FMA latency.
+            float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-            for (int h = 0; h < kIdxHeads; ++h) s = fmaf(relu_nan(__uint_as_float(v[h])), w[h], s);
+            for (int h = 0; h < kIdxHeads; ++h) s4[h & 3] = fmaf(relu_nan(__uint_as_float(v[h])), w[h], s4[h & 3]);
+            const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
             const uint32_t j = tile * kTileKeys + quarter * 32 + lane;
             if (j < p.kv_len[e]) {
                 const bool fin = finite_f(s);
