@@ -234,36 +234,41 @@ int run_topk(const ds_row_set_t* set, const float* scores, uint64_t stride, int3
     return err == cudaSuccess ? DS_OK : cuda_fail(err, "top-k select launch");
 }
 
-int run_attention(const ds_row_set_t* set, const ds_bf16* q_attn, const float* sinks, size_t sinks_row_stride,
-                  const int32_t* indices, const uint32_t* index_offset, float scale, ds_bf16* out,
-                  uint32_t* invalid, uint8_t* ws, const Layout& L, cudaStream_t stream) {
-    AttnParams p;
-    std::memset(&p, 0, sizeof(p));
+// Selection (decode: `given` null) or the caller's indices (`given`), then the
+// attention: one 8-CTA cluster per row.
+int run_tail(const ds_row_set_t* set, const ds_bf16* q_attn, const float* sinks, size_t sinks_row_stride,
+             float scale, ds_bf16* out, uint32_t* invalid, const float* scores, uint64_t score_stride,
+             const int32_t* given, int32_t* indices, uint8_t* ws, const Layout& L, cudaStream_t stream) {
+    TailParams tp;
+    std::memset(&tp, 0, sizeof(tp));
     uint32_t chunks = 0;
     for (int e = 0; e < set->rows; ++e) {
         const ds_row_t& r = set->table[e];
-        p.kv[e] = reinterpret_cast<const __nv_bfloat16*>(set->kv[e]);
-        p.kv_len[e] = r.kv_len;
-        p.width[e] = r.width;
-        p.index_offset[e] = index_offset[e];
-        p.q_row[e] = r.q_row;
-        p.chunk_begin[e] = chunks;
-        chunks += (r.width + kAttnSlots - 1) / kAttnSlots;
+        tp.kv[e] = reinterpret_cast<const __nv_bfloat16*>(set->kv[e]);
+        tp.kv_len[e] = r.kv_len;
+        tp.width[e] = r.width;
+        tp.index_offset[e] = r.index_offset;
+        tp.q_row[e] = r.q_row;
+        tp.chunk_begin[e] = chunks;
+        chunks += (r.width + kTailChunkSlots - 1) / kTailChunkSlots;
     }
-    p.q = reinterpret_cast<const __nv_bfloat16*>(q_attn);
-    p.sinks = sinks;
-    p.sinks_row_stride = sinks_row_stride;
-    p.indices = indices;
-    p.part = reinterpret_cast<float*>(ws + L.part);
-    p.flags = reinterpret_cast<uint32_t*>(ws + L.flags);
-    p.out = reinterpret_cast<__nv_bfloat16*>(out);
-    p.invalid = invalid;
-    p.status = reinterpret_cast<uint32_t*>(ws + L.status);
-    p.scale = scale;
-    p.rows = (uint32_t)set->rows;
-    p.total_chunks = chunks;
-    cudaError_t err = launch_attention(p, stream, true);
-    return err == cudaSuccess ? DS_OK : cuda_fail(err, "attention launch");
+    tp.scores = scores;
+    tp.score_stride = score_stride;
+    tp.hist = reinterpret_cast<const uint32_t*>(ws + L.hist);
+    tp.status = reinterpret_cast<uint32_t*>(ws + L.status);
+    tp.q = reinterpret_cast<const __nv_bfloat16*>(q_attn);
+    tp.sinks = sinks;
+    tp.sinks_row_stride = sinks_row_stride;
+    tp.part = reinterpret_cast<float*>(ws + L.part);
+    tp.flags = reinterpret_cast<uint32_t*>(ws + L.flags);
+    tp.out = reinterpret_cast<__nv_bfloat16*>(out);
+    tp.invalid = invalid;
+    tp.given = given;
+    tp.indices = indices;
+    tp.scale = scale;
+    tp.rows = (uint32_t)set->rows;
+    cudaError_t err = launch_decode_tail(tp, stream, true);
+    return err == cudaSuccess ? DS_OK : cuda_fail(err, given ? "attention launch" : "decode select + attention launch");
 }
 
 int check_attn_args(const ds_bf16* q_attn, const float* sinks, size_t sinks_row_stride, float scale, ds_bf16* out) {
@@ -384,9 +389,7 @@ int ds_rows_sparse_attn(const ds_row_set_t* set, const ds_bf16* q_attn, const fl
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t err = launch_clear(reinterpret_cast<uint32_t*>(ws), (uint32_t)(L.ctl_end / 4), s);
     if (err != cudaSuccess) return cuda_fail(err, "workspace clear");
-    uint32_t off[DS_ROWS_MAX];
-    for (int e = 0; e < set->rows; ++e) off[e] = set->table[e].index_offset;
-    return run_attention(set, q_attn, sinks, sinks_row_stride, indices, off, scale, out, invalid, ws, L, s);
+    return run_tail(set, q_attn, sinks, sinks_row_stride, scale, out, invalid, nullptr, 0, indices, nullptr, ws, L, s);
 }
 
 int ds_rows_decode(const ds_row_set_t* set, const ds_bf16* q_index, const float* w_index, const ds_bf16* q_attn,
@@ -413,35 +416,8 @@ int ds_rows_decode(const ds_row_set_t* set, const ds_bf16* q_index, const float*
     // Selection and attention in one kernel: one 8-CTA cluster per row keeps the
     // selection on chip and attends over it in best-first order, the order of
     // the indices it writes for the caller.
-    TailParams tp;
-    std::memset(&tp, 0, sizeof(tp));
-    uint32_t chunks = 0;
-    for (int e = 0; e < set->rows; ++e) {
-        const ds_row_t& r = set->table[e];
-        tp.kv[e] = reinterpret_cast<const __nv_bfloat16*>(set->kv[e]);
-        tp.kv_len[e] = r.kv_len;
-        tp.width[e] = r.width;
-        tp.index_offset[e] = r.index_offset;
-        tp.q_row[e] = r.q_row;
-        tp.chunk_begin[e] = chunks;
-        chunks += (r.width + kAttnSlots - 1) / kAttnSlots;
-    }
-    tp.part = reinterpret_cast<float*>(ws + L.part);
-    tp.flags = reinterpret_cast<uint32_t*>(ws + L.flags);
-    tp.scores = scores;
-    tp.score_stride = L.score_stride;
-    tp.hist = hist;
-    tp.status = status;
-    tp.q = reinterpret_cast<const __nv_bfloat16*>(q_attn);
-    tp.sinks = sinks;
-    tp.sinks_row_stride = sinks_row_stride;
-    tp.out = reinterpret_cast<__nv_bfloat16*>(out);
-    tp.invalid = invalid;
-    tp.indices = indices;
-    tp.scale = scale;
-    tp.rows = (uint32_t)set->rows;
-    err = launch_decode_tail(tp, s, true);
-    return err == cudaSuccess ? DS_OK : cuda_fail(err, "decode select + attention launch");
+    return run_tail(set, q_attn, sinks, sinks_row_stride, scale, out, invalid, scores, L.score_stride, nullptr,
+                    indices, ws, L, s);
 }
 
 int ds_rows_topk_static(const ds_row_set_t* set, const float* scores, size_t score_stride, int32_t* indices,

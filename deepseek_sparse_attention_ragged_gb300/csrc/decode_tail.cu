@@ -1,26 +1,44 @@
-// The decode step after the indexer: top-k selection and sink-softmax sparse
-// attention of each row in one kernel (mlx-native deepseek_rows.metal: the
-// top-k kernels deepseek_indexer_topk_*_rows_i32 followed by
-// deepseek_sparse_attention_score_rows_bf16 / _reduce_rows_bf16).
+// Top-k selection and sink-softmax sparse attention of each row in one kernel
+// (mlx-native deepseek_rows.metal: the top-k kernels
+// deepseek_indexer_topk_*_rows_i32 followed by
+// deepseek_sparse_attention_score_rows_bf16 / _reduce_rows_bf16; gather
+// semantics of deepseek_sparse_attention_gather_rows_bf16).
 //
-// One 8-CTA thread-block cluster per row, 512 threads per CTA:
-//   1. select: every CTA streams its slice of the row's scores and appends the
-//      candidates at or above the level-0 threshold bin to the leader's shared
-//      memory; the leader refines and keeps the winners' composites;
+// Per row e and head h over the selected slots t (index i_t):
+//   l_t = scale * q_h . KV[i_t],  m = max(sink_h, max l_t),
+//   den = exp(sink_h - m) + sum exp(l_t - m),  out_h = sum exp(l_t - m) KV[i_t] / den.
+//
+// One 8-CTA thread-block cluster per row, 512 threads per CTA. CTA r owns the
+// 128-slot chunk c = r / 2 and the head half r % 2 (32 heads).
+//   1. select (decode only): every CTA streams its slice of the row's scores
+//      and appends the candidates at or above the level-0 threshold bin to the
+//      leader's shared memory; the leader refines and keeps the winners'
+//      composites;
 //   2. place: every CTA ranks 64 of the winners against all of them by
 //      composite (score descending, lower index first): that rank is the
 //      winner's slot, both in the caller's best-first index list and in the
 //      attention, and the CTA stores the index into the shared memory of the
-//      CTA that owns the slot;
-//   3. attend: CTA r takes slots [64 r, 64 r + 64) for all 64 heads:
-//      bulk-copies the 64 KV rows, then logits, chunk softmax and P G (the
-//      query was fetched while the indexer was running); the chunk partial
-//      goes to the workspace;
+//      two CTAs that own the slot. With indices given by the caller, each CTA
+//      reads its chunk's slots instead;
+//   3. attend, on tcgen05 tensor cores with fp32 accumulators in TMEM: gather
+//      the chunk's 128 KV rows into the 128-byte-swizzled K-major layout, then
+//        logits  D[128 slots x 32 heads] = KV_chunk . Q_half^T   (K = 512),
+//      the chunk softmax (max and sum over the 128 slots, per head), and
+//        P G     D[128 features x 32 heads] = KV_chunk^T . P^T    (K = 128 slots)
+//      for the four 128-feature blocks, where the same KV buffer is the
+//      MN-major operand and P enters as a bf16 hi + lo pair;
 //   4. combine: after a cluster barrier CTA r combines feature columns
-//      [64 r, 64 r + 64) of every head over the chunks, in chunk order.
-// Per output element the operations and their order are those of the
-// stand-alone attention kernels, so the decode's output is bitwise the
-// attention of its own best-first index list.
+//      [128 c, 128 c + 128) of its 32 heads over the chunks in chunk order:
+//        m = max(sink, m_c), den = exp(sink - m) + sum_c l_c exp(m_c - m),
+//        out = sum_c acc_c exp(m_c - m) / den.
+// Every reduction order depends on the row's width alone, and the stand-alone
+// attention runs this kernel on the caller's indices, so the decode's output
+// is bitwise the attention of its own best-first index list.
+//
+// Fail-closed rules: a caller's index < -1 or >= kv_len flags the whole row; a
+// non-finite logit (non-finite q or KV element, or overflow) flags its head;
+// a non-finite sink or denominator flags the head; a flagged head is written
+// as zeros, and any non-finite output element is written as zero.
 
 #include <cooperative_groups.h>
 
@@ -32,182 +50,323 @@
 namespace dsrows {
 
 namespace cg = cooperative_groups;
-using namespace attend;
+using attend::CombineSmem;
+using attend::combine_slice;
+using attend::cp_async16;
+using attend::cp_async_commit;
+using attend::cp_async_wait_all;
 using namespace rowsel;
 
 namespace {
 
-constexpr int kRowBytes = kDim * 2;
-constexpr size_t kTailPartFloats = 2 * kHeads + (size_t)kHeads * kDim;  // m[64], l[64], acc[64][512]
-static_assert(kTailPartFloats == 2 * kPartFloats, "a chunk's partial fills the space of its two head halves");
+constexpr int kChunkSlots = 128;                         // slots per chunk (UMMA M of the logits)
+constexpr int kHalfHeads = kHeads / 2;                   // heads per CTA (UMMA N)
+constexpr uint32_t kTmemCols = 256;                      // logits (32) + P G (4 x 32)
+constexpr uint32_t kPvCol = 32;                          // first TMEM column of P G
+constexpr int kGBlock = kChunkSlots * 128;               // one 64-column block of the KV rows: 16 KiB
+constexpr int kQBlock = kHalfHeads * 128;                // one 64-column block of the query half: 4 KiB
+constexpr int kPBlock = kHalfHeads * 128;                // 64 slots of P for 32 heads: 4 KiB
+static_assert(kCluster * kChunkSlots == 2 * kTopK, "4 chunks x 2 head halves per row");
+static_assert(kThreads == 512, "16 warps");
 
 struct TailLayout {
-    static constexpr size_t q = 0;                                       // bf16 [64][kQStride]
-    static constexpr size_t g = q + (size_t)kHeads * kQStride * 2;       // bf16 [64][kQStride]
-    static constexpr size_t lg = g + (size_t)kSlots * kQStride * 2;      // f32 [64][kLgStride]
-    static constexpr size_t p_hi = lg + (size_t)kHeads * kLgStride * 4;  // bf16 [64][kPStride]
-    static constexpr size_t p_lo = p_hi + (size_t)kHeads * kPStride * 2;
-    static constexpr size_t idx = p_lo + (size_t)kHeads * kPStride * 2;  // i32 [64] this CTA's slots
-    static constexpr size_t sel = idx + (size_t)kSlots * 4;              // u64 [512] winners (leader)
-    static constexpr size_t nsel = sel + (size_t)kTopK * 8;              // u32 number of winners (leader)
-    static constexpr size_t gbar = nsel + 16;                            // mbarrier of the KV copies
-    static constexpr size_t cs = gbar + 16;                              // CombineSmem<64>
-    static constexpr size_t total = cs + sizeof(CombineSmem<kHeads>);
-    // Aliases of the KV rows' space, used before the copies land.
-    static constexpr size_t select = g;                                  // SelectSmem (select phase)
-    static constexpr size_t selcopy = g;                                 // u64 [512] (place phase)
-    static constexpr size_t ranks = g + (size_t)kTopK * 8;               // u32 [64] (place phase)
+    static constexpr size_t g = 0;                                     // KV rows [128][512], K-major SW128
+    static constexpr size_t q = g + 8 * (size_t)kGBlock;               // query half [32][512], K-major SW128
+    static constexpr size_t p_hi = q + 8 * (size_t)kQBlock;            // P [32 heads][128 slots], K-major SW128
+    static constexpr size_t p_lo = p_hi + 2 * (size_t)kPBlock;
+    static constexpr size_t idx = p_lo + 2 * (size_t)kPBlock;          // i32 [128] this chunk's slots
+    static constexpr size_t sel = idx + (size_t)kChunkSlots * 4;       // u64 [512] winners (leader)
+    static constexpr size_t red = sel + (size_t)kTopK * 8;             // [4 quarters][32 heads] max, sum, bad
+    static constexpr size_t misc = red + 3 * 4 * (size_t)kHalfHeads * 4;
+    static constexpr size_t cs = misc + 64;                            // CombineSmem<32>
+    static constexpr size_t total = cs + sizeof(CombineSmem<kHalfHeads>);
+    // Aliases of the KV rows' space, used before the rows are gathered.
+    static constexpr size_t select = g;                                // SelectSmem (select phase)
+    static constexpr size_t selcopy = g;                               // u64 [512] (place phase)
+    static constexpr size_t ranks = g + (size_t)kTopK * 8;             // u32 [64] (place phase)
 };
-static_assert(TailLayout::select + sizeof(SelectSmem) <= TailLayout::p_hi, "select state overlaps P");
-static_assert(TailLayout::gbar % 8 == 0 && TailLayout::sel % 8 == 0, "alignment");
-static_assert(TailLayout::total <= 227 * 1024, "shared memory");
-static_assert(kThreads == 512 && kCluster * kSlots == kTopK, "one 64-slot chunk per CTA");
+static_assert(TailLayout::select + sizeof(SelectSmem) <= TailLayout::q, "select state overlaps the query");
+static_assert(TailLayout::misc % 8 == 0, "alignment");
+constexpr size_t kTailSmem = TailLayout::total + 1024;  // + slack to align the swizzled buffers to 1 KiB
+static_assert(kTailSmem <= 227 * 1024, "shared memory");
+
+// Byte offset of 16-byte chunk ch (0..63) of row r in a K-major SW128 buffer of
+// 64-column blocks `block` bytes apart (rows of 128 B per block).
+__device__ __forceinline__ uint32_t sw128_chunk(int r, int ch, int block) {
+    return (uint32_t)((ch >> 3) * block + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
+}
 
 }  // namespace
 
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tail_kernel(const TailParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     using T = TailLayout;
-    __nv_bfloat16* q_s = reinterpret_cast<__nv_bfloat16*>(smem + T::q);
-    __nv_bfloat16* g_s = reinterpret_cast<__nv_bfloat16*>(smem + T::g);
-    float* lg_s = reinterpret_cast<float*>(smem + T::lg);
-    __nv_bfloat16* ph_s = reinterpret_cast<__nv_bfloat16*>(smem + T::p_hi);
-    __nv_bfloat16* pl_s = reinterpret_cast<__nv_bfloat16*>(smem + T::p_lo);
+    uint8_t* g_s = smem + T::g;
+    uint8_t* q_s = smem + T::q;
+    uint8_t* ph_s = smem + T::p_hi;
+    uint8_t* pl_s = smem + T::p_lo;
     int* idx_s = reinterpret_cast<int*>(smem + T::idx);
     uint64_t* sel = reinterpret_cast<uint64_t*>(smem + T::sel);
-    uint32_t* nsel_s = reinterpret_cast<uint32_t*>(smem + T::nsel);
-    uint64_t* gbar = reinterpret_cast<uint64_t*>(smem + T::gbar);
-    CombineSmem<kHeads>& cs = *reinterpret_cast<CombineSmem<kHeads>*>(smem + T::cs);
+    float* red_max = reinterpret_cast<float*>(smem + T::red);
+    float* red_sum = red_max + 4 * kHalfHeads;
+    uint32_t* red_bad = reinterpret_cast<uint32_t*>(red_sum + 4 * kHalfHeads);
+    uint32_t* nsel_s = reinterpret_cast<uint32_t*>(smem + T::misc);
+    uint32_t* tmem_s = nsel_s + 1;
+    uint64_t* mma_bar = reinterpret_cast<uint64_t*>(smem + T::misc + 8);
+    CombineSmem<kHalfHeads>& cs = *reinterpret_cast<CombineSmem<kHalfHeads>*>(smem + T::cs);
     SelectSmem& sm = *reinterpret_cast<SelectSmem*>(smem + T::select);
 
     cg::cluster_group cluster = cg::this_cluster();
     const uint32_t rank = cluster.block_rank();
     const int e = blockIdx.x / kCluster;
+    const uint32_t c = rank >> 1;          // chunk: slots [128 c, 128 c + 128)
+    const int half = (int)(rank & 1);      // heads [32 half, 32 half + 32)
+    const int head0 = half * kHalfHeads;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const uint32_t L = p.kv_len[e];
     const uint32_t W = p.width[e];
     const uint32_t q_row = p.q_row[e];
-    const float* s = p.scores + (size_t)e * p.score_stride;
+    const uint32_t nchunks = (W + kChunkSlots - 1) / kChunkSlots;
+    const bool has_chunk = c < nchunks;
     SelectSmem& leader = *cluster.map_shared_rank(&sm, 0);
 
-    // ---- select --------------------------------------------------------------
+    // ---- setup: counters, barrier, TMEM, and the query (an input of the call) --
     if (t == 0) {
         sm.ncand = 0;
-        mbar_init(gbar, 1);
+        mbar_init(mma_bar, 1);
         fence_barrier_init();
     }
-    // The query is an input of the call: fetch it while the indexer finishes.
-    load_q<kHeads, kThreads>(q_s, p.q + (size_t)q_row * kHeads * kDim, t);
-    cp_async_commit();
-    cluster.sync();  // the leader's counters are zero before anyone appends
-    pdl_wait();      // scores and histogram come from the indexer
-    const Collected col = select_collect(s, L, W, p.hist + (size_t)e * kHistBins, rank, sm, leader);
-    cluster.sync();  // every append into the leader is visible to it
-    if (rank == 0) {
-        const uint32_t n = select_finish(col, s, L, W, false, nullptr, sm, sel, p.status);
-        if (t == 0) *nsel_s = n;
+    if (warp == 0) {
+        tmem_alloc(tmem_s, kTmemCols);
+        tmem_relinquish();
     }
-    cluster.sync();  // the winners are visible to the cluster
-
-    // ---- place: rank 64 winners, store them in their slots ---------------------
     {
+        const __nv_bfloat16* qh = p.q + ((size_t)q_row * kHeads + head0) * kDim;
+        for (int k = t; k < kHalfHeads * (kDim / 8); k += kThreads) {
+            const int h = k >> 6, ch = k & 63;
+            cp_async16(q_s + sw128_chunk(h, ch, kQBlock), qh + (size_t)h * kDim + ch * 8);
+        }
+        cp_async_commit();
+    }
+    tc_fence_before();
+    cluster.sync();  // the leader's counters are zero before anyone appends
+    tc_fence_after();
+    const uint32_t tmem = *tmem_s;
+    pdl_wait();  // scores and histogram (decode) or indices (caller) come from earlier work
+
+    if (p.given == nullptr) {
+        // ---- select -------------------------------------------------------------
+        const float* s = p.scores + (size_t)e * p.score_stride;
+        const Collected col = select_collect(s, L, W, p.hist + (size_t)e * kHistBins, rank, sm, leader);
+        cluster.sync();  // every append into the leader is visible to it
+        if (rank == 0) {
+            const uint32_t n = select_finish(col, s, L, W, false, nullptr, sm, sel, p.status);
+            if (t == 0) *nsel_s = n;
+        }
+        cluster.sync();  // the winners are visible to the cluster
+
+        // ---- place: rank 64 winners, store them in their slots -------------------
         const uint32_t nsel = *cluster.map_shared_rank(nsel_s, 0);
         uint64_t* sc = reinterpret_cast<uint64_t*>(smem + T::selcopy);
         uint32_t* rk = reinterpret_cast<uint32_t*>(smem + T::ranks);
         sc[t] = (uint32_t)t < nsel ? cluster.map_shared_rank(sel, 0)[t] : 0ull;
-        if (t < kSlots) rk[t] = 0;
-        // Slots of this CTA past the last winner are empty.
-        if (t < kSlots && rank * kSlots + (uint32_t)t >= nsel) idx_s[t] = -1;
+        if (t < 64) rk[t] = 0;
+        // Slots of this chunk past the last winner are empty.
+        if (t < kChunkSlots && c * kChunkSlots + (uint32_t)t >= nsel) idx_s[t] = -1;
         __syncthreads();
         // Winner k against the 64 winners of group t / 64: how many are better
         // (the zero padding never is; composites are distinct).
-        const uint32_t k = rank * kSlots + (uint32_t)(t & (kSlots - 1));
+        const uint32_t k = rank * 64 + (uint32_t)(t & 63);
         const uint64_t ck = sc[k];
-        const uint64_t* grp = sc + (t >> 6) * kSlots;
+        const uint64_t* grp = sc + (t >> 6) * 64;
         uint32_t nb = 0;
 #pragma unroll 16
-        for (int j = 0; j < kSlots; ++j) nb += grp[j] > ck ? 1u : 0u;
-        atomicAdd(&rk[t & (kSlots - 1)], nb);
+        for (int j = 0; j < 64; ++j) nb += grp[j] > ck ? 1u : 0u;
+        atomicAdd(&rk[t & 63], nb);
         __syncthreads();
-        if (t < kSlots) {
+        if (t < 64) {
             int32_t* out = p.indices ? p.indices + p.index_offset[e] : nullptr;
             if (k < nsel) {
                 const uint32_t pos = rk[t];
                 const int32_t j = (int32_t)(~(uint32_t)ck);
                 if (out) out[pos] = j;
-                cluster.map_shared_rank(idx_s, pos / kSlots)[pos % kSlots] = j;
+                const uint32_t owner = 2 * (pos / kChunkSlots);
+                cluster.map_shared_rank(idx_s, owner)[pos % kChunkSlots] = j;
+                cluster.map_shared_rank(idx_s, owner + 1)[pos % kChunkSlots] = j;
             } else if (out && k < W) {
                 out[k] = -1;
             }
         }
+    } else if (t < kChunkSlots) {
+        // ---- the caller's indices: -1 for sentinels, bad indices and slots past the width
+        const uint32_t slot = c * kChunkSlots + (uint32_t)t;
+        int i = -1;
+        if (slot < W) {
+            const int v = __ldcg(p.given + p.index_offset[e] + slot);
+            if (v < -1 || v >= (int)L) atomicOr(&p.flags[kRowsMax * kHeads + e], 1u);
+            else i = v;
+        }
+        idx_s[t] = i;
     }
     cluster.sync();  // every CTA's slots are in place
 
-    // ---- attend: slots [64 rank, 64 rank + 64) for all 64 heads ----------------
-    const uint32_t nchunks = (W + kSlots - 1) / kSlots;
-    const bool has_chunk = rank < nchunks;
-    float* part0 = p.part + (size_t)p.chunk_begin[e] * kTailPartFloats;  // this row's first partial
+    // ---- attend: 128 slots x 32 heads on the tensor cores ------------------------
+    const size_t part0_off = ((size_t)2 * p.chunk_begin[e] + (size_t)half * nchunks) * kPartFloats;
     if (has_chunk) {
-        // The KV rows' space held generic-proxy data: order it before the copies.
-        fence_proxy_async_smem();
-        const int live = __syncthreads_count(t < kSlots && idx_s[t] >= 0);
-        if (t == 0) mbar_arrive_expect_tx(gbar, (uint32_t)live * kRowBytes);
-        if (t < kSlots) {
-            const int i = idx_s[t];
-            __nv_bfloat16* dst = g_s + t * kQStride;
-            if (i >= 0) {
-                bulk_copy_g2s(dst, p.kv[e] + (size_t)i * kDim, kRowBytes, gbar);
-            } else {
-                for (int c = 0; c < kDim / 8; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
-            }
-        }
-        mbar_wait(gbar, 0, p.status);
-        cp_async_wait_all();  // the query
-        __syncthreads();
-
-        logits<kHeads>(q_s, g_s, lg_s, p.scale, warp, lane);
-        __syncthreads();
-        float* part = part0 + (size_t)rank * kTailPartFloats;
-        softmax<4>(lg_s, idx_s, ph_s, pl_s, warp, lane, [&](int h, float m, float l, bool bad) {
-            if (bad) atomicOr(&p.flags[e * kHeads + h], 1u);
-            part[h] = m;
-            part[kHeads + h] = l;
-        });
-        __syncthreads();
-        float acc[16][4];
-        pv<128>(ph_s, pl_s, g_s, warp, lane, acc);
-        float* pacc = part + 2 * kHeads;
-        const int h0 = 16 * (warp >> 2) + (lane >> 2);
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-            const int f = (warp & 3) * 128 + nt * 8 + 2 * (lane & 3);
-            *reinterpret_cast<float2*>(pacc + (size_t)h0 * kDim + f) = make_float2(acc[nt][0], acc[nt][1]);
-            *reinterpret_cast<float2*>(pacc + (size_t)(h0 + 8) * kDim + f) = make_float2(acc[nt][2], acc[nt][3]);
+        const __nv_bfloat16* kv = p.kv[e];
+        for (int k = t; k < kChunkSlots * (kDim / 8); k += kThreads) {
+            const int r = k >> 6, ch = k & 63;
+            const int i = idx_s[r];
+            uint8_t* dst = g_s + sw128_chunk(r, ch, kGBlock);
+            if (i >= 0) cp_async16(dst, kv + (size_t)i * kDim + ch * 8);
+            else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
         }
     }
-    cluster.sync();  // every chunk's partial and head flags are visible to the cluster
+    cp_async_wait_all();      // the query and the KV rows
+    fence_proxy_async_smem();  // ... are visible to the tensor cores
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
 
-    // ---- combine: feature columns [64 rank, 64 rank + 64) of every head --------
-    combine_slice<kHeads, kThreads>(part0, kTailPartFloats, (int)nchunks, (int)rank * 64,
-                                    p.sinks + (size_t)q_row * p.sinks_row_stride, false, p.flags + e * kHeads,
-                                    p.out + (size_t)q_row * kHeads * kDim,
-                                    p.invalid && rank == 0 ? p.invalid + (size_t)q_row * kHeads : nullptr, cs);
+    if (has_chunk) {
+        const uint32_t g_addr = smem_u32(g_s), q_addr = smem_u32(q_s);
+        if (t == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(128, kHalfHeads);
+#pragma unroll
+            for (int kk = 0; kk < kDim / 16; ++kk) {
+                const uint32_t koff = (uint32_t)(kk & 3) * 32;  // 16 bf16 = 32 B inside the 128-B row
+                umma_bf16(tmem, smem_desc_sw128_kmajor(g_addr + (kk >> 2) * kGBlock + koff),
+                          smem_desc_sw128_kmajor(q_addr + (kk >> 2) * kQBlock + koff), idesc, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(mma_bar);
+        }
+        mbar_wait(mma_bar, 0, p.status);
+        tc_fence_after();
+
+        // ---- chunk softmax: warp -> (32 slots, 8 heads), lane -> one slot ----------
+        const int qt = warp & 3, hg = warp >> 2;
+        const int slot = 32 * qt + lane;
+        uint32_t v[8];
+        tmem_ld_x8(tmem + ((uint32_t)(32 * qt) << 16) + 8 * hg, v);
+        tmem_ld_wait();
+        const bool live = idx_s[slot] >= 0;
+        float l[8], m[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            l[i] = __uint_as_float(v[i]) * p.scale;
+            const bool ok = live && finite_f(l[i]);
+            const uint32_t bad = __ballot_sync(0xFFFFFFFFu, live && !ok);
+            if (!ok) l[i] = -INFINITY;
+            m[i] = l[i];
+            if (lane == 0) red_bad[qt * kHalfHeads + 8 * hg + i] = bad ? 1u : 0u;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m[i] = fmaxf(m[i], __shfl_xor_sync(0xFFFFFFFFu, m[i], o));
+        if (lane == 0)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) red_max[qt * kHalfHeads + 8 * hg + i] = m[i];
+        __syncthreads();
+        float sum[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int h = 8 * hg + i;
+            const float mh = fmaxf(fmaxf(red_max[h], red_max[kHalfHeads + h]),
+                                   fmaxf(red_max[2 * kHalfHeads + h], red_max[3 * kHalfHeads + h]));
+            const float w = l[i] == -INFINITY ? 0.0f : expf(l[i] - mh);
+            const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(w - __bfloat162float(hi));
+            const uint32_t off = (uint32_t)((slot >> 6) * kPBlock + h * 128 +
+                                            ((((slot & 63) >> 3) ^ (h & 7)) << 4) + ((slot & 7) << 1));
+            *reinterpret_cast<__nv_bfloat16*>(ph_s + off) = hi;
+            *reinterpret_cast<__nv_bfloat16*>(pl_s + off) = lo;
+            sum[i] = w;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sum[i] += __shfl_xor_sync(0xFFFFFFFFu, sum[i], o);
+        if (lane == 0)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) red_sum[qt * kHalfHeads + 8 * hg + i] = sum[i];
+        fence_proxy_async_smem();  // P is visible to the tensor cores
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        float* part = p.part + part0_off + (size_t)c * kPartFloats;
+        if (t < kHalfHeads) {
+            const float mh = fmaxf(fmaxf(red_max[t], red_max[kHalfHeads + t]),
+                                   fmaxf(red_max[2 * kHalfHeads + t], red_max[3 * kHalfHeads + t]));
+            part[t] = mh;
+            part[kHalfHeads + t] = (red_sum[t] + red_sum[kHalfHeads + t]) +
+                                   (red_sum[2 * kHalfHeads + t] + red_sum[3 * kHalfHeads + t]);
+            if (red_bad[t] | red_bad[kHalfHeads + t] | red_bad[2 * kHalfHeads + t] | red_bad[3 * kHalfHeads + t])
+                atomicOr(&p.flags[e * kHeads + head0 + t], 1u);
+        }
+        if (t == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(128, kHalfHeads) | kIdescAMnMajor;
+            const uint32_t p_addr[2] = {smem_u32(ph_s), smem_u32(pl_s)};
+#pragma unroll
+            for (int b = 0; b < kDim / 128; ++b)
+#pragma unroll
+                for (int ks = 0; ks < kChunkSlots / 16; ++ks)
+#pragma unroll
+                    for (int hl = 0; hl < 2; ++hl) {
+                        // A: features [128 b, 128 b + 128) x slots [16 ks, 16 ks + 16), MN-major.
+                        const uint64_t ad = smem_desc_sw128_mnmajor(g_addr + 2 * b * kGBlock + ks * 2048, kGBlock, 1024);
+                        const uint64_t bd = smem_desc_sw128_kmajor(p_addr[hl] + (ks >> 2) * kPBlock + (ks & 3) * 32);
+                        umma_bf16(tmem + kPvCol + 32 * b, ad, bd, idesc, (ks | hl) != 0 ? 1u : 0u);
+                    }
+            umma_commit(mma_bar);
+        }
+        mbar_wait(mma_bar, 1, p.status);
+        tc_fence_after();
+
+        // ---- partial: warp -> (32 features, 32 heads) of block warp / 4 -------------
+        const int b = warp >> 2;
+        uint32_t a[32];
+        tmem_ld_x32(tmem + ((uint32_t)(32 * qt) << 16) + kPvCol + 32 * b, a);
+        tmem_ld_wait();
+        float* pacc = part + 2 * kHalfHeads + 128 * b + 32 * qt + lane;
+#pragma unroll
+        for (int h = 0; h < kHalfHeads; ++h) pacc[(size_t)h * kDim] = __uint_as_float(a[h]);
+    }
+    tc_fence_before();
+    cluster.sync();  // every chunk's partial and head flags are visible to the cluster
+    tc_fence_after();
+
+    // ---- combine: feature columns [128 c, 128 c + 128) of the 32 heads ----------
+    const bool row_bad = __ldcg(p.flags + kRowsMax * kHeads + e) != 0;
+    combine_slice<kHalfHeads, kThreads, 128>(
+        p.part + part0_off, kPartFloats, (int)nchunks, (int)(128 * c),
+        p.sinks + (size_t)q_row * p.sinks_row_stride + head0, row_bad, p.flags + e * kHeads + head0,
+        p.out + ((size_t)q_row * kHeads + head0) * kDim,
+        p.invalid && c == 0 ? p.invalid + (size_t)q_row * kHeads + head0 : nullptr, cs);
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
 }
 
-size_t decode_tail_smem_bytes() { return TailLayout::total; }
+size_t decode_tail_smem_bytes() { return kTailSmem; }
 
 cudaError_t launch_decode_tail(const TailParams& p, cudaStream_t stream, bool pdl) {
     static bool configured = false;
     if (!configured) {
-        cudaError_t err = cudaFuncSetAttribute(decode_tail_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)TailLayout::total);
+        cudaError_t err =
+            cudaFuncSetAttribute(decode_tail_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTailSmem);
         if (err != cudaSuccess) return err;
         configured = true;
     }
     if (p.rows == 0) return cudaSuccess;
-    return launch_kernel(decode_tail_kernel, dim3(p.rows * kCluster), dim3(kThreads), TailLayout::total, stream, pdl,
-                         p);
+    return launch_kernel(decode_tail_kernel, dim3(p.rows * kCluster), dim3(kThreads), kTailSmem, stream, pdl, p);
 }
 
 }  // namespace dsrows

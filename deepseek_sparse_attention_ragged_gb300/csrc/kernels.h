@@ -42,29 +42,10 @@ struct TopkParams {
     uint32_t chunk_begin[DS_ROWS_MAX];
 };
 
-// Sparse attention: per-row KV pointers and the split of each row's slots.
-struct AttnParams {
-    const __nv_bfloat16* kv[DS_ROWS_MAX];
-    const __nv_bfloat16* q;       // [Q, 64, 512]
-    const float* sinks;
-    uint64_t sinks_row_stride;
-    const int32_t* indices;
-    float* part;                  // partials
-    uint32_t* flags;              // [8][64] head-invalid bits (+ row bits at [8*64 + e])
-    __nv_bfloat16* out;           // [Q, 64, 512]
-    uint32_t* invalid;            // optional [Q, 64]
-    uint32_t* status;
-    float scale;
-    uint32_t rows;
-    uint32_t total_chunks;
-    uint32_t kv_len[DS_ROWS_MAX];
-    uint32_t width[DS_ROWS_MAX];
-    uint32_t index_offset[DS_ROWS_MAX];
-    uint32_t q_row[DS_ROWS_MAX];
-    uint32_t chunk_begin[DS_ROWS_MAX];  // first attention chunk of each row
-};
+// Selection (decode) and attention, one 8-CTA cluster per row; with `given`,
+// the attention of the caller's indices.
+constexpr uint32_t kTailChunkSlots = 128;  // slots per attention chunk
 
-// The decode after the indexer: selection + attention, one 8-CTA cluster per row.
 struct TailParams {
     const float* scores;          // indexer scores, entry e at e * score_stride
     uint64_t score_stride;
@@ -74,18 +55,19 @@ struct TailParams {
     const __nv_bfloat16* q;       // [Q, 64, 512]
     const float* sinks;
     uint64_t sinks_row_stride;
-    float* part;                  // chunk partials: m[64], l[64], acc[64][512] per chunk
+    float* part;                  // partials: m[32], l[32], acc[32][512] per (chunk, head half)
     uint32_t* flags;              // [8][64] head flags, zero on entry
     __nv_bfloat16* out;           // [Q, 64, 512]
     uint32_t* invalid;            // optional [Q, 64]
-    int32_t* indices;             // optional best-first selection, entry e at index_offset[e]
+    const int32_t* given;         // the caller's indices (attention only), entry e at index_offset[e]
+    int32_t* indices;             // optional best-first selection (decode), entry e at index_offset[e]
     float scale;
     uint32_t rows;
     uint32_t kv_len[DS_ROWS_MAX];
     uint32_t width[DS_ROWS_MAX];
     uint32_t index_offset[DS_ROWS_MAX];
     uint32_t q_row[DS_ROWS_MAX];
-    uint32_t chunk_begin[DS_ROWS_MAX];  // first 64-slot chunk of each row
+    uint32_t chunk_begin[DS_ROWS_MAX];  // first 128-slot chunk of each row
 };
 
 size_t indexer_smem_bytes();
@@ -98,9 +80,6 @@ cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t stream, bool pd
 
 // Zero `words` 32-bit words (the workspace control region); an ordinary launch.
 cudaError_t launch_clear(uint32_t* p, uint32_t words, cudaStream_t stream);
-
-// Partial kernel (PDL on the previous kernel when `pdl`), then the combine kernel (PDL).
-cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream, bool pdl);
 
 size_t decode_tail_smem_bytes();
 cudaError_t launch_decode_tail(const TailParams& p, cudaStream_t stream, bool pdl);
