@@ -24,9 +24,10 @@
 //      the chunk's 128 KV rows into the 128-byte-swizzled K-major layout, then
 //        logits  D[128 slots x 32 heads] = KV_chunk . Q_half^T   (K = 512),
 //      the chunk softmax (max and sum over the 128 slots, per head), and
-//        P G     D[128 features x 32 heads] = KV_chunk^T . P^T    (K = 128 slots)
+//        P G     D[128 features x 64] = KV_chunk^T . [P_hi; P_lo]^T  (K = 128 slots)
 //      for the four 128-feature blocks, where the same KV buffer is the
-//      MN-major operand and P enters as a bf16 hi + lo pair;
+//      MN-major operand and P enters as a bf16 hi + lo pair stacked along N
+//      (acc = D[:, h] + D[:, 32 + h]);
 //   4. combine: after a cluster barrier CTA r combines feature columns
 //      [128 c, 128 c + 128) of its 32 heads over the chunks in chunk order:
 //        m = max(sink, m_c), den = exp(sink - m) + sum_c l_c exp(m_c - m),
@@ -61,20 +62,19 @@ namespace {
 
 constexpr int kChunkSlots = 128;                         // slots per chunk (UMMA M of the logits)
 constexpr int kHalfHeads = kHeads / 2;                   // heads per CTA (UMMA N)
-constexpr uint32_t kTmemCols = 256;                      // logits (32) + P G (4 x 32)
-constexpr uint32_t kPvCol = 32;                          // first TMEM column of P G
+constexpr uint32_t kTmemCols = 512;                      // logits (32) + P G (4 x 64)
+constexpr uint32_t kPvCol = 64;                          // first TMEM column of P G
 constexpr int kGBlock = kChunkSlots * 128;               // one 64-column block of the KV rows: 16 KiB
 constexpr int kQBlock = kHalfHeads * 128;                // one 64-column block of the query half: 4 KiB
-constexpr int kPBlock = kHalfHeads * 128;                // 64 slots of P for 32 heads: 4 KiB
+constexpr int kPBlock = 2 * kHalfHeads * 128;            // 64 slots of [P_hi; P_lo] (64 rows): 8 KiB
 static_assert(kCluster * kChunkSlots == 2 * kTopK, "4 chunks x 2 head halves per row");
 static_assert(kThreads == 512, "16 warps");
 
 struct TailLayout {
     static constexpr size_t g = 0;                                     // KV rows [128][512], K-major SW128
     static constexpr size_t q = g + 8 * (size_t)kGBlock;               // query half [32][512], K-major SW128
-    static constexpr size_t p_hi = q + 8 * (size_t)kQBlock;            // P [32 heads][128 slots], K-major SW128
-    static constexpr size_t p_lo = p_hi + 2 * (size_t)kPBlock;
-    static constexpr size_t idx = p_lo + 2 * (size_t)kPBlock;          // i32 [128] this chunk's slots
+    static constexpr size_t pmat = q + 8 * (size_t)kQBlock;            // [P_hi; P_lo] [64][128 slots], K-major SW128
+    static constexpr size_t idx = pmat + 2 * (size_t)kPBlock;          // i32 [128] this chunk's slots
     static constexpr size_t sel = idx + (size_t)kChunkSlots * 4;       // u64 [512] winners (leader)
     static constexpr size_t red = sel + (size_t)kTopK * 8;             // [4 quarters][32 heads] max, sum, bad
     static constexpr size_t misc = red + 3 * 4 * (size_t)kHalfHeads * 4;
@@ -105,8 +105,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     using T = TailLayout;
     uint8_t* g_s = smem + T::g;
     uint8_t* q_s = smem + T::q;
-    uint8_t* ph_s = smem + T::p_hi;
-    uint8_t* pl_s = smem + T::p_lo;
+    uint8_t* p_s = smem + T::pmat;
     int* idx_s = reinterpret_cast<int*>(smem + T::idx);
     uint64_t* sel = reinterpret_cast<uint64_t*>(smem + T::sel);
     float* red_max = reinterpret_cast<float*>(smem + T::red);
@@ -159,19 +158,27 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     if (p.given == nullptr) {
         // ---- select -------------------------------------------------------------
         const float* s = p.scores + (size_t)e * p.score_stride;
-        const Collected col = select_collect(s, L, W, p.hist + (size_t)e * kHistBins, rank, sm, leader);
+        // The candidates' KV rows go to L2 while the leader refines.
+        const Collected col = select_collect(s, L, W, p.hist + (size_t)e * kHistBins, rank, sm, leader,
+                                             reinterpret_cast<const uint8_t*>(p.kv[e]), kDim * 2);
         cluster.sync();  // every append into the leader is visible to it
+        uint64_t* sc = reinterpret_cast<uint64_t*>(smem + T::selcopy);
         if (rank == 0) {
+            // The leader refines, then pushes the winners (zero past the last) and
+            // their number into every CTA's shared memory.
             const uint32_t n = select_finish(col, s, L, W, false, nullptr, sm, sel, p.status);
-            if (t == 0) *nsel_s = n;
+            const uint64_t wv = (uint32_t)t < n ? sel[t] : 0ull;
+#pragma unroll
+            for (int r = 0; r < kCluster; ++r) {
+                cluster.map_shared_rank(sc, (unsigned)r)[t] = wv;
+                if (t == 0) *cluster.map_shared_rank(nsel_s, (unsigned)r) = n;
+            }
         }
         cluster.sync();  // the winners are visible to the cluster
 
         // ---- place: rank 64 winners, store them in their slots -------------------
-        const uint32_t nsel = *cluster.map_shared_rank(nsel_s, 0);
-        uint64_t* sc = reinterpret_cast<uint64_t*>(smem + T::selcopy);
+        const uint32_t nsel = *nsel_s;
         uint32_t* rk = reinterpret_cast<uint32_t*>(smem + T::ranks);
-        sc[t] = (uint32_t)t < nsel ? cluster.map_shared_rank(sel, 0)[t] : 0ull;
         if (t < 64) rk[t] = 0;
         // Slots of this chunk past the last winner are empty.
         if (t < kChunkSlots && c * kChunkSlots + (uint32_t)t >= nsel) idx_s[t] = -1;
@@ -279,10 +286,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
             const float w = l[i] == -INFINITY ? 0.0f : expf(l[i] - mh);
             const __nv_bfloat16 hi = __float2bfloat16_rn(w);
             const __nv_bfloat16 lo = __float2bfloat16_rn(w - __bfloat162float(hi));
+            // Row h holds P_hi, row 32 + h P_lo (same swizzle phase: 32 is a multiple of 8).
             const uint32_t off = (uint32_t)((slot >> 6) * kPBlock + h * 128 +
                                             ((((slot & 63) >> 3) ^ (h & 7)) << 4) + ((slot & 7) << 1));
-            *reinterpret_cast<__nv_bfloat16*>(ph_s + off) = hi;
-            *reinterpret_cast<__nv_bfloat16*>(pl_s + off) = lo;
+            *reinterpret_cast<__nv_bfloat16*>(p_s + off) = hi;
+            *reinterpret_cast<__nv_bfloat16*>(p_s + off + kHalfHeads * 128) = lo;
             sum[i] = w;
         }
 #pragma unroll
@@ -308,19 +316,17 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
                 atomicOr(&p.flags[e * kHeads + head0 + t], 1u);
         }
         if (t == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(128, kHalfHeads) | kIdescAMnMajor;
-            const uint32_t p_addr[2] = {smem_u32(ph_s), smem_u32(pl_s)};
+            constexpr uint32_t idesc = idesc_bf16_f32(128, 2 * kHalfHeads) | kIdescAMnMajor;
+            const uint32_t p_addr = smem_u32(p_s);
 #pragma unroll
             for (int b = 0; b < kDim / 128; ++b)
 #pragma unroll
-                for (int ks = 0; ks < kChunkSlots / 16; ++ks)
-#pragma unroll
-                    for (int hl = 0; hl < 2; ++hl) {
-                        // A: features [128 b, 128 b + 128) x slots [16 ks, 16 ks + 16), MN-major.
-                        const uint64_t ad = smem_desc_sw128_mnmajor(g_addr + 2 * b * kGBlock + ks * 2048, kGBlock, 1024);
-                        const uint64_t bd = smem_desc_sw128_kmajor(p_addr[hl] + (ks >> 2) * kPBlock + (ks & 3) * 32);
-                        umma_bf16(tmem + kPvCol + 32 * b, ad, bd, idesc, (ks | hl) != 0 ? 1u : 0u);
-                    }
+                for (int ks = 0; ks < kChunkSlots / 16; ++ks) {
+                    // A: features [128 b, 128 b + 128) x slots [16 ks, 16 ks + 16), MN-major.
+                    const uint64_t ad = smem_desc_sw128_mnmajor(g_addr + 2 * b * kGBlock + ks * 2048, kGBlock, 1024);
+                    const uint64_t bd = smem_desc_sw128_kmajor(p_addr + (ks >> 2) * kPBlock + (ks & 3) * 32);
+                    umma_bf16(tmem + kPvCol + 64 * b, ad, bd, idesc, ks != 0 ? 1u : 0u);
+                }
             umma_commit(mma_bar);
         }
         mbar_wait(mma_bar, 1, p.status);
@@ -328,12 +334,15 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
 
         // ---- partial: warp -> (32 features, 32 heads) of block warp / 4 -------------
         const int b = warp >> 2;
-        uint32_t a[32];
-        tmem_ld_x32(tmem + ((uint32_t)(32 * qt) << 16) + kPvCol + 32 * b, a);
+        uint32_t ahi[32], alo[32];
+        const uint32_t tcol = tmem + ((uint32_t)(32 * qt) << 16) + kPvCol + 64 * b;
+        tmem_ld_x32(tcol, ahi);
+        tmem_ld_x32(tcol + kHalfHeads, alo);
         tmem_ld_wait();
         float* pacc = part + 2 * kHalfHeads + 128 * b + 32 * qt + lane;
 #pragma unroll
-        for (int h = 0; h < kHalfHeads; ++h) pacc[(size_t)h * kDim] = __uint_as_float(a[h]);
+        for (int h = 0; h < kHalfHeads; ++h)
+            pacc[(size_t)h * kDim] = __uint_as_float(ahi[h]) + __uint_as_float(alo[h]);
     }
     tc_fence_before();
     cluster.sync();  // every chunk's partial and head flags are visible to the cluster

@@ -50,8 +50,9 @@ __device__ inline BinPick pick_bin(const uint32_t* h, uint32_t need, uint32_t* s
     if (t == 0) scratch[16] = 0xFFFFFFFFu;
     if (lane == 0) scratch[w] = x;
     __syncthreads();
-    uint32_t after = 0;
-    for (int w2 = w + 1; w2 < kThreads / 32; ++w2) after += scratch[w2];
+    uint32_t after = 0;  // elements in the bins of later warps (16 independent loads)
+#pragma unroll
+    for (int w2 = 0; w2 < kThreads / 32; ++w2) after += w2 > w ? scratch[w2] : 0u;
     const uint32_t excl = x - tot + after;  // elements in bins > 4t+3
     const uint32_t ge3 = excl + v3, ge2 = ge3 + v2, ge1 = ge2 + v1, ge0 = ge1 + v0;
     int b = -1;
@@ -105,12 +106,16 @@ constexpr int kCluster = 8;        // CTAs per row in the select kernel
 constexpr int kLeaderCap = 8192;   // candidates the leader CTA holds in shared memory
 constexpr int kBitmapWords = kLeaderCap * 2;  // the candidate space as a bitmap: rows up to 524288 keys
 
+constexpr uint32_t kRankDirect = 128;  // a threshold bin this small is ranked element by element
+
 struct SelectSmem {
-    uint32_t h[kHistBins];   // level-0 histogram (each CTA), then refinement levels (leader)
+    uint32_t h[kHistBins];   // level-0 histogram (each CTA), then refinement levels (leader),
+                             // then the threshold bin's elements when they are ranked directly
     uint32_t scratch[32];
     uint64_t cand[kLeaderCap];
     uint32_t ncand;
     uint32_t nsel;
+    uint32_t nres;
 };
 
 // Where the refinement stands: the last digit level fixed, the composite
@@ -120,6 +125,7 @@ struct Refine {
     int level;
     uint64_t prefix;
     uint32_t need;
+    uint32_t eq;    // elements in the prefix's bin
     bool done;      // the prefix's whole bin is taken
 };
 
@@ -129,6 +135,7 @@ __device__ __forceinline__ Refine refine_from_level0(const BinPick& l0, uint32_t
     r.level = 0;
     r.prefix = (uint64_t)(l0.bin < 0 ? 0 : l0.bin);
     r.need = r.take_all ? 0 : width - l0.gt;
+    r.eq = l0.eq;
     r.done = r.take_all || l0.eq == r.need;
     return r;
 }
@@ -188,19 +195,22 @@ __device__ __forceinline__ void write_winners(SelectSmem& sm, const uint64_t* se
     for (uint32_t k = nsel + t; k < width; k += kThreads) out[k] = -1;
 }
 
-// Refine digit by digit, keep the winners' composites in sel[0, 512) (zero
-// past the last) and write their indices to out (unless out is null).
-// Returns the number of winners.
+// Refine digit by digit until the threshold bin is taken whole or holds at
+// most kRankDirect elements, then keep the winners' composites in sel[0, 512)
+// (zero past the last): every element above the bin, and the `need` best of
+// the bin's elements, found by counting for each how many of them are better.
+// Writes their indices to out (unless out is null). Returns the number of winners.
 template <class Src>
 __device__ inline uint32_t finish_row(const Src& src, Refine st, uint32_t width, uint32_t L, bool by_index, int32_t* out,
-                               SelectSmem& sm, uint64_t* sel, uint32_t* status) {
+                                      SelectSmem& sm, uint64_t* sel, uint32_t* status) {
     const int t = threadIdx.x, lane = t & 31;
     const bool take_all = st.take_all;
     int level = st.level;
     uint64_t prefix = st.prefix;
     uint32_t need = st.need;
+    uint32_t eq = st.eq;
     bool done = st.done;
-    for (int lv = level + 1; lv < 6 && !done; ++lv) {
+    for (int lv = level + 1; lv < 6 && !done && eq > kRankDirect; ++lv) {
         const LevelSpec up = kLevels[lv - 1];
         const LevelSpec cur = kLevels[lv];
         const uint32_t mask = (1u << cur.bits) - 1;
@@ -215,32 +225,63 @@ __device__ inline uint32_t finish_row(const Src& src, Refine st, uint32_t width,
         const BinPick pk = pick_bin(sm.h, need, sm.scratch);
         if (pk.bin < 0) {  // inconsistent counts: keep what is certain
             if (t == 0) atomicOr(status, kStatusCandOverflow);
+            done = true;
             break;
         }
         need -= pk.gt;
         prefix = (prefix << cur.bits) | (uint64_t)pk.bin;
         level = lv;
+        eq = pk.eq;
         done = pk.eq == need;
     }
+    const bool direct = !done;  // the bin's eq (<= kRankDirect) elements are ranked below
     const int shift = kLevels[level].shift;
+    uint64_t* bin_el = reinterpret_cast<uint64_t*>(sm.h);  // the threshold bin's elements
 
-    if (t == 0) sm.nsel = 0;
+    if (t == 0) {
+        sm.nsel = 0;
+        sm.nres = 0;
+    }
     sel[t] = 0;  // below every finite element's composite
     __syncthreads();
     const uint32_t n = src.size();
     for (uint32_t base = 0; base < n; base += kThreads) {
         const uint32_t i = base + t;
         uint64_t c = 0;
-        const bool take = i < n && src.get(i, c) && (take_all || (c >> shift) >= prefix);
-        const uint32_t m = __ballot_sync(kFull, take);
+        const bool valid = i < n && src.get(i, c);
+        const uint64_t d = c >> shift;
+        const bool take = valid && (take_all || (direct ? d > prefix : d >= prefix));
+        const bool in_bin = valid && direct && !take_all && d == prefix;
+        uint32_t m = __ballot_sync(kFull, take);
         if (m) {
             uint32_t pos = 0;
             if (lane == 0) pos = atomicAdd(&sm.nsel, (uint32_t)__popc(m));
             pos = __shfl_sync(kFull, pos, 0) + __popc(m & ((1u << lane) - 1u));
             if (take && pos < (uint32_t)kTopK) sel[pos] = c;
         }
+        m = __ballot_sync(kFull, in_bin);
+        if (m) {
+            uint32_t pos = 0;
+            if (lane == 0) pos = atomicAdd(&sm.nres, (uint32_t)__popc(m));
+            pos = __shfl_sync(kFull, pos, 0) + __popc(m & ((1u << lane) - 1u));
+            if (in_bin && pos < kRankDirect) bin_el[pos] = c;
+        }
     }
     __syncthreads();
+    if (direct) {
+        const uint32_t nr = sm.nres < kRankDirect ? sm.nres : kRankDirect;
+        if (sm.nres != eq && t == 0) atomicOr(status, kStatusCandOverflow);
+        for (uint32_t k = t; k < nr; k += kThreads) {
+            const uint64_t ck = bin_el[k];
+            uint32_t better = 0;
+            for (uint32_t j = 0; j < nr; ++j) better += bin_el[j] > ck ? 1u : 0u;
+            if (better < need) {
+                const uint32_t pos = atomicAdd(&sm.nsel, 1u);
+                if (pos < (uint32_t)kTopK) sel[pos] = ck;
+            }
+        }
+        __syncthreads();
+    }
     const uint32_t got = sm.nsel;
     const uint32_t nsel = got < width ? got : width;
     if (got > width && t == 0) atomicOr(status, kStatusCandOverflow);
@@ -261,10 +302,13 @@ struct Collected {
 // its slice of the scores once and appends the candidates (finite, top 11 key
 // bits >= that bin) as composites into the leader's shared memory.
 // Before the call the leader's ncand is zero and visible cluster-wide; after
-// it a cluster barrier makes the appends visible to the leader.
+// it a cluster barrier makes the appends visible to the leader. With
+// `prefetch_rows`, each candidate j also asks L2 for the `row_bytes` bytes at
+// prefetch_rows + j * row_bytes (the rows a later stage gathers for winners).
 __device__ __forceinline__ Collected select_collect(const float* s, uint32_t L, uint32_t width,
                                                     const uint32_t* hist_row, uint32_t rank, SelectSmem& sm,
-                                                    SelectSmem& leader) {
+                                                    SelectSmem& leader, const uint8_t* prefetch_rows = nullptr,
+                                                    uint32_t row_bytes = 0) {
     const int t = threadIdx.x, lane = t & 31;
     // This CTA's slice: a multiple of 2048 scores (512 threads x float4).
     const uint32_t per = (((L + kCluster - 1) / kCluster) + 2047) & ~2047u;
@@ -334,6 +378,7 @@ __device__ __forceinline__ Collected select_collect(const float* s, uint32_t L, 
                     const uint32_t j = base + 4 * t + 4 * kThreads * (i >> 2) + (i & 3);
                     if (at < (uint32_t)kLeaderCap) leader.cand[at] = composite(score_key(v[i]), j);
                     ++at;
+                    if (prefetch_rows) bulk_prefetch_l2(prefetch_rows + (size_t)j * row_bytes, row_bytes);
                 }
             }
         }
