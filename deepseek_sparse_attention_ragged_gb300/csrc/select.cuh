@@ -302,13 +302,10 @@ struct Collected {
 // its slice of the scores once and appends the candidates (finite, top 11 key
 // bits >= that bin) as composites into the leader's shared memory.
 // Before the call the leader's ncand is zero and visible cluster-wide; after
-// it a cluster barrier makes the appends visible to the leader. With
-// `prefetch_rows`, each candidate j also asks L2 for the `row_bytes` bytes at
-// prefetch_rows + j * row_bytes (the rows a later stage gathers for winners).
+// it a cluster barrier makes the appends visible to the leader.
 __device__ __forceinline__ Collected select_collect(const float* s, uint32_t L, uint32_t width,
                                                     const uint32_t* hist_row, uint32_t rank, SelectSmem& sm,
-                                                    SelectSmem& leader, const uint8_t* prefetch_rows = nullptr,
-                                                    uint32_t row_bytes = 0) {
+                                                    SelectSmem& leader) {
     const int t = threadIdx.x, lane = t & 31;
     // This CTA's slice: a multiple of 2048 scores (512 threads x float4).
     const uint32_t per = (((L + kCluster - 1) / kCluster) + 2047) & ~2047u;
@@ -378,7 +375,6 @@ __device__ __forceinline__ Collected select_collect(const float* s, uint32_t L, 
                     const uint32_t j = base + 4 * t + 4 * kThreads * (i >> 2) + (i & 3);
                     if (at < (uint32_t)kLeaderCap) leader.cand[at] = composite(score_key(v[i]), j);
                     ++at;
-                    if (prefetch_rows) bulk_prefetch_l2(prefetch_rows + (size_t)j * row_bytes, row_bytes);
                 }
             }
         }
