@@ -158,7 +158,6 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     if (p.given == nullptr) {
         // ---- select -------------------------------------------------------------
         const float* s = p.scores + (size_t)e * p.score_stride;
-        // The candidates' KV rows go to L2 while the leader refines.
         const Collected col = select_collect(s, L, W, p.hist + (size_t)e * kHistBins, rank, sm, leader);
         cluster.sync();  // every append into the leader is visible to it
         uint64_t* sc = reinterpret_cast<uint64_t*>(smem + T::selcopy);
