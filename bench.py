@@ -31,6 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+INDEXER_DRAM_BYTES_8x131072 = 268_653_056 + 3_817_216
 CONFIG_INDEX = 3
 METRIC = "decode rows/s (8 rows, 128K ctx) and achieved HBM GB/s vs GB300 peak"
 
@@ -317,6 +318,9 @@ def main():
     idx_bytes = sum(256 * r.kv_len + 4 * r.kv_len + 16384 + 256 for r in wl.rows)
     peak, peak_kind = peaks()
     idx_gbs = idx_bytes / (idx_ms / 1e3) / 1e9
+    # DRAM bytes of one indexer launch on this workload, read + written, from an
+    # ncu capture of the current kernel (dram__bytes_read.sum + dram__bytes_write.sum).
+    idx_traffic = INDEXER_DRAM_BYTES_8x131072 if args.config == CONFIG_INDEX else None
 
     # End to end through the public call: per step the queries, head weights and
     # sinks go host->device from pinned memory, the output comes back (caches stay
@@ -367,7 +371,7 @@ def main():
             "step_gbs": step_gbs, "step_frac_of_peak": step_gbs / peak,
             "algorithmic_bytes_per_step": alg_bytes,
             "roofline": {"kernel": "indexer_score_kernel", "bound": "hbm", "achieved": idx_gbs, "peak": peak,
-                         "peak_kind": peak_kind, "unit": "GB/s", "frac": idx_gbs / peak, "traffic": None,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": idx_gbs / peak, "traffic": idx_traffic,
                          "bytes_per_launch": idx_bytes, "ms_per_launch": idx_ms},
             "e2e": {"value": world * R / (e2e_ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},

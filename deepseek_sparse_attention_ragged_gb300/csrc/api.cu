@@ -46,7 +46,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 struct Layout {
     size_t status = 0;  // u32 status word at offset 0
     size_t hist, flags, ctl_end;
-    size_t topk, part, scores, total;
+    size_t part, scores, total;
     uint32_t attn_chunks;
     uint64_t score_stride;  // floats per row of the decode scores
 };
@@ -56,15 +56,14 @@ Layout make_layout(int rows, const ds_row_t* table) {
     L.hist = 256;
     L.flags = align256(L.hist + (size_t)kRowsMax * kHistBins * 4);
     L.ctl_end = align256(L.flags + ((size_t)kRowsMax * kHeads + kRowsMax) * 4);
-    L.topk = L.ctl_end;
-    L.part = align256(L.topk + (size_t)kRowsMax * kTopK * 4);
+    L.part = L.ctl_end;
     uint32_t chunks = 0, max_len = 0;
     for (int e = 0; e < rows; ++e) {
-        chunks += (table[e].width + kAttnSlots - 1) / kAttnSlots;
+        chunks += (table[e].width + kTailChunkSlots - 1) / kTailChunkSlots;
         if (table[e].kv_len > max_len) max_len = table[e].kv_len;
     }
     L.attn_chunks = chunks;
-    L.scores = align256(L.part + 2 * (size_t)chunks * kPartFloats * 4);  // two head halves
+    L.scores = align256(L.part + 2 * (size_t)chunks * kPartFloats * 4);  // two head halves per chunk
     L.score_stride = ((uint64_t)max_len + 63) & ~uint64_t(63);
     L.total = align256(L.scores + (size_t)rows * L.score_stride * 4);
     return L;

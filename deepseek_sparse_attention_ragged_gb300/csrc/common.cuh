@@ -31,13 +31,12 @@ constexpr uint64_t kWaitBudgetNs = 2000000000ull;
 // ---------------------------------------------------------------------------
 //   [0, 256)                 control: u32 status, pad
 //   hist   [8][2048] u32     level-0 histogram of score keys per entry
-//   flags  [8][64]  u32      per-entry, per-head attention invalid bits
-//   topk   [8][512] i32      the decode's selection (ascending index order)
-//   part   [chunks][...]     attention partials
+//   flags  [8][64 + 1] u32   per-entry, per-head attention invalid bits, row bits
+//   part   [chunks][2][...]  attention partials: m[32], l[32], acc[32][512] per
+//                            (128-slot chunk, head half)
 //   scores [8][stride] f32   indexer scores (decode only)
 constexpr int kHistBins = 2048;
-constexpr int kAttnSlots = 64;                       // selected slots per attention CTA
-constexpr int kAttnChunksMax = kTopK / kAttnSlots;   // 8
+constexpr int kAttnChunksMax = 8;                    // bound on a row's attention chunks
 // One attention partial (a chunk of one head half): m[32], l[32], acc[32][512] (fp32).
 constexpr size_t kPartFloats = 32 + 32 + (size_t)(kHeads / 2) * kDim;
 
