@@ -24,6 +24,7 @@ __all__ = [
     "DsRowsError", "Row", "load", "build", "library_path",
     "ds_rows_workspace_bytes", "workspace", "ds_rows_indexer_score", "ds_rows_topk", "ds_rows_topk_static",
     "ds_rows_sparse_attn", "ds_rows_decode", "ds_rows_version",
+    "IndexerRow", "ds_rows_indexer_topk_workspace_bytes", "indexer_topk_workspace", "ds_rows_indexer_topk",
     "ROWS_MAX", "INDEX_HEADS", "INDEX_DIM", "TOP_K", "HEADS", "DIM",
 ]
 
@@ -50,6 +51,13 @@ class Row(ctypes.Structure):
 
     _fields_ = [("kv_len", ctypes.c_uint32), ("width", ctypes.c_uint32),
                 ("index_offset", ctypes.c_uint32), ("q_row", ctypes.c_uint32)]
+
+
+class IndexerRow(ctypes.Structure):
+    """One positioned indexer row: ds_indexer_row_t {kv_len, start_pos, offset, q_row, output_offset}."""
+
+    _fields_ = [("kv_len", ctypes.c_uint32), ("start_pos", ctypes.c_uint32), ("offset", ctypes.c_int32),
+                ("q_row", ctypes.c_uint32), ("output_offset", ctypes.c_uint32)]
 
 
 class _RowSet(ctypes.Structure):
@@ -93,6 +101,10 @@ def load():
     lib.ds_rows_sparse_attn.restype = i32
     lib.ds_rows_decode.argtypes = [rs, vp, vp, vp, vp, sz, ctypes.c_float, vp, vp, u32p, vp, sz, vp]
     lib.ds_rows_decode.restype = i32
+    lib.ds_rows_indexer_topk_workspace_bytes.argtypes = [i32, ctypes.POINTER(IndexerRow)]
+    lib.ds_rows_indexer_topk_workspace_bytes.restype = sz
+    lib.ds_rows_indexer_topk.argtypes = [i32, ctypes.POINTER(IndexerRow), ctypes.POINTER(vp), vp, vp, vp, vp, sz, vp]
+    lib.ds_rows_indexer_topk.restype = i32
     lib.ds_rows_last_error.argtypes = []
     lib.ds_rows_last_error.restype = ctypes.c_char_p
     lib.ds_rows_version.argtypes = []
@@ -292,3 +304,55 @@ def ds_rows_decode(rows, q_index, w_index, index_keys, q_attn, kv, sinks, sinks_
     _check(lib, lib.ds_rows_decode(ctypes.byref(rs), _ptr(q_index), _ptr(w_index), _ptr(q_attn), _ptr(sinks),
                                    int(sinks_row_stride), float(scale), _ptr(out), _ptr(indices), _ptr(invalid),
                                    _ptr(workspace_t), workspace_t.numel(), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# positioned indexer + causal top-512
+# ---------------------------------------------------------------------------
+
+def _indexer_table(rows):
+    rows = list(rows)
+    arr = (IndexerRow * max(1, len(rows)))()
+    for i, r in enumerate(rows):
+        if isinstance(r, IndexerRow):
+            arr[i] = r
+        elif hasattr(r, "start_pos"):
+            arr[i] = IndexerRow(r.kv_len, r.start_pos, r.offset, r.q_row, r.output_offset)
+        else:
+            arr[i] = IndexerRow(*r)
+    return arr, len(rows)
+
+
+def ds_rows_indexer_topk_workspace_bytes(rows) -> int:
+    lib = load()
+    tab, n = _indexer_table(rows)
+    b = lib.ds_rows_indexer_topk_workspace_bytes(n, tab)
+    if b == 0:
+        raise DsRowsError(-1, lib.ds_rows_last_error().decode())
+    return int(b)
+
+
+def indexer_topk_workspace(rows, device=None) -> torch.Tensor:
+    """A workspace tensor for ds_rows_indexer_topk (uint8, 256-byte aligned)."""
+    return torch.empty(ds_rows_indexer_topk_workspace_bytes(rows), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def ds_rows_indexer_topk(rows, q_index, w_index, index_keys, indices, workspace_t=None, stream=None):
+    """Positioned indexer score and causal top-512 of each row (IndexerRow entries):
+    512 indices (+ offset, -1 fill) per row at output_offset."""
+    lib = load()
+    tab, n = _indexer_table(rows)
+    q_rows = max(tab[e].q_row for e in range(n)) + 1
+    _require(q_index, "q_index", torch.bfloat16, q_rows * INDEX_HEADS * INDEX_DIM)
+    _require(w_index, "w_index", torch.float32, q_rows * INDEX_HEADS)
+    if len(index_keys) != n:
+        raise ValueError(f"index_keys: {len(index_keys)} caches for {n} rows")
+    for e in range(n):
+        _require(index_keys[e], f"index_keys[{e}]", torch.bfloat16, tab[e].kv_len * INDEX_DIM)
+    _require(indices, "indices", torch.int32, max(tab[e].output_offset for e in range(n)) + TOP_K)
+    if workspace_t is None:
+        workspace_t = indexer_topk_workspace(list(tab)[:n], q_index.device)
+    ks = (ctypes.c_void_p * n)(*[k.data_ptr() for k in index_keys])
+    _check(lib, lib.ds_rows_indexer_topk(n, tab, ks, _ptr(q_index), _ptr(w_index), _ptr(indices),
+                                         _ptr(workspace_t), workspace_t.numel(), _stream(stream)))

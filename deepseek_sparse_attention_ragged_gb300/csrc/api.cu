@@ -51,7 +51,7 @@ struct Layout {
     uint64_t score_stride;  // floats per row of the decode scores
 };
 
-Layout make_layout(int rows, const ds_row_t* table) {
+Layout make_layout(int rows, const ds_row_t* table, bool attention = true) {
     Layout L;
     L.hist = 256;
     L.flags = align256(L.hist + (size_t)kRowsMax * kHistBins * 4);
@@ -62,6 +62,7 @@ Layout make_layout(int rows, const ds_row_t* table) {
         chunks += (table[e].width + kTailChunkSlots - 1) / kTailChunkSlots;
         if (table[e].kv_len > max_len) max_len = table[e].kv_len;
     }
+    if (!attention) chunks = 0;
     L.attn_chunks = chunks;
     L.scores = align256(L.part + 2 * (size_t)chunks * kPartFloats * 4);  // two head halves per chunk
     L.score_stride = ((uint64_t)max_len + 63) & ~uint64_t(63);
@@ -156,6 +157,52 @@ int check_set(const ds_row_set_t* set, unsigned needs) {
     return DS_OK;
 }
 
+// Positioned indexer rows (`dispatch_deepseek_indexer_rows`): kv_len nonzero and
+// not shorter than the causal count (start_pos + 1) / 4; offset nonnegative and
+// offset + count - 1 within int32; 512-slot outputs disjoint.
+int check_indexer_rows(int rows, const ds_indexer_row_t* table, const ds_bf16* const* keys, bool need_keys) {
+    if (rows < 1 || rows > DS_ROWS_MAX) return fail(DS_EINVAL, "rows must be 1..=%d, got %d", DS_ROWS_MAX, rows);
+    if (!table) return fail(DS_EINVAL, "indexer row table is NULL");
+    if (need_keys && !keys) return fail(DS_EINVAL, "index_keys is NULL");
+    for (int e = 0; e < rows; ++e) {
+        const ds_indexer_row_t& r = table[e];
+        if (r.kv_len == 0) return fail(DS_EINVAL, "indexer row %d: kv_len must be nonzero", e);
+        if (r.start_pos == 0xFFFFFFFFu) return fail(DS_EINVAL, "indexer row %d: position overflows", e);
+        const uint32_t causal = (r.start_pos + 1) / 4;
+        if (r.kv_len < causal)
+            return fail(DS_EINVAL, "indexer row %d: kv_len %u is shorter than %u causal compressed entries", e,
+                        r.kv_len, causal);
+        if (r.offset < 0)
+            return fail(DS_EINVAL, "indexer row %d: offset must be nonnegative; -1 is reserved for the sentinel", e);
+        if (causal > 0 && (int64_t)r.offset + (int64_t)causal - 1 > (int64_t)INT32_MAX)
+            return fail(DS_EINVAL, "indexer row %d: offset plus compressed index exceeds i32", e);
+        if ((uint64_t)r.output_offset + DS_TOPK > 0xFFFFFFFFull)
+            return fail(DS_ESIZE, "indexer row %d: output range exceeds u32", e);
+        if ((uint64_t)r.q_row * DS_INDEX_HEADS * DS_INDEX_DIM > 0xFFFFFFFFFFull)
+            return fail(DS_ESIZE, "indexer row %d: q_row %u is out of range", e, r.q_row);
+        if (need_keys) {
+            if (!keys[e]) return fail(DS_EINVAL, "indexer row %d: keys are NULL", e);
+            if (!aligned16(keys[e])) return fail(DS_EALIGN, "indexer row %d: keys not 16-B aligned", e);
+        }
+        for (int o = 0; o < e; ++o) {
+            const uint64_t a0 = r.output_offset, a1 = a0 + DS_TOPK;
+            const uint64_t b0 = table[o].output_offset, b1 = b0 + DS_TOPK;
+            if (a0 < b1 && b0 < a1) return fail(DS_EINVAL, "indexer outputs of rows %d and %d overlap", o, e);
+        }
+    }
+    return DS_OK;
+}
+
+// The selection table of positioned rows: kv_len = the causal count, 512 slots.
+void indexer_selection_table(int rows, const ds_indexer_row_t* table, ds_row_t* sel) {
+    for (int e = 0; e < rows; ++e) {
+        sel[e].kv_len = (table[e].start_pos + 1) / 4;
+        sel[e].width = DS_TOPK;
+        sel[e].index_offset = table[e].output_offset;
+        sel[e].q_row = table[e].q_row;
+    }
+}
+
 int check_workspace(const ds_row_set_t* set, void* ws, size_t bytes, const Layout& L) {
     (void)set;
     if (!ws) return fail(DS_EINVAL, "workspace is NULL");
@@ -171,8 +218,11 @@ uint32_t max_q_row(const ds_row_set_t* set) {
 }
 
 // ---- stage launchers ---------------------------------------------------------------
+// With `valid`, entry e scores only its keys j < valid[e] (the tensor map still
+// spans the row's kv_len keys).
 int run_indexer(const ds_row_set_t* set, const ds_bf16* q_index, const float* w_index, float* scores,
-                uint64_t stride, uint32_t* hist, uint32_t* status, cudaStream_t stream, bool pdl) {
+                uint64_t stride, uint32_t* hist, uint32_t* status, cudaStream_t stream, bool pdl,
+                const uint32_t* valid = nullptr) {
     int rc = get_encoder();
     if (rc) return rc;
     IndexerParams p;  // ~1.3 KB with the tensor maps; built per call on the host
@@ -181,10 +231,11 @@ int run_indexer(const ds_row_set_t* set, const ds_bf16* q_index, const float* w_
     uint32_t tiles = 0;
     for (int e = 0; e < set->rows; ++e) {
         const ds_row_t& r = set->table[e];
-        p.kv_len[e] = r.kv_len;
+        const uint32_t n = valid ? valid[e] : r.kv_len;
+        p.kv_len[e] = n;
         p.q_row[e] = r.q_row;
         p.tile_begin[e] = tiles;
-        tiles += (r.kv_len + tile - 1) / tile;
+        tiles += (n + tile - 1) / tile;
         rc = encode_rows128(&p.kmap[e], set->index_keys[e], r.kv_len, 128, "indexer keys");
         if (rc) return rc;
     }
@@ -204,7 +255,8 @@ int run_indexer(const ds_row_set_t* set, const ds_bf16* q_index, const float* w_
 }
 
 int run_topk(const ds_row_set_t* set, const float* scores, uint64_t stride, int32_t* out, const uint32_t* out_offset,
-             uint8_t* ws, const Layout& L, bool with_hist, bool by_index, cudaStream_t stream) {
+             uint8_t* ws, const Layout& L, bool with_hist, bool by_index, cudaStream_t stream,
+             const int32_t* offsets = nullptr) {
     TopkParams p;
     std::memset(&p, 0, sizeof(p));
     const uint32_t chunk = topk_chunk();
@@ -213,6 +265,7 @@ int run_topk(const ds_row_set_t* set, const float* scores, uint64_t stride, int3
         p.kv_len[e] = set->table[e].kv_len;
         p.width[e] = set->table[e].width;
         p.out_offset[e] = out_offset[e];
+        p.offset[e] = offsets ? offsets[e] : 0;
         p.chunk_begin[e] = chunks;
         chunks += (set->table[e].kv_len + chunk - 1) / chunk;
     }
@@ -444,6 +497,49 @@ int ds_rows_topk_static(const ds_row_set_t* set, const float* scores, size_t sco
     uint32_t off[DS_ROWS_MAX];
     for (int e = 0; e < set->rows; ++e) off[e] = set->table[e].index_offset;
     return run_topk(set, scores, score_stride, indices, off, ws, L, true, false, s);
+}
+
+size_t ds_rows_indexer_topk_workspace_bytes(int rows, const ds_indexer_row_t* table) {
+    if (check_indexer_rows(rows, table, nullptr, false)) return 0;
+    ds_row_t sel[DS_ROWS_MAX];
+    indexer_selection_table(rows, table, sel);
+    return make_layout(rows, sel, false).total;
+}
+
+int ds_rows_indexer_topk(int rows, const ds_indexer_row_t* table, const ds_bf16* const* index_keys,
+                         const ds_bf16* q_index, const float* w_index, int32_t* indices, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    int rc = check_indexer_rows(rows, table, index_keys, true);
+    if (rc) return rc;
+    rc = check_indexer_args(q_index, w_index);
+    if (rc) return rc;
+    if (!indices) return fail(DS_EINVAL, "indices is NULL");
+    ds_row_t keys_tab[DS_ROWS_MAX], sel_tab[DS_ROWS_MAX];
+    uint32_t valid[DS_ROWS_MAX], out_off[DS_ROWS_MAX];
+    int32_t offsets[DS_ROWS_MAX];
+    indexer_selection_table(rows, table, sel_tab);
+    for (int e = 0; e < rows; ++e) {
+        keys_tab[e] = sel_tab[e];
+        keys_tab[e].kv_len = table[e].kv_len;  // the tensor map spans the whole cache
+        valid[e] = sel_tab[e].kv_len;
+        out_off[e] = table[e].output_offset;
+        offsets[e] = table[e].offset;
+    }
+    const Layout L = make_layout(rows, sel_tab, false);
+    const ds_row_set_t kset = {rows, keys_tab, index_keys, nullptr};
+    const ds_row_set_t sset = {rows, sel_tab, nullptr, nullptr};
+    rc = check_workspace(&sset, workspace, workspace_bytes, L);
+    if (rc) return rc;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t err = launch_clear(reinterpret_cast<uint32_t*>(ws), (uint32_t)(L.ctl_end / 4), s);
+    if (err != cudaSuccess) return cuda_fail(err, "workspace clear");
+    float* scores = reinterpret_cast<float*>(ws + L.scores);
+    rc = run_indexer(&kset, q_index, w_index, scores, L.score_stride, reinterpret_cast<uint32_t*>(ws + L.hist),
+                     reinterpret_cast<uint32_t*>(ws + L.status), s, true, valid);
+    if (rc) return rc;
+    // The indexer built the level-0 histogram of the valid scores.
+    return run_topk(&sset, scores, L.score_stride, indices, out_off, ws, L, false, false, s, offsets);
 }
 
 const char* ds_rows_last_error(void) { return g_error.c_str(); }

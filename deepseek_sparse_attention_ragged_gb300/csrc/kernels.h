@@ -40,6 +40,7 @@ struct TopkParams {
     uint32_t width[DS_ROWS_MAX];
     uint32_t out_offset[DS_ROWS_MAX];
     uint32_t chunk_begin[DS_ROWS_MAX];
+    int32_t offset[DS_ROWS_MAX];   // added to every emitted index (positioned indexer)
 };
 
 // Selection (decode) and attention, one 8-CTA cluster per row; with `given`,

@@ -140,12 +140,13 @@ __device__ __forceinline__ Refine refine_from_level0(const BinPick& l0, uint32_t
     return r;
 }
 
-// Write the nsel winners of sel (composites) to out[0, width), then -1; `out`
-// may point to global or shared memory, and sel is left unchanged.
+// Write the nsel winners of sel (composites), as index + offset, to
+// out[0, width), then -1; `out` may point to global or shared memory, and sel
+// is left unchanged.
 // Best first: sorted by composite. Index order (ascending): through a bitmap of
 // the row's L positions in the candidate space when it fits, else sorted by index.
 __device__ __forceinline__ void write_winners(SelectSmem& sm, const uint64_t* sel, uint32_t nsel, uint32_t width,
-                                              uint32_t L, bool by_index, int32_t* out) {
+                                              uint32_t L, bool by_index, int32_t* out, int32_t offset) {
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const uint32_t words = (L + 31) / 32;
     if (!by_index || words > (uint32_t)kBitmapWords) {
@@ -155,7 +156,7 @@ __device__ __forceinline__ void write_winners(SelectSmem& sm, const uint64_t* se
         uint64_t x[1] = {by_index ? (uint64_t)(uint32_t)c : c};
         __syncthreads();  // every thread holds its element before the buffer is reused
         sort512_desc<kThreads>(x, sm.cand);  // the candidates are consumed
-        if ((uint32_t)t < width) out[t] = (uint32_t)t < nsel ? (int32_t)(~(uint32_t)x[0]) : -1;
+        if ((uint32_t)t < width) out[t] = (uint32_t)t < nsel ? (int32_t)(~(uint32_t)x[0]) + offset : -1;
         return;
     }
     uint32_t* bm = reinterpret_cast<uint32_t*>(sm.cand);  // the candidates are consumed
@@ -188,7 +189,7 @@ __device__ __forceinline__ void write_winners(SelectSmem& sm, const uint64_t* se
         while (bits) {
             const int b = __ffs(bits) - 1;
             bits &= bits - 1;
-            if (at < width) out[at] = (int32_t)(32 * w + b);
+            if (at < width) out[at] = (int32_t)(32 * w + b) + offset;
             ++at;
         }
     }
@@ -202,7 +203,7 @@ __device__ __forceinline__ void write_winners(SelectSmem& sm, const uint64_t* se
 // Writes their indices to out (unless out is null). Returns the number of winners.
 template <class Src>
 __device__ inline uint32_t finish_row(const Src& src, Refine st, uint32_t width, uint32_t L, bool by_index, int32_t* out,
-                                      SelectSmem& sm, uint64_t* sel, uint32_t* status) {
+                                      SelectSmem& sm, uint64_t* sel, uint32_t* status, int32_t offset = 0) {
     const int t = threadIdx.x, lane = t & 31;
     const bool take_all = st.take_all;
     int level = st.level;
@@ -285,7 +286,7 @@ __device__ inline uint32_t finish_row(const Src& src, Refine st, uint32_t width,
     const uint32_t got = sm.nsel;
     const uint32_t nsel = got < width ? got : width;
     if (got > width && t == 0) atomicOr(status, kStatusCandOverflow);
-    if (out) write_winners(sm, sel, nsel, width, L, by_index, out);
+    if (out) write_winners(sm, sel, nsel, width, L, by_index, out, offset);
     return nsel;
 }
 
@@ -386,7 +387,7 @@ __device__ __forceinline__ Collected select_collect(const float* s, uint32_t L, 
 // cluster barrier: refine, keep the winners in sel and write their indices.
 __device__ __forceinline__ uint32_t select_finish(const Collected& c, const float* s, uint32_t L, uint32_t width,
                                                   bool by_index, int32_t* out, SelectSmem& sm, uint64_t* sel,
-                                                  uint32_t* status) {
+                                                  uint32_t* status, int32_t offset = 0) {
     if (c.fast) {
         const uint32_t got = sm.ncand;
         const uint32_t n_cand = c.take_all ? c.l0.total : c.l0.gt + c.l0.eq;
@@ -395,9 +396,10 @@ __device__ __forceinline__ uint32_t select_finish(const Collected& c, const floa
         l0f.bin = (int)c.b0;
         const Refine st = refine_from_level0(l0f, width);
         return finish_row(SmemCandSource{sm.cand, got < (uint32_t)kLeaderCap ? got : (uint32_t)kLeaderCap}, st, width,
-                          L, by_index, out, sm, sel, status);
+                          L, by_index, out, sm, sel, status, offset);
     }
-    return finish_row(RowSource{s, L}, refine_from_level0(c.l0, width), width, L, by_index, out, sm, sel, status);
+    return finish_row(RowSource{s, L}, refine_from_level0(c.l0, width), width, L, by_index, out, sm, sel, status,
+                      offset);
 }
 
 }  // namespace rowsel

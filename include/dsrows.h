@@ -175,15 +175,61 @@ int ds_rows_sparse_attn(const ds_row_set_t* set, const ds_bf16* q_attn, const fl
 
 /*
  * The whole decode step: (1) indexer score -> (2) top-`width` -> (3)+(4)
- * gather and sink attention, on one stream. Scores and candidate lists stay
- * in the workspace. Arguments as in the stages above; `indices` is optional
- * (NULL keeps them in the workspace) and, when given, receives the selected
- * indices at each entry's index_offset (ranges must not overlap).
+ * gather and sink attention, on one stream. Scores and the selection stay in
+ * the workspace. Arguments as in the stages above; `indices` is optional
+ * (NULL: the selection is not written out) and, when given, receives the
+ * selected indices best first at each entry's index_offset (ranges must not
+ * overlap). The attention takes the slots in that best-first order, so `out`
+ * is bitwise what ds_rows_sparse_attn gives on those indices.
  */
 int ds_rows_decode(const ds_row_set_t* set, const ds_bf16* q_index, const float* w_index,
                    const ds_bf16* q_attn, const float* sinks, size_t sinks_row_stride,
                    float scale, ds_bf16* out, int32_t* indices, uint32_t* invalid,
                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * One row of a positioned indexer call (`DeepSeekIndexerRow`; compression
+ * ratio 4, one query per row):
+ *   kv_len        compressed keys in the row's indexer cache (> 0).
+ *   start_pos     the query's absolute position. The row's valid keys are
+ *                 j < valid_count = (start_pos + 1) / 4; kv_len must be at
+ *                 least valid_count (start_pos < 2^32 - 1).
+ *   offset        added to every emitted index: >= 0, and
+ *                 offset + valid_count - 1 must fit int32 (-1 is the sentinel).
+ *   q_row         row of the [*, 64, 128] queries and [*, 64] head weights.
+ *   output_offset element offset of the row's 512 output indices; the ranges
+ *                 [output_offset, output_offset + 512) must not overlap.
+ */
+typedef struct {
+    uint32_t kv_len;
+    uint32_t start_pos;
+    int32_t offset;
+    uint32_t q_row;
+    uint32_t output_offset;
+} ds_indexer_row_t;
+
+/* Workspace bytes for ds_rows_indexer_topk with this table; 0 when the table
+ * is invalid (see ds_rows_last_error). 256-byte aligned, scratch between calls. */
+size_t ds_rows_indexer_topk_workspace_bytes(int rows, const ds_indexer_row_t* table);
+
+/*
+ * (1)+(2) Positioned indexer and causal top-512 (`dispatch_deepseek_indexer_rows`:
+ * `deepseek_indexer_score_mma_rows_bf16` with its valid_count, then
+ * `deepseek_indexer_topk_block/merge/finalize_rows_i32`). For each entry e, with
+ * valid_count = min(kv_len, (start_pos + 1) / 4):
+ *   s[j] = sum_{h<64} w_index[q_row, h] * max(0, q_index[q_row, h, :] . K_e[j, :])
+ * for j < valid_count (keys at or past valid_count take no part), and
+ *   indices[output_offset + t], t < 512 = the t-th best j (score descending,
+ *   then lower index, finite scores only) plus offset, for t < valid_count when
+ *   such a j exists; every other slot is -1.
+ *   index_keys  host array of `rows` device pointers: bf16 [kv_len, 128] (16-B aligned).
+ *   q_index     bf16 [Q, 64, 128] (16-B aligned); w_index fp32 [Q, 64].
+ *   indices     int32, 512 per entry at output_offset.
+ *   workspace   at least ds_rows_indexer_topk_workspace_bytes(...) bytes.
+ */
+int ds_rows_indexer_topk(int rows, const ds_indexer_row_t* table, const ds_bf16* const* index_keys,
+                         const ds_bf16* q_index, const float* w_index, int32_t* indices,
+                         void* workspace, size_t workspace_bytes, void* stream);
 
 /* Message of the last failed call on this host thread ("" if none). */
 const char* ds_rows_last_error(void);

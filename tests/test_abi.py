@@ -166,3 +166,51 @@ def test_python_binding_checks_tensors():
         ds._require(torch.zeros(4, dtype=torch.float32), "x", torch.bfloat16, 4)
     with pytest.raises(ValueError):
         ds._require(torch.zeros(4, dtype=torch.bfloat16), "x", torch.bfloat16, 4)  # not CUDA
+
+
+# ---------------------------------------------------------------------------
+# positioned indexer rows (dispatch_deepseek_indexer_rows checks)
+# ---------------------------------------------------------------------------
+
+def _indexer_topk(lib, rows, ws_bytes=1 << 30, ws=FAKE, keys=True, q=FAKE):
+    tab, n = ds._indexer_table(rows)
+    ptrs = (ctypes.c_void_p * max(1, n))(*[FAKE + 4096 * i for i in range(n)])
+    return lib.ds_rows_indexer_topk(n, tab, ptrs if keys else None, q, FAKE, FAKE, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("row,msg", [
+    ((0, 1, 0, 0, 0), "kv_len must be nonzero"),
+    ((10, 100, 0, 0, 0), "shorter than 25 causal compressed entries"),
+    ((10, 3, -1, 0, 0), "offset must be nonnegative"),
+    ((10, 0xFFFFFFFF, 0, 0, 0), "position overflows"),
+    ((10, 39, 2**31 - 5, 0, 0), "offset plus compressed index exceeds i32"),
+    ((10, 3, 0, 0, 0xFFFFFF00), "output range exceeds u32"),
+])
+def test_indexer_row_checks(lib, row, msg):
+    assert _indexer_topk(lib, [row]) in (-1, -2)
+    assert msg in _err(lib)
+    tab, n = ds._indexer_table([row])
+    assert lib.ds_rows_indexer_topk_workspace_bytes(n, tab) == 0
+
+
+def test_indexer_rows_edges_accepted(lib):
+    # valid_count = (start_pos + 1) / 4 may be 0 (no valid key) or equal kv_len.
+    for row in [(10, 2, 0, 0, 0), (10, 39, 0, 0, 0), (10, 39, 2**31 - 10, 0, 0)]:
+        tab, n = ds._indexer_table([row])
+        assert lib.ds_rows_indexer_topk_workspace_bytes(n, tab) > 0, _err(lib)
+
+
+def test_indexer_rows_outputs_disjoint_and_counts(lib):
+    assert _indexer_topk(lib, [(600, 2399, 0, 0, 0), (600, 2399, 0, 1, 511)]) == -1
+    assert "overlap" in _err(lib)
+    rows9 = [(10, 39, 0, 0, 512 * i) for i in range(9)]
+    assert _indexer_topk(lib, rows9) == -1 and "rows must be 1..=8" in _err(lib)
+
+
+def test_indexer_rows_pointers_and_workspace(lib):
+    rows = [(600, 2399, 0, 0, 0)]
+    assert _indexer_topk(lib, rows, keys=False) == -1 and "index_keys is NULL" in _err(lib)
+    assert _indexer_topk(lib, rows, q=FAKE + 2) == -3
+    need = ds.ds_rows_indexer_topk_workspace_bytes(rows)
+    assert _indexer_topk(lib, rows, ws_bytes=need - 1) == -2 and "workspace holds" in _err(lib)
+    assert _indexer_topk(lib, rows, ws=FAKE + 16) == -3
