@@ -22,7 +22,9 @@
 //      reads its chunk's slots instead;
 //   3. attend, on tcgen05 tensor cores with fp32 accumulators in TMEM: gather
 //      the chunk's 128 KV rows into the 128-byte-swizzled K-major layout, then
-//        logits  D[128 slots x 32 heads] = KV_chunk . Q_half^T   (K = 512),
+//        logits  D[128 slots x 32 heads] = KV_chunk . Q_half^T   (K = 512,
+//                as four accumulators over the K-steps k = a mod 4, added
+//                as (D0 + D1) + (D2 + D3)),
 //      the chunk softmax (max and sum over the 128 slots, per head), and
 //        P G     D[128 features x 64] = KV_chunk^T . [P_hi; P_lo]^T  (K = 128 slots)
 //      for the four 128-feature blocks, where the same KV buffer is the
@@ -62,8 +64,12 @@ namespace {
 
 constexpr int kChunkSlots = 128;                         // slots per chunk (UMMA M of the logits)
 constexpr int kHalfHeads = kHeads / 2;                   // heads per CTA (UMMA N)
-constexpr uint32_t kTmemCols = 512;                      // logits (32) + P G (4 x 64)
-constexpr uint32_t kPvCol = 64;                          // first TMEM column of P G
+constexpr uint32_t kTmemCols = 512;                      // logits (4 x 32) + P G (4 x 64)
+constexpr uint32_t kPvCol = 128;                         // first TMEM column of P G
+// MMAs are issued by one thread in each of this many warps, into independent
+// accumulators: one thread issues a tcgen05.mma in about 80 cycles, far longer
+// than these N=32/64 MMAs take, so the issue rate sets the phase's time.
+constexpr int kIssuers = 4;
 constexpr int kGBlock = kChunkSlots * 128;               // one 64-column block of the KV rows: 16 KiB
 constexpr int kQBlock = kHalfHeads * 128;                // one 64-column block of the query half: 4 KiB
 constexpr int kPBlock = 2 * kHalfHeads * 128;            // 64 slots of [P_hi; P_lo] (64 rows): 8 KiB
@@ -134,7 +140,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     // ---- setup: counters, barrier, TMEM, and the query (an input of the call) --
     if (t == 0) {
         sm.ncand = 0;
-        mbar_init(mma_bar, 1);
+        mbar_init(mma_bar, kIssuers);
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -237,14 +243,14 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (has_chunk) {
         const uint32_t g_addr = smem_u32(g_s), q_addr = smem_u32(q_s);
-        if (t == 0) {
+        if (lane == 0 && warp < kIssuers) {
+            // Accumulator a = warp takes the K-steps kk = 4 j + a.
             constexpr uint32_t idesc = idesc_bf16_f32(128, kHalfHeads);
+            const uint32_t koff = (uint32_t)warp * 32;  // 16 bf16 = 32 B inside the 128-B row
 #pragma unroll
-            for (int kk = 0; kk < kDim / 16; ++kk) {
-                const uint32_t koff = (uint32_t)(kk & 3) * 32;  // 16 bf16 = 32 B inside the 128-B row
-                umma_bf16(tmem, smem_desc_sw128_kmajor(g_addr + (kk >> 2) * kGBlock + koff),
-                          smem_desc_sw128_kmajor(q_addr + (kk >> 2) * kQBlock + koff), idesc, kk > 0 ? 1u : 0u);
-            }
+            for (int j = 0; j < kDim / 64; ++j)
+                umma_bf16(tmem + 32 * warp, smem_desc_sw128_kmajor(g_addr + j * kGBlock + koff),
+                          smem_desc_sw128_kmajor(q_addr + j * kQBlock + koff), idesc, j > 0 ? 1u : 0u);
             umma_commit(mma_bar);
         }
         mbar_wait(mma_bar, 0, p.status);
@@ -253,14 +259,16 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         // ---- chunk softmax: warp -> (32 slots, 8 heads), lane -> one slot ----------
         const int qt = warp & 3, hg = warp >> 2;
         const int slot = 32 * qt + lane;
-        uint32_t v[8];
-        tmem_ld_x8(tmem + ((uint32_t)(32 * qt) << 16) + 8 * hg, v);
+        uint32_t v[4][8];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) tmem_ld_x8(tmem + ((uint32_t)(32 * qt) << 16) + 32 * a + 8 * hg, v[a]);
         tmem_ld_wait();
         const bool live = idx_s[slot] >= 0;
         float l[8], m[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            l[i] = __uint_as_float(v[i]) * p.scale;
+            l[i] = ((__uint_as_float(v[0][i]) + __uint_as_float(v[1][i])) +
+                    (__uint_as_float(v[2][i]) + __uint_as_float(v[3][i]))) * p.scale;
             const bool ok = live && finite_f(l[i]);
             const uint32_t bad = __ballot_sync(0xFFFFFFFFu, live && !ok);
             if (!ok) l[i] = -INFINITY;
@@ -313,18 +321,18 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
             if (red_bad[t] | red_bad[kHalfHeads + t] | red_bad[2 * kHalfHeads + t] | red_bad[3 * kHalfHeads + t])
                 atomicOr(&p.flags[e * kHeads + head0 + t], 1u);
         }
-        if (t == 0) {
+        if (lane == 0 && warp < kIssuers) {
+            // Feature block b = warp: features [128 b, 128 b + 128).
             constexpr uint32_t idesc = idesc_bf16_f32(128, 2 * kHalfHeads) | kIdescAMnMajor;
             const uint32_t p_addr = smem_u32(p_s);
+            const int b = warp;
 #pragma unroll
-            for (int b = 0; b < kDim / 128; ++b)
-#pragma unroll
-                for (int ks = 0; ks < kChunkSlots / 16; ++ks) {
-                    // A: features [128 b, 128 b + 128) x slots [16 ks, 16 ks + 16), MN-major.
-                    const uint64_t ad = smem_desc_sw128_mnmajor(g_addr + 2 * b * kGBlock + ks * 2048, kGBlock, 1024);
-                    const uint64_t bd = smem_desc_sw128_kmajor(p_addr + (ks >> 2) * kPBlock + (ks & 3) * 32);
-                    umma_bf16(tmem + kPvCol + 64 * b, ad, bd, idesc, ks != 0 ? 1u : 0u);
-                }
+            for (int ks = 0; ks < kChunkSlots / 16; ++ks) {
+                // A: features [128 b, 128 b + 128) x slots [16 ks, 16 ks + 16), MN-major.
+                const uint64_t ad = smem_desc_sw128_mnmajor(g_addr + 2 * b * kGBlock + ks * 2048, kGBlock, 1024);
+                const uint64_t bd = smem_desc_sw128_kmajor(p_addr + (ks >> 2) * kPBlock + (ks & 3) * 32);
+                umma_bf16(tmem + kPvCol + 64 * b, ad, bd, idesc, ks != 0 ? 1u : 0u);
+            }
             umma_commit(mma_bar);
         }
         mbar_wait(mma_bar, 1, p.status);
