@@ -219,6 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_score_kernel(const __grid
         // The histogram may still be being cleared by the previous kernel (PDL):
         // the producer and MMA warps start streaming, the epilogue waits here.
         pdl_wait();
+        // The scores are read back by the next kernel: keep them in L2 while the
+        // key stream (evict-first) passes through.
+        const uint64_t keep = l2_policy_evict_last();
         int cur = -1;
         uint32_t it = 0;
         for (uint32_t g = g_begin; g < g_end; ++g, ++it) {
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_score_kernel(const __grid
             const uint32_t j = tile * kTileKeys + quarter * 32 + lane;
             if (j < p.kv_len[e]) {
                 const bool fin = finite_f(s);
-                p.scores[(size_t)e * p.score_stride + j] = fin ? s : -INFINITY;
+                st_global_hint(p.scores + (size_t)e * p.score_stride + j, fin ? s : -INFINITY, keep);
                 if (want_hist && fin) atomicAdd(&hist_s[score_key(s) >> 21], 1u);
             }
         }

@@ -329,14 +329,14 @@ __device__ __forceinline__ Collected select_collect(const float* s, uint32_t L, 
             }
         }
     };
-    load_batch(begin);  // in flight while the threshold is picked
-    {
-        uint32_t hv[kHistBins / kThreads];
+    // The histogram first (the threshold pick waits for it), then the slice's
+    // scores, which stay in flight while the threshold is picked.
+    uint32_t hv[kHistBins / kThreads];
 #pragma unroll
-        for (int i = 0; i < kHistBins / kThreads; ++i) hv[i] = __ldcg(hist_row + t + i * kThreads);
+    for (int i = 0; i < kHistBins / kThreads; ++i) hv[i] = __ldcg(hist_row + t + i * kThreads);
+    load_batch(begin);
 #pragma unroll
-        for (int i = 0; i < kHistBins / kThreads; ++i) sm.h[t + i * kThreads] = hv[i];
-    }
+    for (int i = 0; i < kHistBins / kThreads; ++i) sm.h[t + i * kThreads] = hv[i];
     __syncthreads();
     Collected r;
     r.l0 = pick_bin(sm.h, width, sm.scratch);
