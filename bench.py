@@ -44,6 +44,7 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--config", type=int, default=CONFIG_INDEX)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the other workloads' step latencies")
     return ap.parse_args()
 
 
@@ -173,6 +174,46 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # native arm
 # ---------------------------------------------------------------------------
+
+def other_configs(ds, workloads, to_device, device, stream, flush_l2, skip, steps=10):
+    """Flushed single-step latency of the decode on the other benchmark workloads."""
+    import torch
+    res = {}
+    for i in range(5):
+        if i == skip:
+            continue
+        wl = workloads.config(i)
+        dev = to_device(wl, device)
+        nq = max(r.q_row for r in wl.rows) + 1
+        out = torch.empty((nq, 64, 512), dtype=torch.bfloat16, device=device)
+        idx = torch.empty((wl.index_elements,), dtype=torch.int32, device=device)
+        ws = ds.workspace(wl.rows, device)
+
+        def step():
+            ds.ds_rows_decode(dev.rows, dev.q_index, dev.w_index, dev.keys, dev.q_attn, dev.kv, dev.sinks,
+                              dev.sinks_row_stride, dev.scale, out, indices=idx, workspace_t=ws, stream=stream)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                step()
+        torch.cuda.synchronize(device)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        with torch.cuda.stream(stream):
+            for k in range(steps):
+                flush_l2(k)
+                starts[k].record(stream)
+                step()
+                ends[k].record(stream)
+        torch.cuda.synchronize(device)
+        ms = sorted(s.elapsed_time(e) for s, e in zip(starts, ends))[steps // 2]
+        res[str(i)] = {"workload": wl.name, "rows": wl.num_rows, "us_per_step_flushed_median": ms * 1e3,
+                       "rows_per_s": wl.num_rows / (ms / 1e3),
+                       "gbs": wl.algorithmic_bytes() / (ms / 1e3) / 1e9}
+        del dev, out, idx, ws
+        torch.cuda.empty_cache()
+    return res
+
 
 def main():
     args = parse()
@@ -353,6 +394,27 @@ def main():
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         e2e_ms = float(t.item())
 
+    # The positioned indexer with its causal top-512 (every key valid, offset 0)
+    # on the same caches: 20 calls back to back.
+    prow = [ds.IndexerRow(r.kv_len, 4 * r.kv_len - 1, 0, r.q_row, 512 * e) for e, r in enumerate(wl.rows)]
+    pidx = torch.empty((512 * R,), dtype=torch.int32, device=device)
+    pws = ds.indexer_topk_workspace(prow, device)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            ds.ds_rows_indexer_topk(prow, dev.q_index, dev.w_index, dev.keys, pidx, workspace_t=pws, stream=stream)
+        a_ev.record(stream)
+        for i in range(n_idx):
+            qI, wI, _ = qsets[i % 4]
+            ds.ds_rows_indexer_topk(prow, qI, wI, dev.keys, pidx, workspace_t=pws, stream=stream)
+        b_ev.record(stream)
+    torch.cuda.synchronize(device)
+    pidx_ms = a_ev.elapsed_time(b_ev) / n_idx
+    pidx_bytes = sum(256 * r.kv_len + 16384 + 256 + 4 * 512 for r in wl.rows)
+
+    per_config = None
+    if rank == 0 and world == 1 and not args.no_per_config:
+        per_config = other_configs(ds, workloads, to_device, device, stream, flush_l2, skip=args.config)
+
     if rank == 0:
         cb = None
         if world == 1 and not args.no_cpu_baseline:
@@ -376,6 +438,10 @@ def main():
             "e2e": {"value": world * R / (e2e_ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": 3 * args.steps,
+            "indexer_topk": {"entry": "ds_rows_indexer_topk", "workload": "same caches, every key valid, offset 0",
+                             "ms_per_call": pidx_ms, "gbs": pidx_bytes / (pidx_ms / 1e3) / 1e9,
+                             "frac": pidx_bytes / (pidx_ms / 1e3) / 1e9 / peak},
+            "per_config": per_config,
             "clocks": clocks.summary(),
             "cpu_baseline": cb,
         }
