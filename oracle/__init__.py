@@ -206,6 +206,93 @@ def round_bf16(x: np.ndarray) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# (5) Learned KV compressor, one decode token per row
+# deepseek_rows.metal, kernel deepseek_compressor_rows_bf16 (the append
+# branch of deepseek_compressor_bf16 at one token, no cache write), dispatched
+# by dispatch_deepseek_compressor_rows.
+# ---------------------------------------------------------------------------
+
+COMPRESSOR_SHAPES = ((4, 128), (4, 512), (128, 512))  # supported (ratio, head_dim)
+
+
+def compress_kv(kv, score, ape, norm, kv_state, score_state, start_pos: int, ratio: int, head_dim: int,
+                eps: float):
+    """One token of the learned KV compressor for one row.
+
+    With coff = 2 when ratio == 4 (overlapping windows) and 1 otherwise, and
+    P = coff * head_dim features per token:
+      kv, score  fp32 [P]           the token's projected values and scores
+      ape        fp32 [ratio, P]    position bias added to the score
+      norm       fp32 [head_dim]    RMSNorm weight
+      kv_state, score_state  fp32 [coff * ratio, P]  the row's window (not modified)
+    Returns (out [head_dim] float64 holding bf16 values, new kv_state, new score_state).
+
+    The state is kept in fp32 as the pages keep it (the score + ape sum is an
+    fp32 add); the pooling and the norm run in float64, with the pages' bf16
+    rounding of the pooled value and of the output.
+    1. The token (position start_pos, token = start_pos mod ratio) is written
+       to state row (ratio if overlapping else 0) + token: its kv (0 where not
+       finite) and score + ape (NaN where either is not finite).
+    2. When start_pos + 1 is a multiple of ratio the block is complete: each
+       feature f softmax-pools the window's values with its scores over the
+       window's rows (2 ratio rows when overlapping: the first ratio rows read
+       feature f, the last ratio rows feature head_dim + f), the pooled value
+       is rounded to bf16, and the row is RMS-normalised and scaled by norm:
+         out = bf16(c * norm / sqrt(mean(c^2) + eps)).
+       A NaN or +inf score, a non-finite value, pooled value or norm, or a
+       non-finite sum or result zeroes the whole row ("fail closed").
+       Overlapping windows then move the current block into the previous rows
+       (whether or not the row was zeroed).
+    3. Otherwise the output is zero.
+    """
+    ratio, head_dim = int(ratio), int(head_dim)
+    overlap = ratio == 4
+    coff = 2 if overlap else 1
+    proj = coff * head_dim
+    kv32 = np.asarray(kv, np.float32).reshape(proj)
+    with np.errstate(invalid="ignore", over="ignore"):
+        s32 = np.asarray(score, np.float32).reshape(proj) + np.asarray(ape, np.float32).reshape(ratio, proj)[
+            int(start_pos) % ratio]
+    kv_new = np.array(kv_state, np.float32).reshape(coff * ratio, proj)
+    sc_new = np.array(score_state, np.float32).reshape(coff * ratio, proj)
+    slot = (ratio if overlap else 0) + int(start_pos) % ratio
+    v_ok = np.isfinite(kv32)
+    kv_new[slot] = np.where(v_ok, kv32, np.float32(0.0))
+    sc_new[slot] = np.where(v_ok & np.isfinite(s32), s32, np.float32(np.nan))
+
+    out = np.zeros(head_dim)
+    if (int(start_pos) + 1) % ratio != 0:
+        return out, kv_new, sc_new
+
+    items = coff * ratio
+    feat = np.arange(head_dim)
+    # Row i of the window reads feature f, or head_dim + f for the current block
+    # of an overlapping window.
+    src = np.where((np.arange(items)[:, None] >= ratio) & overlap, head_dim + feat[None, :], feat[None, :])
+    S = sc_new.astype(np.float64)[np.arange(items)[:, None], src]   # [items, head_dim]
+    V = kv_new.astype(np.float64)[np.arange(items)[:, None], src]
+    nrm = np.asarray(norm, np.float64).reshape(head_dim)
+    bad = np.isnan(S).any(0) | (S == np.inf).any(0) | ~np.isfinite(V).all(0)
+    with np.errstate(invalid="ignore", over="ignore", divide="ignore"):
+        m = np.max(np.where(np.isnan(S), -np.inf, S), axis=0)
+        w = np.exp(S - m[None, :])
+        pooled = (w * V).sum(0) / w.sum(0)
+    bad |= ~_fp32_finite(pooled) | ~np.isfinite(nrm)
+    c = round_bf16(np.where(_fp32_finite(pooled), pooled, 0.0))
+    ss = float(np.sum(c * c))
+    if not bad.any() and _fp32_finite(ss):
+        scale = 1.0 / math.sqrt(ss / head_dim + float(eps))
+        with np.errstate(invalid="ignore", over="ignore"):
+            y = c * scale * nrm
+        if math.isfinite(scale) and _fp32_finite(y).all():
+            out = round_bf16(y)
+    if overlap:
+        kv_new[:ratio] = kv_new[ratio:].copy()
+        sc_new[:ratio] = sc_new[ratio:].copy()
+    return out, kv_new, sc_new
+
+
+# ---------------------------------------------------------------------------
 # The whole decode step over a row table
 # ---------------------------------------------------------------------------
 

@@ -281,6 +281,155 @@ def test_bf16_decode_exact():
 
 
 # ---------------------------------------------------------------------------
+# Learned KV compressor (one token per row)
+# ---------------------------------------------------------------------------
+
+def _comp_inputs(seed, ratio, head_dim, pos):
+    rng = np.random.default_rng(seed)
+    coff = 2 if ratio == 4 else 1
+    P = coff * head_dim
+    f32 = lambda *sh: rng.standard_normal(sh).astype(np.float32)
+    return dict(kv=f32(P), score=f32(P), ape=f32(ratio, P), norm=(1.0 + 0.1 * f32(head_dim)).astype(np.float32),
+                kv_state=f32(coff * ratio, P), score_state=f32(coff * ratio, P), start_pos=pos, ratio=ratio,
+                head_dim=head_dim, eps=1e-6)
+
+
+def _bf16_ulp(x):
+    x = np.abs(np.asarray(x, np.float64))
+    return np.exp2(np.floor(np.log2(np.maximum(x, 1e-30))) - 7.0)
+
+
+@pytest.mark.parametrize("ratio,head_dim", [(4, 128), (4, 512), (128, 512)])
+def test_compressor_uniform_scores_give_the_window_mean(ratio, head_dim):
+    a = _comp_inputs(1, ratio, head_dim, pos=ratio * 3 - 1)  # completes a block
+    coff = 2 if ratio == 4 else 1
+    a["score_state"][:] = 0.5
+    a["score"][:] = 0.25
+    a["ape"][:] = 0.25  # the token's score + ape is 0.5 too: all equal
+    out, kv_new, _ = oracle.compress_kv(**a)
+    # The softmax of equal scores is uniform: the pooled value is the mean of
+    # the window's values (feature f, and head_dim + f for the current block).
+    # The window before the shift: the previous block (untouched by the token's
+    # write) and the current block (after it; the shift leaves those rows).
+    V = kv_new.astype(np.float64)
+    if coff == 2:
+        prev = np.asarray(a["kv_state"], np.float64)[:ratio, :head_dim]
+        win = np.concatenate([prev, V[ratio:, head_dim:]], 0)
+    else:
+        win = V[:, :head_dim]
+    c = oracle.round_bf16(win.mean(0))
+    y = c * np.asarray(a["norm"], np.float64) / np.sqrt(np.mean(c * c) + a["eps"])
+    np.testing.assert_allclose(out, oracle.round_bf16(y), rtol=0, atol=0)
+
+
+def test_compressor_dominant_score_selects_its_value():
+    a = _comp_inputs(2, 128, 512, pos=127)
+    a["score_state"][:] = 0.0
+    a["score_state"][37] = 80.0       # row 37 outweighs the others by e^80
+    out, kv_new, _ = oracle.compress_kv(**a)
+    c = oracle.round_bf16(kv_new[37].astype(np.float64))
+    y = c * np.asarray(a["norm"], np.float64) / np.sqrt(np.mean(c * c) + 1e-6)
+    np.testing.assert_allclose(out, oracle.round_bf16(y), rtol=0, atol=0)
+
+
+@pytest.mark.parametrize("ratio,head_dim", [(4, 128), (128, 512)])
+def test_compressor_token_write_and_no_output_mid_block(ratio, head_dim):
+    pos = ratio * 5 + 1                    # mid block: (pos + 1) % ratio != 0
+    a = _comp_inputs(3, ratio, head_dim, pos)
+    out, kv_new, sc_new = oracle.compress_kv(**a)
+    assert not out.any()
+    slot = (ratio if ratio == 4 else 0) + pos % ratio
+    changed = np.nonzero((kv_new != a["kv_state"]).any(1) | (sc_new != a["score_state"]).any(1))[0]
+    assert list(changed) == [slot]
+    np.testing.assert_array_equal(kv_new[slot], a["kv"])
+    # score + ape is an fp32 add (the state is fp32), of the token's ape row.
+    np.testing.assert_array_equal(sc_new[slot], np.float32(a["score"]) + np.float32(a["ape"][pos % ratio]))
+
+
+def test_compressor_first_half_of_the_token_waits_for_the_next_block():
+    # A NaN in the first half of the completing token is not read by this block.
+    a = _comp_inputs(10, 4, 128, pos=7)
+    a["kv"][5] = np.nan
+    out, kv_new, sc_new = oracle.compress_kv(**a)
+    assert out.any()
+    assert kv_new[0 + 3, 5] == 0.0 and np.isnan(sc_new[0 + 3, 5])  # shifted into the previous block
+
+
+def test_compressor_overlap_reads_each_half_from_its_block():
+    # ratio 4: window rows 0..3 (previous block) read features [0, D), rows 4..7
+    # (current block) read [D, 2D). Garbage in the other halves changes nothing.
+    a = _comp_inputs(4, 4, 128, pos=11)
+    out, _, _ = oracle.compress_kv(**a)
+    b = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in a.items()}
+    b["kv_state"][:4, 128:] = 1e6
+    b["score_state"][:4, 128:] = 50.0
+    b["kv_state"][4:, :128] = -1e6
+    b["score_state"][4:, :128] = 50.0
+    b["kv"][:128] = 7e5                     # the token's first half lands in row 4+3, unread
+    out2, _, _ = oracle.compress_kv(**b)
+    np.testing.assert_array_equal(out, out2)
+
+
+def test_compressor_overlap_shift_after_a_block():
+    a = _comp_inputs(5, 4, 512, pos=3)
+    out, kv_new, sc_new = oracle.compress_kv(**a)
+    assert out.any()
+    np.testing.assert_array_equal(kv_new[:4], kv_new[4:])
+    np.testing.assert_array_equal(sc_new[:4], sc_new[4:])
+    b = _comp_inputs(5, 4, 512, pos=2)      # mid block: no shift
+    _, kv2, _ = oracle.compress_kv(**b)
+    np.testing.assert_array_equal(kv2[:4], b["kv_state"][:4])
+
+
+def test_compressor_unit_norm_gives_unit_rms():
+    a = _comp_inputs(6, 4, 512, pos=7)
+    a["norm"][:] = 1.0
+    out, _, _ = oracle.compress_kv(**a)
+    rms = np.sqrt(np.mean(out ** 2))
+    assert abs(rms - 1.0) < 4e-3  # bf16 rounding of c and of the output; eps 1e-6
+
+
+@pytest.mark.parametrize("what", ["kv_nan", "norm_inf", "state_score_inf", "state_kv_nan"])
+def test_compressor_fail_closed_zeroes_the_row(what):
+    a = _comp_inputs(7, 4, 128, pos=7)
+    if what == "kv_nan":
+        # The token's second half is read by this block (the first half only
+        # after the shift): its score becomes NaN and its value 0.
+        a["kv"][128 + 5] = np.nan
+    elif what == "norm_inf":
+        a["norm"][9] = np.inf
+    elif what == "state_score_inf":
+        a["score_state"][1, 3] = np.inf
+    else:
+        a["kv_state"][2, 4] = np.nan
+    out, kv_new, _ = oracle.compress_kv(**a)
+    assert not out.any()
+    np.testing.assert_array_equal(kv_new[:4], kv_new[4:])  # the window still shifts
+    if what == "kv_nan":
+        assert kv_new[4 + 3, 128 + 5] == 0.0
+
+
+def test_compressor_window_order_does_not_matter():
+    a = _comp_inputs(8, 128, 512, pos=127)
+    out, kv_new, sc_new = oracle.compress_kv(**a)
+    perm = np.random.default_rng(9).permutation(128)
+    b = dict(a)
+    b["kv_state"] = kv_new[perm]
+    b["score_state"] = sc_new[perm]
+    slot = int(np.nonzero(perm == 127)[0][0])   # the token's row moves to `slot`
+    b["kv"], b["score"] = kv_new[127].copy(), sc_new[127].copy()
+    b["ape"] = np.zeros_like(a["ape"])
+    b["start_pos"] = 128 * 9 + slot - 128 if slot == 127 else None
+    # Recompute with the permuted window and the token written to its new row.
+    if b["start_pos"] is None:
+        b["start_pos"] = 128 * 9 + 127
+        b["kv_state"][slot], b["kv_state"][127] = b["kv_state"][127].copy(), b["kv_state"][slot].copy()
+        b["score_state"][slot], b["score_state"][127] = b["score_state"][127].copy(), b["score_state"][slot].copy()
+    out2, _, _ = oracle.compress_kv(**b)
+    assert np.all(np.abs(out2 - out) <= _bf16_ulp(out) + 1e-12)
+
+
+# ---------------------------------------------------------------------------
 # Decode composition on a small workload
 # ---------------------------------------------------------------------------
 
@@ -320,6 +469,22 @@ def _topk_high_index_ties(scores, width):
 
 
 _REAL_ATTENTION = oracle.sparse_attention
+_REAL_COMPRESS = oracle.compress_kv
+
+
+def _compress_without_ape(**a):
+    # mistake: the position bias is not added to the token's score
+    return _REAL_COMPRESS(**{**a, "ape": np.zeros_like(np.asarray(a["ape"]))})
+
+
+def _compress_current_block_only(**a):
+    # mistake: an overlapping window pools only its current block
+    if a["ratio"] != 4:
+        return _REAL_COMPRESS(**a)
+    sc = np.array(a["score_state"], np.float32)
+    sc[:4] = -np.inf
+    out, kv, s = _REAL_COMPRESS(**{**a, "score_state": sc})
+    return out, kv, s
 
 
 def _attention_sink_with_value(q, kv, idx, sinks, scale):
@@ -332,13 +497,16 @@ def test_planted_mistakes_are_caught(monkeypatch):
     caught = []
     for name, fake in [("indexer_score", _no_relu), ("indexer_score", _transposed_weights),
                        ("topk", _topk_high_index_ties),
-                       ("sparse_attention", _attention_sink_with_value)]:
+                       ("sparse_attention", _attention_sink_with_value),
+                       ("compress_kv", _compress_without_ape), ("compress_kv", _compress_current_block_only)]:
         monkeypatch.setattr(oracle, name, fake)
         tests = {
             "indexer_score": [test_indexer_golden, test_indexer_relu_identity,
                               test_indexer_one_hot_weights_select_head],
             "topk": [test_topk_golden, test_topk_signed_zero_ties],
             "sparse_attention": [test_attention_golden, test_attention_dense_closed_form],
+            "compress_kv": [lambda: test_compressor_uniform_scores_give_the_window_mean(4, 128),
+                            lambda: test_compressor_token_write_and_no_output_mid_block(4, 128)],
         }[name]
         failed = 0
         for t in tests:
