@@ -215,6 +215,41 @@ def other_configs(ds, workloads, to_device, device, stream, flush_l2, skip, step
     return res
 
 
+def compressor_timings(ds, device, stream, calls=50):
+    """ds_rows_compress_kv per supported shape, 8 rows, every row completing a
+    block (the call that pools its window): microseconds per call and the bytes
+    it must move (token inputs, the window read, the state row written, the
+    overlap shift, ape, norm and the output)."""
+    import torch
+    res = {}
+    g = torch.Generator(device="cpu").manual_seed(5)
+    for ratio, head_dim in ((4, 128), (4, 512), (128, 512)):
+        coff = 2 if ratio == 4 else 1
+        P = coff * head_dim
+        f = lambda *sh: torch.randn(*sh, generator=g).to(device)
+        ks = [f(coff * ratio, P) for _ in range(8)]
+        ss = [f(coff * ratio, P) for _ in range(8)]
+        kv, sc, ape, norm = f(8, P), f(8, P), f(ratio, P), f(head_dim)
+        out = torch.empty((8, head_dim), dtype=torch.bfloat16, device=device)
+        pos = [ratio * (e + 1) - 1 for e in range(8)]
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                ds.ds_rows_compress_kv(ks, ss, pos, kv, sc, ape, norm, ratio, head_dim, 1e-6, out, stream=stream)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(calls):
+                ds.ds_rows_compress_kv(ks, ss, pos, kv, sc, ape, norm, ratio, head_dim, 1e-6, out, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize(device)
+        us = a.elapsed_time(b) / calls * 1e3
+        shift = 2 * 2 * ratio * P * 4 if ratio == 4 else 0
+        per_row = 3 * P * 4 + 2 * coff * ratio * head_dim * 4 + 2 * P * 4 + shift + head_dim * 2
+        nbytes = 8 * per_row + ratio * P * 4 + head_dim * 4
+        res[f"{ratio}x{head_dim}"] = {"us_per_call": us, "bytes_per_call": nbytes, "gbs": nbytes / (us / 1e6) / 1e9}
+    return res
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -412,8 +447,10 @@ def main():
     pidx_bytes = sum(256 * r.kv_len + 16384 + 256 + 4 * 512 for r in wl.rows)
 
     per_config = None
+    compressor = None
     if rank == 0 and world == 1 and not args.no_per_config:
         per_config = other_configs(ds, workloads, to_device, device, stream, flush_l2, skip=args.config)
+        compressor = compressor_timings(ds, device, stream)
 
     if rank == 0:
         cb = None
@@ -442,6 +479,7 @@ def main():
                              "ms_per_call": pidx_ms, "gbs": pidx_bytes / (pidx_ms / 1e3) / 1e9,
                              "frac": pidx_bytes / (pidx_ms / 1e3) / 1e9 / peak},
             "per_config": per_config,
+            "compressor": compressor,
             "clocks": clocks.summary(),
             "cpu_baseline": cb,
         }

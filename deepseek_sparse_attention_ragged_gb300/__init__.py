@@ -25,6 +25,7 @@ __all__ = [
     "ds_rows_workspace_bytes", "workspace", "ds_rows_indexer_score", "ds_rows_topk", "ds_rows_topk_static",
     "ds_rows_sparse_attn", "ds_rows_decode", "ds_rows_version",
     "IndexerRow", "ds_rows_indexer_topk_workspace_bytes", "indexer_topk_workspace", "ds_rows_indexer_topk",
+    "CompressorRow", "ds_rows_compress_kv",
     "ROWS_MAX", "INDEX_HEADS", "INDEX_DIM", "TOP_K", "HEADS", "DIM",
 ]
 
@@ -58,6 +59,12 @@ class IndexerRow(ctypes.Structure):
 
     _fields_ = [("kv_len", ctypes.c_uint32), ("start_pos", ctypes.c_uint32), ("offset", ctypes.c_int32),
                 ("q_row", ctypes.c_uint32), ("output_offset", ctypes.c_uint32)]
+
+
+class CompressorRow(ctypes.Structure):
+    """One compressor row: ds_compressor_row_t {kv_state, score_state, start_pos} (device pointers)."""
+
+    _fields_ = [("kv_state", ctypes.c_void_p), ("score_state", ctypes.c_void_p), ("start_pos", ctypes.c_uint32)]
 
 
 class _RowSet(ctypes.Structure):
@@ -105,6 +112,9 @@ def load():
     lib.ds_rows_indexer_topk_workspace_bytes.restype = sz
     lib.ds_rows_indexer_topk.argtypes = [i32, ctypes.POINTER(IndexerRow), ctypes.POINTER(vp), vp, vp, vp, vp, sz, vp]
     lib.ds_rows_indexer_topk.restype = i32
+    lib.ds_rows_compress_kv.argtypes = [i32, ctypes.POINTER(CompressorRow), vp, vp, vp, vp, ctypes.c_uint32,
+                                         ctypes.c_uint32, ctypes.c_float, vp, vp]
+    lib.ds_rows_compress_kv.restype = i32
     lib.ds_rows_last_error.argtypes = []
     lib.ds_rows_last_error.restype = ctypes.c_char_p
     lib.ds_rows_version.argtypes = []
@@ -356,3 +366,34 @@ def ds_rows_indexer_topk(rows, q_index, w_index, index_keys, indices, workspace_
     ks = (ctypes.c_void_p * n)(*[k.data_ptr() for k in index_keys])
     _check(lib, lib.ds_rows_indexer_topk(n, tab, ks, _ptr(q_index), _ptr(w_index), _ptr(indices),
                                          _ptr(workspace_t), workspace_t.numel(), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# learned KV compressor, one decode token per row
+# ---------------------------------------------------------------------------
+
+def ds_rows_compress_kv(kv_states, score_states, start_pos, kv, score, ape, norm, ratio, head_dim, epsilon, out,
+                        stream=None):
+    """One token of the learned KV compressor per row. kv_states / score_states:
+    per-row fp32 [coff*ratio, coff*head_dim] CUDA tensors, updated in place;
+    start_pos: per-row positions; kv, score fp32 [rows, coff*head_dim]; ape
+    fp32 [ratio, coff*head_dim]; norm fp32 [head_dim]; out bf16 [rows, head_dim]."""
+    lib = load()
+    n = len(start_pos)
+    if len(kv_states) != n or len(score_states) != n:
+        raise ValueError("one kv_state, score_state and start_pos per row")
+    coff = 2 if ratio == 4 else 1
+    proj = coff * head_dim
+    for e in range(n):
+        _require(kv_states[e], f"kv_states[{e}]", torch.float32, coff * ratio * proj)
+        _require(score_states[e], f"score_states[{e}]", torch.float32, coff * ratio * proj)
+    _require(kv, "kv", torch.float32, n * proj)
+    _require(score, "score", torch.float32, n * proj)
+    _require(ape, "ape", torch.float32, ratio * proj)
+    _require(norm, "norm", torch.float32, head_dim)
+    _require(out, "out", torch.bfloat16, n * head_dim)
+    tab = (CompressorRow * max(1, n))()
+    for e in range(n):
+        tab[e] = CompressorRow(kv_states[e].data_ptr(), score_states[e].data_ptr(), int(start_pos[e]))
+    _check(lib, lib.ds_rows_compress_kv(n, tab, _ptr(kv), _ptr(score), _ptr(ape), _ptr(norm), int(ratio),
+                                        int(head_dim), float(epsilon), _ptr(out), _stream(stream)))

@@ -542,6 +542,59 @@ int ds_rows_indexer_topk(int rows, const ds_indexer_row_t* table, const ds_bf16*
     return run_topk(&sset, scores, L.score_stride, indices, out_off, ws, L, false, false, s, offsets);
 }
 
+int ds_rows_compress_kv(int rows, const ds_compressor_row_t* table, const float* kv, const float* score,
+                        const float* ape, const float* norm, uint32_t ratio, uint32_t head_dim, float epsilon,
+                        ds_bf16* out, void* stream) {
+    if (rows < 1 || rows > DS_ROWS_MAX) return fail(DS_EINVAL, "rows must be 1..=%d, got %d", DS_ROWS_MAX, rows);
+    if (!table) return fail(DS_EINVAL, "compressor row table is NULL");
+    const bool supported = (ratio == 4 && (head_dim == 128 || head_dim == 512)) || (ratio == 128 && head_dim == 512);
+    if (!supported)
+        return fail(DS_EINVAL, "compressor (ratio, head_dim) must be (4,128), (4,512) or (128,512), got (%u,%u)",
+                    ratio, head_dim);
+    if (!(epsilon > 0.0f) || !(epsilon < __builtin_huge_valf()))
+        return fail(DS_EINVAL, "compressor epsilon must be finite and positive");
+    if (!kv || !score || !ape || !norm || !out) return fail(DS_EINVAL, "kv, score, ape, norm and out must be non-NULL");
+    if (!aligned16(kv) || !aligned16(score) || !aligned16(ape) || !aligned16(norm) || !aligned16(out))
+        return fail(DS_EALIGN, "kv, score, ape, norm and out must be 16-B aligned");
+    const uint32_t coff = ratio == 4 ? 2 : 1;
+    const size_t state_bytes = (size_t)coff * ratio * coff * head_dim * sizeof(float);
+    CompressorParams p;
+    std::memset(&p, 0, sizeof(p));
+    for (int e = 0; e < rows; ++e) {
+        const ds_compressor_row_t& r = table[e];
+        if (r.start_pos == 0 || r.start_pos == 0xFFFFFFFFu)
+            return fail(DS_EINVAL, "compressor row %d: position must be in 1..u32::MAX, got %u", e, r.start_pos);
+        if (!r.kv_state || !r.score_state) return fail(DS_EINVAL, "compressor row %d: state is NULL", e);
+        if (!aligned16(r.kv_state) || !aligned16(r.score_state))
+            return fail(DS_EALIGN, "compressor row %d: state not 16-B aligned", e);
+        const uintptr_t mine[2] = {reinterpret_cast<uintptr_t>(r.kv_state), reinterpret_cast<uintptr_t>(r.score_state)};
+        if (mine[0] < mine[1] + state_bytes && mine[1] < mine[0] + state_bytes)
+            return fail(DS_EINVAL, "compressor row %d: kv_state and score_state overlap", e);
+        for (int o = 0; o < e; ++o) {
+            const uintptr_t other[2] = {reinterpret_cast<uintptr_t>(table[o].kv_state),
+                                        reinterpret_cast<uintptr_t>(table[o].score_state)};
+            for (uintptr_t a : mine)
+                for (uintptr_t b : other)
+                    if (a < b + state_bytes && b < a + state_bytes)
+                        return fail(DS_EINVAL, "compressor states of rows %d and %d overlap", o, e);
+        }
+        p.kv_state[e] = r.kv_state;
+        p.score_state[e] = r.score_state;
+        p.start_pos[e] = r.start_pos;
+    }
+    p.kv = kv;
+    p.score = score;
+    p.ape = ape;
+    p.norm = norm;
+    p.out = reinterpret_cast<__nv_bfloat16*>(out);
+    p.rows = (uint32_t)rows;
+    p.ratio = ratio;
+    p.head_dim = head_dim;
+    p.eps = epsilon;
+    cudaError_t err = launch_compressor(p, (cudaStream_t)stream, true);
+    return err == cudaSuccess ? DS_OK : cuda_fail(err, "compressor launch");
+}
+
 const char* ds_rows_last_error(void) { return g_error.c_str(); }
 
 const char* ds_rows_version(void) { return "dsrows 0.1.0 (sm_103a)"; }

@@ -1,0 +1,228 @@
+// Learned KV compressor, one decode token per row (mlx-native deepseek_rows.metal,
+// kernel deepseek_compressor_rows_bf16; dispatch_deepseek_compressor_rows).
+//
+// With coff = 2 for ratio 4 (overlapping windows) and 1 for ratio 128, and
+// P = coff * head_dim features per token, per row:
+//   1. the token (token = start_pos mod ratio) is written to state row
+//      (ratio if overlapping else 0) + token: its kv (0 where not finite) and
+//      score + ape[token] (NaN where either is not finite);
+//   2. when start_pos + 1 is a multiple of ratio, each feature f softmax-pools
+//      the window's values with its scores (2 ratio rows when overlapping: the
+//      first ratio rows read feature f, the rest feature head_dim + f), the
+//      pooled value is rounded to bf16, and the row is RMS-normalised:
+//        out = bf16(c * norm / sqrt(mean(c^2) + eps)),
+//      all zero when any score is NaN or +inf, any value, pooled value, norm,
+//      sum or result is not finite; overlapping windows then shift the current
+//      block into the previous rows. Otherwise the output row is zero.
+//
+// GB300 design: one 8-CTA cluster per row; CTA r owns output features
+// [r D/8, (r+1) D/8) in float4 columns, 16 threads per column splitting the
+// window's rows (a fixed-order shuffle tree combines them), so a CTA keeps
+// its whole share of the window in flight. Each thread owns its features in
+// every state row, so the token write, the pooling and the shift need no
+// barrier beyond the block's; the RMS sum and the fail-closed flags cross the
+// cluster through distributed shared memory in rank order.
+
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dsrows {
+
+namespace cg = cooperative_groups;
+
+namespace {
+
+constexpr int kCompCluster = 8;
+constexpr int kCompThreads = 256;
+constexpr int kSplit = 16;  // threads per float4 column
+
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ float comp(const float4& v, int k) {
+    return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
+}
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+struct CompSmem {
+    float col_sq[kSplit];      // per float4 column: sum of c^2
+    uint32_t col_bad[kSplit];
+    float cta_sq;              // this CTA's share, read by the cluster
+    uint32_t cta_bad;
+    uint32_t cta_ybad;
+};
+
+}  // namespace
+
+__global__ void __cluster_dims__(kCompCluster, 1, 1) __launch_bounds__(kCompThreads)
+    compressor_kernel(const CompressorParams p) {
+    __shared__ CompSmem sm;
+    cg::cluster_group cluster = cg::this_cluster();
+    const uint32_t rank = cluster.block_rank();
+    const int row = blockIdx.x / kCompCluster;
+    const int t = threadIdx.x;
+    const int D = (int)p.head_dim, R = (int)p.ratio;
+    const bool overlap = R == 4;
+    const int coff = overlap ? 2 : 1;
+    const int P = coff * D;
+    const uint32_t pos = p.start_pos[row];
+    const int token = (int)(pos % (uint32_t)R);
+    const int slot = (overlap ? R : 0) + token;
+    const int FB = D / kCompCluster;          // features of this CTA: 16 or 64
+    const int ncol = FB / 4;
+    const int col = t / kSplit, sub = t % kSplit;
+    const bool active = col < ncol;
+    const int f0 = FB * (int)rank + 4 * col;  // first of this column's four features
+    float* kvs = p.kv_state[row];
+    float* scs = p.score_state[row];
+
+    pdl_wait();  // inputs and states may come from the previous kernel
+
+    // ---- 1. the token's state row, for this column's features ----------------
+    if (active && sub < coff) {
+        const int sf = sub * D + f0;
+        const float4 v = ld4(p.kv + (size_t)row * P + sf);
+        const float4 s0 = ld4(p.score + (size_t)row * P + sf);
+        const float4 a = ld4(p.ape + (size_t)token * P + sf);
+        float4 vk, sk;
+        float* vo = &vk.x;
+        float* so = &sk.x;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float vv = comp(v, k);
+            const float ss = comp(s0, k) + comp(a, k);
+            const bool ok = finite_f(vv);
+            vo[k] = ok ? vv : 0.0f;
+            so[k] = ok && finite_f(ss) ? ss : __int_as_float(0x7FC00000);
+        }
+        st4(kvs + (size_t)slot * P + sf, vk);
+        st4(scs + (size_t)slot * P + sf, sk);
+    }
+    __syncthreads();  // the row is visible to the column's other threads
+
+    const bool complete = (pos + 1) % (uint32_t)R == 0;  // the same for the whole cluster
+    if (!complete) {
+        if (active && sub == 0)
+            *reinterpret_cast<uint2*>(p.out + (size_t)row * D + f0) = make_uint2(0u, 0u);
+        return;
+    }
+
+    // ---- 2. pooling: this thread takes window rows sub, sub + 16, ... ---------
+    const int items = coff * R;
+    float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    uint32_t bad = 0;
+    if (active) {
+        for (int i = sub; i < items; i += kSplit) {
+            const int sf = (overlap && i >= R) ? D + f0 : f0;
+            const float4 s4 = ld4(scs + (size_t)i * P + sf);
+            const float4 v4 = ld4(kvs + (size_t)i * P + sf);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float s = comp(s4, k);
+                bad |= (s != s || s == INFINITY || !finite_f(comp(v4, k))) ? 1u : 0u;
+                m[k] = fmaxf(m[k], s);
+            }
+        }
+    }
+#pragma unroll
+    for (int o = kSplit / 2; o > 0; o >>= 1) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m[k] = fmaxf(m[k], __shfl_xor_sync(0xFFFFFFFFu, m[k], o));
+        bad |= __shfl_xor_sync(0xFFFFFFFFu, bad, o);
+    }
+    float den[4] = {0, 0, 0, 0}, num[4] = {0, 0, 0, 0};
+    if (active) {
+        for (int i = sub; i < items; i += kSplit) {
+            const int sf = (overlap && i >= R) ? D + f0 : f0;
+            const float4 s4 = ld4(scs + (size_t)i * P + sf);
+            const float4 v4 = ld4(kvs + (size_t)i * P + sf);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float w = expf(comp(s4, k) - m[k]);
+                den[k] += w;
+                num[k] = fmaf(w, comp(v4, k), num[k]);
+            }
+        }
+    }
+#pragma unroll
+    for (int o = kSplit / 2; o > 0; o >>= 1)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            den[k] += __shfl_xor_sync(0xFFFFFFFFu, den[k], o);
+            num[k] += __shfl_xor_sync(0xFFFFFFFFu, num[k], o);
+        }
+    float c[4];
+    float sq = 0.0f;
+    const float4 nrm = active ? ld4(p.norm + f0) : make_float4(0, 0, 0, 0);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float pooled = num[k] / den[k];
+        const bool ok = finite_f(pooled);
+        c[k] = bf16_round(ok ? pooled : 0.0f);
+        bad |= (!ok || !finite_f(comp(nrm, k))) ? 1u : 0u;
+        sq = fmaf(c[k], c[k], sq);
+    }
+
+    // ---- 3. RMS over the row: column -> CTA -> cluster, in fixed order ----------
+    if (active && sub == 0) {
+        sm.col_sq[col] = sq;
+        sm.col_bad[col] = bad;
+    }
+    __syncthreads();
+    if (t == 0) {
+        float s = 0.0f;
+        uint32_t b = 0;
+        for (int j = 0; j < ncol; ++j) {
+            s += sm.col_sq[j];
+            b |= sm.col_bad[j];
+        }
+        sm.cta_sq = s;
+        sm.cta_bad = b;
+    }
+    cluster.sync();
+    float total = 0.0f;
+    uint32_t any_bad = 0;
+    for (int r = 0; r < kCompCluster; ++r) {
+        total += cluster.map_shared_rank(&sm, (unsigned)r)->cta_sq;
+        any_bad |= cluster.map_shared_rank(&sm, (unsigned)r)->cta_bad;
+    }
+    bool invalid = any_bad != 0 || !finite_f(total);
+    const float scale = invalid ? 0.0f : 1.0f / sqrtf(total / (float)D + p.eps);
+    if (!finite_f(scale)) invalid = true;
+    float y[4];
+    uint32_t ybad = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        y[k] = c[k] * scale * comp(nrm, k);
+        ybad |= finite_f(y[k]) ? 0u : 1u;
+    }
+    if (t == 0) sm.cta_ybad = 0;
+    __syncthreads();
+    if (active && sub == 0 && ybad) atomicOr(&sm.cta_ybad, 1u);
+    cluster.sync();
+    for (int r = 0; r < kCompCluster; ++r) invalid = invalid || cluster.map_shared_rank(&sm, (unsigned)r)->cta_ybad;
+
+    if (active && sub == 0) {
+        __align__(8) __nv_bfloat16 o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[k] = __float2bfloat16_rn(invalid ? 0.0f : y[k]);
+        *reinterpret_cast<uint2*>(p.out + (size_t)row * D + f0) = *reinterpret_cast<const uint2*>(o);
+    }
+
+    // ---- 4. overlapping windows: the current block becomes the previous one ---
+    if (overlap && active && sub < 2 * R) {
+        const int i = sub >> 1, h = sub & 1;  // previous row i, feature half h
+        const size_t dst = (size_t)i * P + h * D + f0, src = (size_t)(R + i) * P + h * D + f0;
+        st4(kvs + dst, ld4(kvs + src));
+        st4(scs + dst, ld4(scs + src));
+    }
+    cluster.sync();  // no CTA leaves while the others may still read its shared memory
+}
+
+cudaError_t launch_compressor(const CompressorParams& p, cudaStream_t stream, bool pdl) {
+    if (p.rows == 0) return cudaSuccess;
+    return launch_kernel(compressor_kernel, dim3(p.rows * kCompCluster), dim3(kCompThreads), 0, stream, pdl, p);
+}
+
+}  // namespace dsrows

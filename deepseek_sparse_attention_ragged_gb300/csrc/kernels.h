@@ -71,6 +71,24 @@ struct TailParams {
     uint32_t chunk_begin[DS_ROWS_MAX];  // first 128-slot chunk of each row
 };
 
+// Learned KV compressor, one decode token per row: one 8-CTA cluster per row.
+struct CompressorParams {
+    float* kv_state[DS_ROWS_MAX];     // fp32 [coff * ratio, coff * head_dim], updated in place
+    float* score_state[DS_ROWS_MAX];
+    const float* kv;                  // fp32 [rows, coff * head_dim]
+    const float* score;               // fp32 [rows, coff * head_dim]
+    const float* ape;                 // fp32 [ratio, coff * head_dim]
+    const float* norm;                // fp32 [head_dim]
+    __nv_bfloat16* out;               // bf16 [rows, head_dim]
+    uint32_t start_pos[DS_ROWS_MAX];
+    uint32_t rows;
+    uint32_t ratio;
+    uint32_t head_dim;
+    float eps;
+};
+
+cudaError_t launch_compressor(const CompressorParams& p, cudaStream_t stream, bool pdl);
+
 size_t indexer_smem_bytes();
 uint32_t indexer_tile_keys();
 cudaError_t launch_indexer(const IndexerParams& p, int num_sms, cudaStream_t stream, bool pdl);

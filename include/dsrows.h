@@ -231,6 +231,43 @@ int ds_rows_indexer_topk(int rows, const ds_indexer_row_t* table, const ds_bf16*
                          const ds_bf16* q_index, const float* w_index, int32_t* indices,
                          void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * One row of a KV compressor call (`DeepSeekCompressorRow`): the row's
+ * recurrent window (device fp32, updated in place) and its token's position.
+ *   kv_state     fp32 [coff * ratio, coff * head_dim]     (16-B aligned)
+ *   score_state  fp32, same shape                          (16-B aligned)
+ *   start_pos    the decode token's absolute position, 1 .. 2^32 - 2.
+ * coff is 2 for ratio 4 (overlapping windows) and 1 for ratio 128. The state
+ * buffers of a call must not overlap.
+ */
+typedef struct {
+    float* kv_state;
+    float* score_state;
+    uint32_t start_pos;
+} ds_compressor_row_t;
+
+/*
+ * (5) Learned KV compressor, one decode token per row
+ * (`deepseek_compressor_rows_bf16`, `dispatch_deepseek_compressor_rows`), for
+ * (ratio, head_dim) in {(4, 128), (4, 512), (128, 512)}. With P = coff * head_dim:
+ *   1. the token (t = start_pos mod ratio) is written to state row
+ *      (ratio if coff == 2 else 0) + t: kv (0 where not finite) and
+ *      score + ape[t] (NaN where either is not finite);
+ *   2. when start_pos + 1 is a multiple of ratio, each feature f softmax-pools
+ *      the window's values with its scores (coff * ratio rows; with coff == 2
+ *      the first ratio rows read feature f, the others head_dim + f), rounds
+ *      to bf16 (c) and writes out = bf16(c * norm / sqrt(mean(c^2) + epsilon)),
+ *      or zeros when a score is NaN or +inf, or a value, pooled value, norm,
+ *      sum or result is not finite; with coff == 2 the window then shifts the
+ *      current block into the previous rows. Otherwise out is zero.
+ *   kv, score  fp32 [rows, P]; ape fp32 [ratio, P]; norm fp32 [head_dim]
+ *              (all 16-B aligned); epsilon finite and > 0.
+ *   out        bf16 [rows, head_dim]                       (16-B aligned)
+ */
+int ds_rows_compress_kv(int rows, const ds_compressor_row_t* table, const float* kv, const float* score,
+                        const float* ape, const float* norm, uint32_t ratio, uint32_t head_dim,
+                        float epsilon, ds_bf16* out, void* stream);
+
 /* Message of the last failed call on this host thread ("" if none). */
 const char* ds_rows_last_error(void);
 

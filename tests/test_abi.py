@@ -214,3 +214,35 @@ def test_indexer_rows_pointers_and_workspace(lib):
     need = ds.ds_rows_indexer_topk_workspace_bytes(rows)
     assert _indexer_topk(lib, rows, ws_bytes=need - 1) == -2 and "workspace holds" in _err(lib)
     assert _indexer_topk(lib, rows, ws=FAKE + 16) == -3
+
+
+# ---------------------------------------------------------------------------
+# KV compressor rows (dispatch_deepseek_compressor_rows checks)
+# ---------------------------------------------------------------------------
+
+def _compress(lib, rows, ratio=4, head_dim=128, eps=1e-6, ptr=FAKE):
+    tab = (ds.CompressorRow * max(1, len(rows)))(*[ds.CompressorRow(*r) for r in rows])
+    return lib.ds_rows_compress_kv(len(rows), tab, ptr, ptr, ptr, ptr, ratio, head_dim, ctypes.c_float(eps), ptr,
+                                   None)
+
+
+STATE = 2 * 4 * 2 * 128 * 4  # bytes of one (4, 128) state
+
+
+@pytest.mark.parametrize("ratio,head_dim", [(4, 256), (128, 128), (8, 512), (0, 512)])
+def test_compressor_shape_checks(lib, ratio, head_dim):
+    assert _compress(lib, [(FAKE, FAKE + STATE, 3)], ratio, head_dim) == -1
+    assert "(4,128), (4,512) or (128,512)" in _err(lib)
+
+
+def test_compressor_argument_checks(lib):
+    ok_row = (FAKE, FAKE + STATE, 3)
+    for eps in (0.0, -1.0, float("inf"), float("nan")):
+        assert _compress(lib, [ok_row], eps=eps) == -1 and "epsilon" in _err(lib)
+    for pos in (0, 0xFFFFFFFF):
+        assert _compress(lib, [(FAKE, FAKE + STATE, pos)]) == -1 and "position" in _err(lib)
+    assert _compress(lib, [ok_row], ptr=FAKE + 4) == -3
+    assert _compress(lib, [(FAKE, FAKE + STATE - 16, 3)]) == -1 and "overlap" in _err(lib)
+    assert _compress(lib, [ok_row, (FAKE + STATE, FAKE + 2 * STATE, 3)]) == -1 and "overlap" in _err(lib)
+    assert _compress(lib, [ok_row, (FAKE + 2 * STATE, FAKE + 3 * STATE, 3)]) != -1 or "overlap" not in _err(lib)
+    assert _compress(lib, [(FAKE, FAKE + STATE, 3)] * 9) == -1 and "rows must be 1..=8" in _err(lib)
