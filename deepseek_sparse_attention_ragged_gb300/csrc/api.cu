@@ -219,9 +219,11 @@ uint32_t max_q_row(const ds_row_set_t* set) {
 
 // ---- stage launchers ---------------------------------------------------------------
 // With `valid`, entry e scores only its keys j < valid[e] (the tensor map still
-// spans the row's kv_len keys).
+// spans the row's kv_len keys). `inputs_ready`: the launch follows an ordinary
+// launch (the clear kernel), so every input is complete and the key stream may
+// start before the programmatic wait.
 int run_indexer(const ds_row_set_t* set, const ds_bf16* q_index, const float* w_index, float* scores,
-                uint64_t stride, uint32_t* hist, uint32_t* status, cudaStream_t stream, bool pdl,
+                uint64_t stride, uint32_t* hist, uint32_t* status, cudaStream_t stream, bool inputs_ready,
                 const uint32_t* valid = nullptr) {
     int rc = get_encoder();
     if (rc) return rc;
@@ -246,11 +248,12 @@ int run_indexer(const ds_row_set_t* set, const ds_bf16* q_index, const float* w_
     p.hist = hist;
     p.status = status;
     p.score_stride = stride;
+    p.inputs_ready = inputs_ready ? 1u : 0u;
     p.rows = (uint32_t)set->rows;
     p.total_tiles = tiles;
     const int sms = num_sms();
     if (sms <= 0) return fail(DS_ECUDA, "no CUDA device");
-    cudaError_t err = launch_indexer(p, sms, stream, pdl);
+    cudaError_t err = launch_indexer(p, sms, stream, true);
     return err == cudaSuccess ? DS_OK : cuda_fail(err, "indexer launch");
 }
 

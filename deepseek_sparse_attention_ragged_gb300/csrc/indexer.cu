@@ -96,6 +96,10 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_score_kernel(const __grid
     const uint32_t g_begin = (uint32_t)(((uint64_t)blockIdx.x * T) / G);
     const uint32_t g_end = (uint32_t)(((uint64_t)(blockIdx.x + 1) * T) / G);
 
+    // Inputs may still be in flight from the previous kernel (programmatic
+    // launch): then nothing is read before it completes.
+    if (!p.inputs_ready) pdl_wait();
+
     // ---- setup -------------------------------------------------------------
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {

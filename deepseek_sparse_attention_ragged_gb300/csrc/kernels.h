@@ -18,6 +18,8 @@ struct IndexerParams {
     float* scores;                  // entry e at e * score_stride
     uint32_t* hist;                 // optional [8][2048] score-key histogram
     uint32_t* status;               // device status word
+    uint32_t inputs_ready;          // 1: every input was complete when the launch began (it follows an
+                                    // ordinary launch), so loads may start before griddepcontrol.wait
     uint64_t score_stride;
     uint32_t rows;
     uint32_t total_tiles;
