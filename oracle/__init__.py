@@ -127,6 +127,25 @@ def topk_causal(scores, start_pos: int, offset: int = 0, ratio: int = 4,
     return out
 
 
+def indexer_topk_queries(q, w, keys, start_pos: int, offset: int = 0, ratio: int = 4,
+                         width: int = TOP_K) -> Tuple[np.ndarray, np.ndarray]:
+    """Several consecutive queries of one row (the score kernel's query loop,
+    deepseek_indexer_score_mma_rows_bf16): query j (q[j], w[j]) sits at position
+    start_pos + j, so its causal count is min(L, (start_pos + j + 1) // ratio).
+    Reading for the selection: each query takes its own top-`width` with the
+    finalize rule at its own count (the pages' top-k kernels take query 0 only).
+    Returns scores [Q, L] and indices int32 [Q, width]."""
+    q = np.asarray(q, np.float64)
+    w = np.asarray(w, np.float64)
+    nq = q.shape[0]
+    scores = np.empty((nq, len(keys)))
+    out = np.empty((nq, int(width)), np.int32)
+    for j in range(nq):
+        scores[j] = indexer_score_causal(q[j], w[j], keys, int(start_pos) + j, ratio)
+        out[j] = topk_causal(scores[j], int(start_pos) + j, offset, ratio, width)
+    return scores, out
+
+
 # ---------------------------------------------------------------------------
 # (3)+(4) Gather and sink-softmax sparse attention
 # deepseek_rows.metal, "Sparse attention (selected shared-KV rows with learned

@@ -157,6 +157,49 @@ def test_topk_causal_offset_and_fill():
     assert out.tolist() == [103, 102, 101, 100, -1, -1]
 
 
+def _queries_bruteforce(q, w, keys, start_pos, offset, width):
+    """Per query: exact integer scores (Fractions), the causal count from the
+    query's own position, and ranks counted pairwise."""
+    out = []
+    for j in range(len(q)):
+        valid = min(len(keys), (start_pos + j + 1) // 4)
+        s = []
+        for k in keys[:valid]:
+            s.append(sum(Fraction(w[j][h]) * max(0, sum(Fraction(a) * b for a, b in zip(q[j][h], k)))
+                          for h in range(len(w[j]))))
+        row = [-1] * width
+        for a in range(valid):
+            rank = sum(1 for b in range(valid) if s[b] > s[a] or (s[b] == s[a] and b < a))
+            if rank < width:
+                row[rank] = a + offset
+        out.append(row)
+    return out
+
+
+def test_indexer_queries_bruteforce():
+    rng = np.random.default_rng(31)
+    nq, heads, dim, L = 6, 3, 4, 24
+    q = rng.integers(-2, 3, size=(nq, heads, dim))
+    w = rng.integers(-2, 3, size=(nq, heads))
+    keys = rng.integers(-2, 3, size=(L, dim))
+    # start_pos 73: counts 18, 18, 18, 19, 19, 19 (the count steps inside the run)
+    for start_pos, offset, width in [(73, 0, 30), (73, 5, 7), (90, 2, 10)]:
+        s, idx = oracle.indexer_topk_queries(q, w, keys, start_pos, offset=offset, width=width)
+        assert idx.tolist() == _queries_bruteforce(q.tolist(), w.tolist(), keys.tolist(), start_pos, offset, width)
+        for j in range(nq):
+            valid = min(L, (start_pos + j + 1) // 4)
+            assert np.all(s[j, valid:] == -np.inf)
+
+
+def test_indexer_queries_one_query_is_the_positioned_indexer():
+    rng = np.random.default_rng(32)
+    q, w, keys = rng.standard_normal((1, 4, 8)), rng.standard_normal((1, 4)), rng.standard_normal((50, 8))
+    s, idx = oracle.indexer_topk_queries(q, w, keys, 130, offset=3, width=16)
+    ref = oracle.indexer_score_causal(q[0], w[0], keys, 130)
+    np.testing.assert_array_equal(s[0], ref)
+    assert idx[0].tolist() == oracle.topk_causal(ref, 130, offset=3, width=16).tolist()
+
+
 # ---------------------------------------------------------------------------
 # Sparse attention
 # ---------------------------------------------------------------------------
@@ -468,6 +511,23 @@ def _topk_high_index_ties(scores, width):
     return out
 
 
+_REAL_QUERIES = oracle.indexer_topk_queries
+
+
+def _queries_one_position(q, w, keys, start_pos, offset=0, ratio=4, width=512):
+    # mistake: every query takes the first query's causal count
+    s, _ = _REAL_QUERIES(q, w, keys, start_pos, offset, ratio, width)
+    idx = np.stack([oracle.topk_causal(np.asarray(oracle.indexer_score_causal(q[j], w[j], keys, start_pos, ratio)),
+                                       start_pos, offset, ratio, width) for j in range(len(q))])
+    return s, idx
+
+
+def _queries_first_weights(q, w, keys, start_pos, offset=0, ratio=4, width=512):
+    # mistake: every query uses the first query's head weights
+    w = np.broadcast_to(np.asarray(w)[:1], np.asarray(w).shape)
+    return _REAL_QUERIES(q, w, keys, start_pos, offset, ratio, width)
+
+
 _REAL_ATTENTION = oracle.sparse_attention
 _REAL_COMPRESS = oracle.compress_kv
 
@@ -497,6 +557,8 @@ def test_planted_mistakes_are_caught(monkeypatch):
     caught = []
     for name, fake in [("indexer_score", _no_relu), ("indexer_score", _transposed_weights),
                        ("topk", _topk_high_index_ties),
+                       ("indexer_topk_queries", _queries_one_position),
+                       ("indexer_topk_queries", _queries_first_weights),
                        ("sparse_attention", _attention_sink_with_value),
                        ("compress_kv", _compress_without_ape), ("compress_kv", _compress_current_block_only)]:
         monkeypatch.setattr(oracle, name, fake)
@@ -504,6 +566,7 @@ def test_planted_mistakes_are_caught(monkeypatch):
             "indexer_score": [test_indexer_golden, test_indexer_relu_identity,
                               test_indexer_one_hot_weights_select_head],
             "topk": [test_topk_golden, test_topk_signed_zero_ties],
+            "indexer_topk_queries": [test_indexer_queries_bruteforce],
             "sparse_attention": [test_attention_golden, test_attention_dense_closed_form],
             "compress_kv": [lambda: test_compressor_uniform_scores_give_the_window_mean(4, 128),
                             lambda: test_compressor_token_write_and_no_output_mid_block(4, 128)],
