@@ -25,6 +25,7 @@ __all__ = [
     "ds_rows_workspace_bytes", "workspace", "ds_rows_indexer_score", "ds_rows_topk", "ds_rows_topk_static",
     "ds_rows_sparse_attn", "ds_rows_decode", "ds_rows_version",
     "IndexerRow", "ds_rows_indexer_topk_workspace_bytes", "indexer_topk_workspace", "ds_rows_indexer_topk",
+    "ds_rows_indexer_topk_queries_workspace_bytes", "ds_rows_indexer_topk_queries",
     "CompressorRow", "ds_rows_compress_kv",
     "ROWS_MAX", "INDEX_HEADS", "INDEX_DIM", "TOP_K", "HEADS", "DIM",
 ]
@@ -112,6 +113,11 @@ def load():
     lib.ds_rows_indexer_topk_workspace_bytes.restype = sz
     lib.ds_rows_indexer_topk.argtypes = [i32, ctypes.POINTER(IndexerRow), ctypes.POINTER(vp), vp, vp, vp, vp, sz, vp]
     lib.ds_rows_indexer_topk.restype = i32
+    lib.ds_rows_indexer_topk_queries_workspace_bytes.argtypes = [i32, ctypes.POINTER(IndexerRow), ctypes.c_uint32]
+    lib.ds_rows_indexer_topk_queries_workspace_bytes.restype = sz
+    lib.ds_rows_indexer_topk_queries.argtypes = [i32, ctypes.POINTER(IndexerRow), ctypes.c_uint32,
+                                                 ctypes.POINTER(vp), vp, vp, vp, vp, sz, vp]
+    lib.ds_rows_indexer_topk_queries.restype = i32
     lib.ds_rows_compress_kv.argtypes = [i32, ctypes.POINTER(CompressorRow), vp, vp, vp, vp, ctypes.c_uint32,
                                          ctypes.c_uint32, ctypes.c_float, vp, vp]
     lib.ds_rows_compress_kv.restype = i32
@@ -333,6 +339,15 @@ def _indexer_table(rows):
     return arr, len(rows)
 
 
+def ds_rows_indexer_topk_queries_workspace_bytes(rows, query_len=1) -> int:
+    lib = load()
+    tab, n = _indexer_table(rows)
+    b = lib.ds_rows_indexer_topk_queries_workspace_bytes(n, tab, int(query_len))
+    if b == 0:
+        raise DsRowsError(-1, lib.ds_rows_last_error().decode())
+    return int(b)
+
+
 def ds_rows_indexer_topk_workspace_bytes(rows) -> int:
     lib = load()
     tab, n = _indexer_table(rows)
@@ -342,30 +357,45 @@ def ds_rows_indexer_topk_workspace_bytes(rows) -> int:
     return int(b)
 
 
-def indexer_topk_workspace(rows, device=None) -> torch.Tensor:
-    """A workspace tensor for ds_rows_indexer_topk (uint8, 256-byte aligned)."""
-    return torch.empty(ds_rows_indexer_topk_workspace_bytes(rows), dtype=torch.uint8,
+def indexer_topk_workspace(rows, device=None, query_len=1) -> torch.Tensor:
+    """A workspace tensor for ds_rows_indexer_topk(_queries) (uint8, 256-byte aligned)."""
+    return torch.empty(ds_rows_indexer_topk_queries_workspace_bytes(rows, query_len), dtype=torch.uint8,
                        device=device if device is not None else "cuda")
 
 
-def ds_rows_indexer_topk(rows, q_index, w_index, index_keys, indices, workspace_t=None, stream=None):
-    """Positioned indexer score and causal top-512 of each row (IndexerRow entries):
-    512 indices (+ offset, -1 fill) per row at output_offset."""
+def _indexer_call(fn, rows, query_len, q_index, w_index, index_keys, indices, workspace_t, stream):
     lib = load()
     tab, n = _indexer_table(rows)
-    q_rows = max(tab[e].q_row for e in range(n)) + 1
+    q_rows = max(tab[e].q_row for e in range(n)) + query_len
     _require(q_index, "q_index", torch.bfloat16, q_rows * INDEX_HEADS * INDEX_DIM)
     _require(w_index, "w_index", torch.float32, q_rows * INDEX_HEADS)
     if len(index_keys) != n:
         raise ValueError(f"index_keys: {len(index_keys)} caches for {n} rows")
     for e in range(n):
         _require(index_keys[e], f"index_keys[{e}]", torch.bfloat16, tab[e].kv_len * INDEX_DIM)
-    _require(indices, "indices", torch.int32, max(tab[e].output_offset for e in range(n)) + TOP_K)
+    _require(indices, "indices", torch.int32, max(tab[e].output_offset for e in range(n)) + TOP_K * query_len)
     if workspace_t is None:
-        workspace_t = indexer_topk_workspace(list(tab)[:n], q_index.device)
+        workspace_t = indexer_topk_workspace(list(tab)[:n], q_index.device, query_len)
     ks = (ctypes.c_void_p * n)(*[k.data_ptr() for k in index_keys])
-    _check(lib, lib.ds_rows_indexer_topk(n, tab, ks, _ptr(q_index), _ptr(w_index), _ptr(indices),
-                                         _ptr(workspace_t), workspace_t.numel(), _stream(stream)))
+    args = (_ptr(q_index), _ptr(w_index), _ptr(indices), _ptr(workspace_t), workspace_t.numel(), _stream(stream))
+    if fn == "single":
+        _check(lib, lib.ds_rows_indexer_topk(n, tab, ks, *args))
+    else:
+        _check(lib, lib.ds_rows_indexer_topk_queries(n, tab, int(query_len), ks, *args))
+
+
+def ds_rows_indexer_topk(rows, q_index, w_index, index_keys, indices, workspace_t=None, stream=None):
+    """Positioned indexer score and causal top-512 of each row (IndexerRow entries):
+    512 indices (+ offset, -1 fill) per row at output_offset."""
+    _indexer_call("single", rows, 1, q_index, w_index, index_keys, indices, workspace_t, stream)
+
+
+def ds_rows_indexer_topk_queries(rows, query_len, q_index, w_index, index_keys, indices, workspace_t=None,
+                                 stream=None):
+    """ds_rows_indexer_topk for query_len consecutive queries per row: query j of a
+    row uses query row q_row + j, position start_pos + j, and writes its 512
+    indices at output_offset + 512 j."""
+    _indexer_call("queries", rows, query_len, q_index, w_index, index_keys, indices, workspace_t, stream)
 
 
 # ---------------------------------------------------------------------------

@@ -51,10 +51,12 @@ struct Layout {
     uint64_t score_stride;  // floats per row of the decode scores
 };
 
+// `rows` table entries (up to kVRowsMax virtual rows for the multi-query
+// indexer): one histogram and one score row each.
 Layout make_layout(int rows, const ds_row_t* table, bool attention = true) {
     Layout L;
     L.hist = 256;
-    L.flags = align256(L.hist + (size_t)kRowsMax * kHistBins * 4);
+    L.flags = align256(L.hist + (size_t)(rows > kRowsMax ? rows : kRowsMax) * kHistBins * 4);
     L.ctl_end = align256(L.flags + ((size_t)kRowsMax * kHeads + kRowsMax) * 4);
     L.part = L.ctl_end;
     uint32_t chunks = 0, max_len = 0;
@@ -157,18 +159,25 @@ int check_set(const ds_row_set_t* set, unsigned needs) {
     return DS_OK;
 }
 
-// Positioned indexer rows (`dispatch_deepseek_indexer_rows`): kv_len nonzero and
-// not shorter than the causal count (start_pos + 1) / 4; offset nonnegative and
-// offset + count - 1 within int32; 512-slot outputs disjoint.
-int check_indexer_rows(int rows, const ds_indexer_row_t* table, const ds_bf16* const* keys, bool need_keys) {
+// Positioned indexer rows (`dispatch_deepseek_indexer_rows`), each with
+// query_len consecutive queries (query j at position start_pos + j): kv_len
+// nonzero and not shorter than the last query's causal count
+// (start_pos + query_len) / 4; offset nonnegative and offset + count - 1
+// within int32; the rows' query_len x 512 output slots disjoint.
+int check_indexer_rows(int rows, const ds_indexer_row_t* table, const ds_bf16* const* keys, bool need_keys,
+                       uint32_t query_len = 1) {
     if (rows < 1 || rows > DS_ROWS_MAX) return fail(DS_EINVAL, "rows must be 1..=%d, got %d", DS_ROWS_MAX, rows);
     if (!table) return fail(DS_EINVAL, "indexer row table is NULL");
+    if (query_len < 1 || (uint64_t)rows * query_len > DS_INDEX_VROWS_MAX)
+        return fail(DS_EINVAL, "rows x query_len must be 1..=%d, got %d x %u", DS_INDEX_VROWS_MAX, rows, query_len);
     if (need_keys && !keys) return fail(DS_EINVAL, "index_keys is NULL");
+    const uint64_t span = (uint64_t)DS_TOPK * query_len;
     for (int e = 0; e < rows; ++e) {
         const ds_indexer_row_t& r = table[e];
         if (r.kv_len == 0) return fail(DS_EINVAL, "indexer row %d: kv_len must be nonzero", e);
-        if (r.start_pos == 0xFFFFFFFFu) return fail(DS_EINVAL, "indexer row %d: position overflows", e);
-        const uint32_t causal = (r.start_pos + 1) / 4;
+        if ((uint64_t)r.start_pos + query_len > 0xFFFFFFFFull)
+            return fail(DS_EINVAL, "indexer row %d: position overflows", e);
+        const uint32_t causal = (r.start_pos + query_len) / 4;  // the last query's count
         if (r.kv_len < causal)
             return fail(DS_EINVAL, "indexer row %d: kv_len %u is shorter than %u causal compressed entries", e,
                         r.kv_len, causal);
@@ -176,31 +185,35 @@ int check_indexer_rows(int rows, const ds_indexer_row_t* table, const ds_bf16* c
             return fail(DS_EINVAL, "indexer row %d: offset must be nonnegative; -1 is reserved for the sentinel", e);
         if (causal > 0 && (int64_t)r.offset + (int64_t)causal - 1 > (int64_t)INT32_MAX)
             return fail(DS_EINVAL, "indexer row %d: offset plus compressed index exceeds i32", e);
-        if ((uint64_t)r.output_offset + DS_TOPK > 0xFFFFFFFFull)
+        if ((uint64_t)r.output_offset + span > 0xFFFFFFFFull)
             return fail(DS_ESIZE, "indexer row %d: output range exceeds u32", e);
-        if ((uint64_t)r.q_row * DS_INDEX_HEADS * DS_INDEX_DIM > 0xFFFFFFFFFFull)
+        if (((uint64_t)r.q_row + query_len) * DS_INDEX_HEADS * DS_INDEX_DIM > 0xFFFFFFFFFFull)
             return fail(DS_ESIZE, "indexer row %d: q_row %u is out of range", e, r.q_row);
         if (need_keys) {
             if (!keys[e]) return fail(DS_EINVAL, "indexer row %d: keys are NULL", e);
             if (!aligned16(keys[e])) return fail(DS_EALIGN, "indexer row %d: keys not 16-B aligned", e);
         }
         for (int o = 0; o < e; ++o) {
-            const uint64_t a0 = r.output_offset, a1 = a0 + DS_TOPK;
-            const uint64_t b0 = table[o].output_offset, b1 = b0 + DS_TOPK;
+            const uint64_t a0 = r.output_offset, a1 = a0 + span;
+            const uint64_t b0 = table[o].output_offset, b1 = b0 + span;
             if (a0 < b1 && b0 < a1) return fail(DS_EINVAL, "indexer outputs of rows %d and %d overlap", o, e);
         }
     }
     return DS_OK;
 }
 
-// The selection table of positioned rows: kv_len = the causal count, 512 slots.
-void indexer_selection_table(int rows, const ds_indexer_row_t* table, ds_row_t* sel) {
-    for (int e = 0; e < rows; ++e) {
-        sel[e].kv_len = (table[e].start_pos + 1) / 4;
-        sel[e].width = DS_TOPK;
-        sel[e].index_offset = table[e].output_offset;
-        sel[e].q_row = table[e].q_row;
-    }
+// The selection table of positioned rows, one entry per (row e, query j) at
+// v = e * query_len + j: kv_len = that query's causal count, 512 slots at
+// output_offset + 512 j, query row q_row + j.
+void indexer_selection_table(int rows, const ds_indexer_row_t* table, uint32_t query_len, ds_row_t* sel) {
+    for (int e = 0; e < rows; ++e)
+        for (uint32_t j = 0; j < query_len; ++j) {
+            ds_row_t& v = sel[e * query_len + j];
+            v.kv_len = (table[e].start_pos + j + 1) / 4;
+            v.width = DS_TOPK;
+            v.index_offset = table[e].output_offset + DS_TOPK * j;
+            v.q_row = table[e].q_row + j;
+        }
 }
 
 int check_workspace(const ds_row_set_t* set, void* ws, size_t bytes, const Layout& L) {
@@ -211,37 +224,52 @@ int check_workspace(const ds_row_set_t* set, void* ws, size_t bytes, const Layou
     return DS_OK;
 }
 
-uint32_t max_q_row(const ds_row_set_t* set) {
-    uint32_t m = 0;
-    for (int e = 0; e < set->rows; ++e) m = set->table[e].q_row > m ? set->table[e].q_row : m;
-    return m;
-}
-
 // ---- stage launchers ---------------------------------------------------------------
-// With `valid`, entry e scores only its keys j < valid[e] (the tensor map still
-// spans the row's kv_len keys). `inputs_ready`: the launch follows an ordinary
-// launch (the clear kernel), so every input is complete and the key stream may
-// start before the programmatic wait.
-int run_indexer(const ds_row_set_t* set, const ds_bf16* q_index, const float* w_index, float* scores,
-                uint64_t stride, uint32_t* hist, uint32_t* status, cudaStream_t stream, bool inputs_ready,
-                const uint32_t* valid = nullptr) {
+// Entry e of `set` has query_len consecutive queries, virtual rows
+// v = e * query_len + j with query row q_row + j; with `valid`, virtual row v
+// scores only its keys j < valid[v] (the tensor map still spans the entry's
+// kv_len keys), else every key. One query per entry runs the one-query kernel;
+// more run the grouped kernel, up to kIndexerGroup queries per key tile.
+// `inputs_ready`: the launch follows an ordinary launch (the clear kernel), so
+// every input is complete and the key stream may start before the programmatic
+// wait.
+template <class P>
+int fill_and_launch_indexer(P& p, int group, const ds_row_set_t* set, uint32_t query_len, const ds_bf16* q_index,
+                            const float* w_index, float* scores, uint64_t stride, uint32_t* hist, uint32_t* status,
+                            cudaStream_t stream, bool inputs_ready, const uint32_t* valid) {
     int rc = get_encoder();
     if (rc) return rc;
-    IndexerParams p;  // ~1.3 KB with the tensor maps; built per call on the host
     std::memset(&p, 0, sizeof(p));
     const uint32_t tile = indexer_tile_keys();
-    uint32_t tiles = 0;
+    constexpr uint32_t kSegs = sizeof(p.tile_begin) / sizeof(p.tile_begin[0]);
+    constexpr uint32_t kVRows = sizeof(p.valid) / sizeof(p.valid[0]);
+    if ((uint64_t)set->rows * query_len > kVRows) return fail(DS_EINVAL, "too many indexer rows");
+    uint32_t tiles = 0, segs = 0, max_q = 0;
     for (int e = 0; e < set->rows; ++e) {
         const ds_row_t& r = set->table[e];
-        const uint32_t n = valid ? valid[e] : r.kv_len;
-        p.kv_len[e] = n;
-        p.q_row[e] = r.q_row;
-        p.tile_begin[e] = tiles;
-        tiles += (n + tile - 1) / tile;
+        for (uint32_t j0 = 0; j0 < query_len; j0 += group) {
+            const uint32_t nq = query_len - j0 < (uint32_t)group ? query_len - j0 : (uint32_t)group;
+            const uint32_t v0 = e * query_len + j0;
+            uint32_t cover = 0;
+            for (uint32_t i = 0; i < nq; ++i) {
+                const uint32_t n = valid ? valid[v0 + i] : r.kv_len;
+                p.valid[v0 + i] = n;
+                p.q_row[v0 + i] = r.q_row + j0 + i;
+                cover = n > cover ? n : cover;
+            }
+            if (segs >= kSegs) return fail(DS_EINVAL, "too many indexer segments");
+            p.tile_begin[segs] = tiles;
+            p.seg_entry[segs] = (uint8_t)e;
+            p.seg_vrow[segs] = (uint8_t)v0;
+            p.seg_queries[segs] = (uint8_t)nq;
+            ++segs;
+            tiles += (cover + tile - 1) / tile;
+        }
+        if (r.q_row + query_len > max_q) max_q = r.q_row + query_len;
         rc = encode_rows128(&p.kmap[e], set->index_keys[e], r.kv_len, 128, "indexer keys");
         if (rc) return rc;
     }
-    rc = encode_rows128(&p.qmap, q_index, (uint64_t)(max_q_row(set) + 1) * DS_INDEX_HEADS, 64, "indexer q");
+    rc = encode_rows128(&p.qmap, q_index, (uint64_t)max_q * DS_INDEX_HEADS, 64, "indexer q");
     if (rc) return rc;
     p.w = w_index;
     p.scores = scores;
@@ -250,6 +278,8 @@ int run_indexer(const ds_row_set_t* set, const ds_bf16* q_index, const float* w_
     p.score_stride = stride;
     p.inputs_ready = inputs_ready ? 1u : 0u;
     p.rows = (uint32_t)set->rows;
+    p.segs = segs;
+    p.vrows = (uint32_t)set->rows * query_len;
     p.total_tiles = tiles;
     const int sms = num_sms();
     if (sms <= 0) return fail(DS_ECUDA, "no CUDA device");
@@ -257,9 +287,24 @@ int run_indexer(const ds_row_set_t* set, const ds_bf16* q_index, const float* w_
     return err == cudaSuccess ? DS_OK : cuda_fail(err, "indexer launch");
 }
 
+int run_indexer(const ds_row_set_t* set, uint32_t query_len, const ds_bf16* q_index, const float* w_index,
+                float* scores, uint64_t stride, uint32_t* hist, uint32_t* status, cudaStream_t stream,
+                bool inputs_ready, const uint32_t* valid = nullptr) {
+    // The tables hold CUtensorMaps (~1.3-2.2 KB); built per call on the host.
+    if (query_len == 1) {
+        IndexerParams1 p;
+        return fill_and_launch_indexer(p, 1, set, query_len, q_index, w_index, scores, stride, hist, status, stream,
+                                       inputs_ready, valid);
+    }
+    IndexerParamsG p;
+    return fill_and_launch_indexer(p, kIndexerGroup, set, query_len, q_index, w_index, scores, stride, hist, status,
+                                   stream, inputs_ready, valid);
+}
+
 int run_topk(const ds_row_set_t* set, const float* scores, uint64_t stride, int32_t* out, const uint32_t* out_offset,
              uint8_t* ws, const Layout& L, bool with_hist, bool by_index, cudaStream_t stream,
              const int32_t* offsets = nullptr) {
+    if (set->rows > kVRowsMax) return fail(DS_EINVAL, "too many top-k rows");
     TopkParams p;
     std::memset(&p, 0, sizeof(p));
     const uint32_t chunk = topk_chunk();
@@ -405,7 +450,7 @@ int ds_rows_indexer_score(const ds_row_set_t* set, const ds_bf16* q_index, const
         if (score_stride < set->table[e].kv_len)
             return fail(DS_EINVAL, "score_stride %zu is shorter than row %d (kv_len %u)", score_stride, e,
                         set->table[e].kv_len);
-    return run_indexer(set, q_index, w_index, scores, score_stride, nullptr, nullptr, (cudaStream_t)stream, false);
+    return run_indexer(set, 1, q_index, w_index, scores, score_stride, nullptr, nullptr, (cudaStream_t)stream, false);
 }
 
 int ds_rows_topk(const ds_row_set_t* set, const float* scores, size_t score_stride, int32_t* indices,
@@ -466,7 +511,7 @@ int ds_rows_decode(const ds_row_set_t* set, const ds_bf16* q_index, const float*
     float* scores = reinterpret_cast<float*>(ws + L.scores);
     uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
     uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
-    rc = run_indexer(set, q_index, w_index, scores, L.score_stride, hist, status, s, true);
+    rc = run_indexer(set, 1, q_index, w_index, scores, L.score_stride, hist, status, s, true);
     if (rc) return rc;
     // Selection and attention in one kernel: one 8-CTA cluster per row keeps the
     // selection on chip and attends over it in best-first order, the order of
@@ -502,35 +547,43 @@ int ds_rows_topk_static(const ds_row_set_t* set, const float* scores, size_t sco
     return run_topk(set, scores, score_stride, indices, off, ws, L, true, false, s);
 }
 
-size_t ds_rows_indexer_topk_workspace_bytes(int rows, const ds_indexer_row_t* table) {
-    if (check_indexer_rows(rows, table, nullptr, false)) return 0;
-    ds_row_t sel[DS_ROWS_MAX];
-    indexer_selection_table(rows, table, sel);
-    return make_layout(rows, sel, false).total;
+size_t ds_rows_indexer_topk_queries_workspace_bytes(int rows, const ds_indexer_row_t* table, uint32_t query_len) {
+    if (check_indexer_rows(rows, table, nullptr, false, query_len)) return 0;
+    ds_row_t sel[DS_INDEX_VROWS_MAX];
+    indexer_selection_table(rows, table, query_len, sel);
+    return make_layout(rows * (int)query_len, sel, false).total;
 }
 
-int ds_rows_indexer_topk(int rows, const ds_indexer_row_t* table, const ds_bf16* const* index_keys,
-                         const ds_bf16* q_index, const float* w_index, int32_t* indices, void* workspace,
-                         size_t workspace_bytes, void* stream) {
-    int rc = check_indexer_rows(rows, table, index_keys, true);
+size_t ds_rows_indexer_topk_workspace_bytes(int rows, const ds_indexer_row_t* table) {
+    return ds_rows_indexer_topk_queries_workspace_bytes(rows, table, 1);
+}
+
+int ds_rows_indexer_topk_queries(int rows, const ds_indexer_row_t* table, uint32_t query_len,
+                                 const ds_bf16* const* index_keys, const ds_bf16* q_index, const float* w_index,
+                                 int32_t* indices, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_indexer_rows(rows, table, index_keys, true, query_len);
     if (rc) return rc;
     rc = check_indexer_args(q_index, w_index);
     if (rc) return rc;
     if (!indices) return fail(DS_EINVAL, "indices is NULL");
-    ds_row_t keys_tab[DS_ROWS_MAX], sel_tab[DS_ROWS_MAX];
-    uint32_t valid[DS_ROWS_MAX], out_off[DS_ROWS_MAX];
-    int32_t offsets[DS_ROWS_MAX];
-    indexer_selection_table(rows, table, sel_tab);
+    const int vrows = rows * (int)query_len;
+    ds_row_t keys_tab[DS_ROWS_MAX], sel_tab[DS_INDEX_VROWS_MAX];
+    uint32_t valid[DS_INDEX_VROWS_MAX], out_off[DS_INDEX_VROWS_MAX];
+    int32_t offsets[DS_INDEX_VROWS_MAX];
+    indexer_selection_table(rows, table, query_len, sel_tab);
     for (int e = 0; e < rows; ++e) {
-        keys_tab[e] = sel_tab[e];
+        keys_tab[e] = sel_tab[e * query_len];
         keys_tab[e].kv_len = table[e].kv_len;  // the tensor map spans the whole cache
-        valid[e] = sel_tab[e].kv_len;
-        out_off[e] = table[e].output_offset;
-        offsets[e] = table[e].offset;
+        keys_tab[e].q_row = table[e].q_row;
     }
-    const Layout L = make_layout(rows, sel_tab, false);
+    for (int v = 0; v < vrows; ++v) {
+        valid[v] = sel_tab[v].kv_len;
+        out_off[v] = sel_tab[v].index_offset;
+        offsets[v] = table[v / query_len].offset;
+    }
+    const Layout L = make_layout(vrows, sel_tab, false);
     const ds_row_set_t kset = {rows, keys_tab, index_keys, nullptr};
-    const ds_row_set_t sset = {rows, sel_tab, nullptr, nullptr};
+    const ds_row_set_t sset = {vrows, sel_tab, nullptr, nullptr};
     rc = check_workspace(&sset, workspace, workspace_bytes, L);
     if (rc) return rc;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -538,11 +591,19 @@ int ds_rows_indexer_topk(int rows, const ds_indexer_row_t* table, const ds_bf16*
     cudaError_t err = launch_clear(reinterpret_cast<uint32_t*>(ws), (uint32_t)(L.ctl_end / 4), s);
     if (err != cudaSuccess) return cuda_fail(err, "workspace clear");
     float* scores = reinterpret_cast<float*>(ws + L.scores);
-    rc = run_indexer(&kset, q_index, w_index, scores, L.score_stride, reinterpret_cast<uint32_t*>(ws + L.hist),
-                     reinterpret_cast<uint32_t*>(ws + L.status), s, true, valid);
+    rc = run_indexer(&kset, query_len, q_index, w_index, scores, L.score_stride,
+                     reinterpret_cast<uint32_t*>(ws + L.hist), reinterpret_cast<uint32_t*>(ws + L.status), s, true,
+                     valid);
     if (rc) return rc;
-    // The indexer built the level-0 histogram of the valid scores.
+    // The indexer built the level-0 histogram of each query's valid scores.
     return run_topk(&sset, scores, L.score_stride, indices, out_off, ws, L, false, false, s, offsets);
+}
+
+int ds_rows_indexer_topk(int rows, const ds_indexer_row_t* table, const ds_bf16* const* index_keys,
+                         const ds_bf16* q_index, const float* w_index, int32_t* indices, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    return ds_rows_indexer_topk_queries(rows, table, 1, index_keys, q_index, w_index, indices, workspace,
+                                        workspace_bytes, stream);
 }
 
 int ds_rows_compress_kv(int rows, const ds_compressor_row_t* table, const float* kv, const float* score,

@@ -21,6 +21,17 @@
 //
 // Optional fused output: a 2048-bin histogram of the order-preserving score
 // keys per row (top 11 bits), used by the top-k stage to find its threshold.
+//
+// Several queries per row (the kernel's query loop on the pages; query i of an
+// entry sits at its position + i and scores its own causal count of keys): a
+// segment is an entry with up to four consecutive queries, whose query rows
+// stack along N, so each key tile is read from HBM once for all of them:
+// D[128 keys x 64 nq] = K_tile . [q_0; ...; q_{nq-1}]^T. Eight epilogue warps
+// split the queries, two warps per TMEM lane quarter; each
+// query's score of a key is the same arithmetic as with one query, so it does
+// not depend on its neighbours.
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -29,49 +40,94 @@ namespace dsrows {
 
 namespace {
 
-constexpr int kThreads = 192;
 constexpr int kTileKeys = 128;
-constexpr int kStages = 5;
 constexpr int kHalfBytes = kTileKeys * 64 * 2;  // one 64-column SW128 box of a key tile
 constexpr int kTileBytes = 2 * kHalfBytes;      // 32 KiB
-constexpr int kQHalfBytes = 64 * 64 * 2;        // 8 KiB
-constexpr int kQBytes = 2 * kQHalfBytes;        // 16 KiB
-constexpr int kAccCols = 64;
-constexpr int kAccBufs = 2;
-constexpr uint32_t kTmemCols = kAccCols * kAccBufs;  // 128 (power of two >= 32)
+constexpr int kQBoxBytes = 64 * 64 * 2;         // one query's 64 heads x 64 columns: 8 KiB
 
+// Shape of the kernel for G queries per key tile.
+//   G = 1: 5-stage key ring, double-buffered query, 4 epilogue warps (one
+//          key per thread), accumulators 2 x 64 TMEM columns, the head
+//          weights of every row and a 2048-bin u32 histogram in shared memory;
+//   G = 4: 4-stage key ring, one query buffer (up to 4 x 16 KiB), 8 epilogue
+//          warps (two per TMEM lane quarter, splitting the segment's queries
+//          evenly), accumulators 2 x 256 columns, the head weights of the
+//          current segment, and per query a 2048-bin histogram of 16-bit
+//          counts packed two to a word (flushed at least every kFlushTiles
+//          tiles, so a count stays below 2^16).
+template <int G>
+struct Shape {
+    static constexpr int kStages = G == 1 ? 5 : 4;
+    static constexpr int kQBufs = G == 1 ? 2 : 1;
+    static constexpr int kEpiWarps = G == 1 ? 4 : 8;
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    static constexpr int kQPerWarp = G * 4 / kEpiWarps;  // queries per epilogue thread, at most
+    static constexpr int kSegs = G == 1 ? kRowsMax : kSegMax;
+    static constexpr int kVRows = G == 1 ? kRowsMax : kVRowsMax;
+    static constexpr int kWRows = G == 1 ? kRowsMax : G;  // rows of head weights held
+    static constexpr int kHistWords = G == 1 ? kHistBins : G * kHistBins / 2;
+    static constexpr uint32_t kFlushTiles = 256;           // 256 x 128 keys < 2^16
+    static constexpr int kQHalfBytes = G * kQBoxBytes;    // 64 columns of G x 64 query rows
+    static constexpr int kQBytes = 2 * kQHalfBytes;
+    static constexpr uint32_t kAccCols = 64 * G;
+    static constexpr uint32_t kTmemCols = 2 * kAccCols;   // double-buffered; a power of two >= 32
+    // shared memory
+    static constexpr size_t keys = 0;
+    static constexpr size_t q = keys + (size_t)kStages * kTileBytes;
+    static constexpr size_t w = q + (size_t)kQBufs * kQBytes;
+    static constexpr size_t hist = w + (size_t)kWRows * kIdxHeads * 4;
+    static constexpr size_t bars = hist + (size_t)kHistWords * 4;
+};
+
+template <int G>
 struct __align__(8) Barriers {
-    uint64_t k_full[kStages];
-    uint64_t k_empty[kStages];
-    uint64_t q_full[2];
-    uint64_t q_empty[2];
-    uint64_t acc_full[kAccBufs];
-    uint64_t acc_empty[kAccBufs];
+    uint64_t k_full[Shape<G>::kStages];
+    uint64_t k_empty[Shape<G>::kStages];
+    uint64_t q_full[Shape<G>::kQBufs];
+    uint64_t q_empty[Shape<G>::kQBufs];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
     uint32_t tmem_base;
     uint32_t abort_flag;
 };
 
-struct SmemLayout {
-    static constexpr size_t keys = 0;
-    static constexpr size_t q = keys + (size_t)kStages * kTileBytes;
-    static constexpr size_t w = q + 2 * (size_t)kQBytes;
-    static constexpr size_t hist = w + (size_t)kRowsMax * kIdxHeads * 4;
-    static constexpr size_t bars = hist + (size_t)kHistBins * 4;
-    static constexpr size_t total = bars + sizeof(Barriers);
-};
-constexpr size_t kSmemBytes = SmemLayout::total + 1024;  // + alignment slack
+template <int G>
+constexpr size_t smem_bytes() {
+    return Shape<G>::bars + sizeof(Barriers<G>) + 1024;  // + alignment slack
+}
+static_assert(smem_bytes<1>() <= 227 * 1024 && smem_bytes<kIndexerGroup>() <= 227 * 1024, "shared memory");
 
-__device__ __forceinline__ int entry_of_tile(const IndexerParams& p, uint32_t g) {
-    int e = 0;
+template <int S, int V>
+__device__ __forceinline__ int segment_of_tile(const IndexerParamsT<S, V>& p, uint32_t g) {
+    int s = 0;
 #pragma unroll
-    for (int i = 1; i < kRowsMax; ++i)
-        if (i < (int)p.rows && g >= p.tile_begin[i]) e = i;
-    return e;
+    for (int i = 1; i < S; ++i)
+        if (i < (int)p.segs && g >= p.tile_begin[i]) s = i;
+    return s;
 }
 
 __device__ __forceinline__ float relu_nan(float x) {
     // max(0, x) that keeps NaN (a NaN dot product must poison the score).
-    return (x > 0.0f || x != x) ? x : 0.0f;
+    float r;
+    asm("max.NaN.f32 %0, %1, 0f00000000;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// sum_h w[h] relu(x[h]) over the 64 head dot products x of one key, with w in
+// registers (wr) or shared memory (w_s): four chains (heads h = c mod 4, in
+// head order), added pairwise.
+__device__ __forceinline__ float head_sum(const uint32_t (&x)[64], const float* wr, const float* w_s) {
+    float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int h = 0; h < kIdxHeads; h += 4) {
+        const float4 w4 = wr ? make_float4(wr[h], wr[h + 1], wr[h + 2], wr[h + 3])
+                             : *reinterpret_cast<const float4*>(w_s + h);
+        s4[0] = fmaf(relu_nan(__uint_as_float(x[h])), w4.x, s4[0]);
+        s4[1] = fmaf(relu_nan(__uint_as_float(x[h + 1])), w4.y, s4[1]);
+        s4[2] = fmaf(relu_nan(__uint_as_float(x[h + 2])), w4.z, s4[2]);
+        s4[3] = fmaf(relu_nan(__uint_as_float(x[h + 3])), w4.w, s4[3]);
+    }
+    return (s4[0] + s4[1]) + (s4[2] + s4[3]);
 }
 
 __device__ __forceinline__ void named_bar(int id, int count) {
@@ -80,21 +136,26 @@ __device__ __forceinline__ void named_bar(int id, int count) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThreads, 1) indexer_score_kernel(const __grid_constant__ IndexerParams p) {
+template <int G>
+using ParamsOf = IndexerParamsT<Shape<G>::kSegs, Shape<G>::kVRows>;
+
+template <int G>
+__device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
+    using S = Shape<G>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* keys_s = smem + SmemLayout::keys;
-    uint8_t* q_s = smem + SmemLayout::q;
-    float* w_s = reinterpret_cast<float*>(smem + SmemLayout::w);
-    uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + SmemLayout::hist);
-    Barriers* bar = reinterpret_cast<Barriers*>(smem + SmemLayout::bars);
+    uint8_t* keys_s = smem + S::keys;
+    uint8_t* q_s = smem + S::q;
+    float* w_s = reinterpret_cast<float*>(smem + S::w);
+    uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + S::hist);
+    Barriers<G>* bar = reinterpret_cast<Barriers<G>*>(smem + S::bars);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t G = gridDim.x;
+    const uint32_t NB = gridDim.x;
     const uint32_t T = p.total_tiles;
-    const uint32_t g_begin = (uint32_t)(((uint64_t)blockIdx.x * T) / G);
-    const uint32_t g_end = (uint32_t)(((uint64_t)(blockIdx.x + 1) * T) / G);
+    const uint32_t g_begin = (uint32_t)(((uint64_t)blockIdx.x * T) / NB);
+    const uint32_t g_end = (uint32_t)(((uint64_t)(blockIdx.x + 1) * T) / NB);
 
     // Inputs may still be in flight from the previous kernel (programmatic
     // launch): then nothing is read before it completes.
@@ -102,17 +163,17 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_score_kernel(const __grid
 
     // ---- setup -------------------------------------------------------------
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S::kStages; ++s) {
             mbar_init(&bar->k_full[s], 1);
             mbar_init(&bar->k_empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < S::kQBufs; ++b) {
             mbar_init(&bar->q_full[b], 1);
             mbar_init(&bar->q_empty[b], 1);
         }
-        for (int a = 0; a < kAccBufs; ++a) {
+        for (int a = 0; a < 2; ++a) {
             mbar_init(&bar->acc_full[a], 1);
-            mbar_init(&bar->acc_empty[a], 4);
+            mbar_init(&bar->acc_empty[a], S::kEpiWarps);
         }
         bar->abort_flag = 0;
         fence_barrier_init();
@@ -122,14 +183,15 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_score_kernel(const __grid
         tma_prefetch_map(&p.qmap);
     }
     if (warp == 1) {
-        tmem_alloc(&bar->tmem_base, kTmemCols);
+        tmem_alloc(&bar->tmem_base, S::kTmemCols);
         tmem_relinquish();
     }
-    for (int i = threadIdx.x; i < (int)p.rows * kIdxHeads; i += kThreads) {
-        const int e = i / kIdxHeads, h = i % kIdxHeads;
-        w_s[i] = p.w[(size_t)p.q_row[e] * kIdxHeads + h];
-    }
-    for (int i = threadIdx.x; i < kHistBins; i += kThreads) hist_s[i] = 0;
+    if (G == 1)
+        for (int i = threadIdx.x; i < (int)p.vrows * kIdxHeads; i += S::kThreads) {
+            const int v = i / kIdxHeads, h = i % kIdxHeads;
+            w_s[i] = p.w[(size_t)p.q_row[v] * kIdxHeads + h];
+        }
+    for (int i = threadIdx.x; i < S::kHistWords; i += S::kThreads) hist_s[i] = 0;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -139,30 +201,36 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_score_kernel(const __grid
     if (warp == 0) {
         // ---- TMA producer ----------------------------------------------------
         if (lane == 0) {
+            // A key tile is read once per segment; with several segments per
+            // entry (more than G queries) it is read again and may come from L2.
             const uint64_t policy = l2_policy_evict_first();
             const uint64_t q_policy = l2_policy_evict_last();
             int cur = -1;
             uint32_t q_uses = 0, it = 0;
-            uint32_t last_parity[kStages];
-            bool used[kStages];
-            for (int s = 0; s < kStages; ++s) used[s] = false;
+            uint32_t last_parity[S::kStages];
+            bool used[S::kStages];
+            for (int s = 0; s < S::kStages; ++s) used[s] = false;
             bool ok = true;
             for (uint32_t g = g_begin; g < g_end && ok; ++g, ++it) {
-                const int e = entry_of_tile(p, g);
-                const uint32_t tile = g - p.tile_begin[e];
-                if (e != cur) {
-                    cur = e;
-                    const uint32_t qb = q_uses & 1;
-                    if (!mbar_wait(&bar->q_empty[qb], ((q_uses >> 1) & 1) ^ 1, p.status)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&bar->q_full[qb], kQBytes);
-                    uint8_t* dst = q_s + (size_t)qb * kQBytes;
-                    const int y = (int)(p.q_row[e] * kIdxHeads);
-                    tma_load_2d(dst, &p.qmap, &bar->q_full[qb], 0, y, q_policy);
-                    tma_load_2d(dst + kQHalfBytes, &p.qmap, &bar->q_full[qb], 64, y, q_policy);
+                const int sg = segment_of_tile(p, g);
+                const int e = G == 1 ? sg : p.seg_entry[sg];  // one segment per entry with one query
+                const uint32_t tile = g - p.tile_begin[sg];
+                if (sg != cur) {
+                    cur = sg;
+                    const uint32_t qb = q_uses % S::kQBufs, use = q_uses / S::kQBufs;
+                    if (!mbar_wait(&bar->q_empty[qb], (use & 1) ^ 1, p.status)) { ok = false; break; }
+                    const int nq = p.seg_queries[sg];
+                    mbar_arrive_expect_tx(&bar->q_full[qb], (uint32_t)nq * 2 * kQBoxBytes);
+                    uint8_t* dst = q_s + (size_t)qb * S::kQBytes;
+                    for (int i = 0; i < nq; ++i) {
+                        const int y = (int)(p.q_row[p.seg_vrow[sg] + i] * kIdxHeads);
+                        tma_load_2d(dst + i * kQBoxBytes, &p.qmap, &bar->q_full[qb], 0, y, q_policy);
+                        tma_load_2d(dst + S::kQHalfBytes + i * kQBoxBytes, &p.qmap, &bar->q_full[qb], 64, y, q_policy);
+                    }
                     ++q_uses;
                 }
-                const uint32_t s = it % kStages;
-                const uint32_t ph = (it / kStages) & 1;
+                const uint32_t s = it % S::kStages;
+                const uint32_t ph = (it / S::kStages) & 1;
                 if (!mbar_wait(&bar->k_empty[s], ph ^ 1, p.status)) { ok = false; break; }
                 mbar_arrive_expect_tx(&bar->k_full[s], kTileBytes);
                 uint8_t* dst = keys_s + (size_t)s * kTileBytes;
@@ -174,40 +242,41 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_score_kernel(const __grid
             }
             if (!ok) atomicExch(&bar->abort_flag, 1u);
             // Drain: every load this thread issued has landed before the CTA exits.
-            for (int s = 0; s < kStages; ++s)
+            for (int s = 0; s < S::kStages; ++s)
                 if (used[s]) (void)mbar_wait(&bar->k_full[s], last_parity[s], p.status);
         }
     } else if (warp == 1) {
         // ---- MMA issuer --------------------------------------------------------
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(128, 64);
             int cur = -1;
-            uint32_t q_uses = 0, qb = 0, it = 0;
+            uint32_t q_uses = 0, qb = 0, it = 0, idesc = 0;
             for (uint32_t g = g_begin; g < g_end; ++g, ++it) {
                 if (*(volatile uint32_t*)&bar->abort_flag) break;
-                const int e = entry_of_tile(p, g);
-                if (e != cur) {
+                const int sg = segment_of_tile(p, g);
+                if (sg != cur) {
                     if (cur >= 0) umma_commit(&bar->q_empty[qb]);
-                    qb = q_uses & 1;
-                    if (!mbar_wait(&bar->q_full[qb], (q_uses >> 1) & 1, p.status)) break;
+                    qb = q_uses % S::kQBufs;
+                    if (!mbar_wait(&bar->q_full[qb], (q_uses / S::kQBufs) & 1, p.status)) break;
                     ++q_uses;
-                    cur = e;
+                    cur = sg;
+                    // D[128 keys x 64 nq] = K_tile . [q_0; ...; q_{nq-1}]^T
+                    idesc = idesc_bf16_f32(128, 64 * (G == 1 ? 1 : (int)p.seg_queries[sg]));
                 }
-                const uint32_t s = it % kStages;
-                const uint32_t ph = (it / kStages) & 1;
-                const uint32_t a = it % kAccBufs;
-                const uint32_t aph = (it / kAccBufs) & 1;
+                const uint32_t s = it % S::kStages;
+                const uint32_t ph = (it / S::kStages) & 1;
+                const uint32_t a = it & 1;
+                const uint32_t aph = (it >> 1) & 1;
                 if (!mbar_wait(&bar->k_full[s], ph, p.status)) break;
                 if (!mbar_wait(&bar->acc_empty[a], aph ^ 1, p.status)) break;
                 tc_fence_after();
                 const uint32_t a_base = smem_u32(keys_s + (size_t)s * kTileBytes);
-                const uint32_t b_base = smem_u32(q_s + (size_t)qb * kQBytes);
-                const uint32_t d_tmem = tmem_base + a * kAccCols;
+                const uint32_t b_base = smem_u32(q_s + (size_t)qb * S::kQBytes);
+                const uint32_t d_tmem = tmem_base + a * S::kAccCols;
 #pragma unroll
                 for (int kk = 0; kk < kIdxDim / 16; ++kk) {
                     const uint32_t koff = (uint32_t)(kk & 3) * 32;  // 16 bf16 = 32 B inside the 128-B row
                     const uint64_t adesc = smem_desc_sw128_kmajor(a_base + (kk >> 2) * kHalfBytes + koff);
-                    const uint64_t bdesc = smem_desc_sw128_kmajor(b_base + (kk >> 2) * kQHalfBytes + koff);
+                    const uint64_t bdesc = smem_desc_sw128_kmajor(b_base + (kk >> 2) * S::kQHalfBytes + koff);
                     umma_bf16(d_tmem, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&bar->k_empty[s]);
@@ -216,9 +285,12 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_score_kernel(const __grid
         }
         __syncwarp();
     } else {
-        // ---- epilogue: one key per thread --------------------------------------
-        const int quarter = warp & 3;          // TMEM lanes [32*quarter, 32*quarter+32)
-        const int ep_tid = threadIdx.x - 64;   // 0..127
+        // ---- epilogue: one key per thread, kQPerWarp queries ---------------------
+        constexpr int kEpiThreads = 32 * S::kEpiWarps;
+        const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter+32)
+        const int ep_tid = threadIdx.x - 64;
+        constexpr int kGroups = S::kEpiWarps / 4;  // warps per TMEM lane quarter: they split the queries
+        const int sub = G == 1 ? 0 : (warp - 2) >> 2;
         const bool want_hist = p.hist != nullptr;
         // The histogram may still be being cleared by the previous kernel (PDL):
         // the producer and MMA warps start streaming, the epilogue waits here.
@@ -226,57 +298,106 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_score_kernel(const __grid
         // The scores are read back by the next kernel: keep them in L2 while the
         // key stream (evict-first) passes through.
         const uint64_t keep = l2_policy_evict_last();
-        int cur = -1;
-        uint32_t it = 0;
-        for (uint32_t g = g_begin; g < g_end; ++g, ++it) {
-            const int e = entry_of_tile(p, g);
-            const uint32_t tile = g - p.tile_begin[e];
-            if (want_hist && e != cur && cur >= 0) {
-                named_bar(1, 128);
-                for (int b = ep_tid; b < kHistBins; b += 128) {
-                    const uint32_t v = hist_s[b];
-                    if (v) {
-                        atomicAdd(&p.hist[(size_t)cur * kHistBins + b], v);
-                        hist_s[b] = 0;
+        // Add this CTA's counts of segment `sg` to the row histograms and zero them.
+        auto flush = [&](int sg) {
+            const int nq = G == 1 ? 1 : (int)p.seg_queries[sg];
+            for (int i = 0; i < nq; ++i) {
+                uint32_t* dst = p.hist + (size_t)(p.seg_vrow[sg] + i) * kHistBins;
+                if (G == 1) {
+                    for (int b = ep_tid; b < kHistBins; b += kEpiThreads) {
+                        const uint32_t v = hist_s[b];
+                        if (v) {
+                            atomicAdd(dst + b, v);
+                            hist_s[b] = 0;
+                        }
+                    }
+                } else {
+                    uint32_t* h = hist_s + i * (kHistBins / 2);
+                    for (int b = ep_tid; b < kHistBins / 2; b += kEpiThreads) {
+                        const uint32_t v = h[b];
+                        if (v) {
+                            if (v & 0xFFFFu) atomicAdd(dst + 2 * b, v & 0xFFFFu);
+                            if (v >> 16) atomicAdd(dst + 2 * b + 1, v >> 16);
+                            h[b] = 0;
+                        }
                     }
                 }
-                named_bar(1, 128);
             }
-            cur = e;
-            const uint32_t a = it % kAccBufs;
-            const uint32_t aph = (it / kAccBufs) & 1;
+        };
+        int cur = -1;
+        uint32_t it = 0, since_flush = 0;
+        // One query: the row's head weights stay in registers.
+        float wr[G == 1 ? kIdxHeads : 4];
+        for (uint32_t g = g_begin; g < g_end; ++g, ++it) {
+            const int sg = segment_of_tile(p, g);
+            const uint32_t tile = g - p.tile_begin[sg];
+            if (G == 1) {
+                if (want_hist && sg != cur && cur >= 0) {
+                    named_bar(1, kEpiThreads);
+                    flush(cur);
+                    named_bar(1, kEpiThreads);
+                }
+                if (sg != cur)
+#pragma unroll
+                    for (int h = 0; h < kIdxHeads; h += 4)
+                        *reinterpret_cast<float4*>(&wr[h]) = *reinterpret_cast<const float4*>(w_s + sg * kIdxHeads + h);
+            } else if (sg != cur || (want_hist && since_flush == S::kFlushTiles)) {
+                named_bar(1, kEpiThreads);  // every thread is done with the weights and counts
+                if (want_hist && cur >= 0) flush(cur);
+                if (sg != cur) {
+                    const int nq = p.seg_queries[sg];
+                    for (int i = ep_tid; i < nq * kIdxHeads; i += kEpiThreads)
+                        w_s[i] = p.w[(size_t)p.q_row[p.seg_vrow[sg] + i / kIdxHeads] * kIdxHeads + i % kIdxHeads];
+                }
+                named_bar(1, kEpiThreads);
+                since_flush = 0;
+            }
+            cur = sg;
+            ++since_flush;
+            const int nq = G == 1 ? 1 : (int)p.seg_queries[sg];
+            // This warp's queries of the segment: [q0, q0 + nk).
+            const int per = (nq + kGroups - 1) / kGroups;
+            const int q0 = sub * per;
+            const int nk = nq - q0 < 0 ? 0 : (nq - q0 < per ? nq - q0 : per);
+            const uint32_t a = it & 1;
+            const uint32_t aph = (it >> 1) & 1;
             if (!mbar_wait(&bar->acc_full[a], aph, p.status)) break;
             tc_fence_after();
-            uint32_t v[64];
-            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + a * kAccCols;
-            tmem_ld_x16(taddr + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-            tmem_ld_x16(taddr + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-            tmem_ld_x16(taddr + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
-            tmem_ld_x16(taddr + 48, *reinterpret_cast<uint32_t(*)[16]>(&v[48]));
+            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + a * S::kAccCols;
+            const uint32_t j = tile * kTileKeys + quarter * 32 + lane;
+            uint32_t v[S::kQPerWarp][64];
+#pragma unroll
+            for (int k = 0; k < S::kQPerWarp; ++k)
+                if (k < nk) {
+                    const uint32_t c = taddr + 64 * (q0 + k);
+                    tmem_ld_x16(c + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[k][0]));
+                    tmem_ld_x16(c + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[k][16]));
+                    tmem_ld_x16(c + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[k][32]));
+                    tmem_ld_x16(c + 48, *reinterpret_cast<uint32_t(*)[16]>(&v[k][48]));
+                }
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar->acc_empty[a]);
-
-            const float* w = w_s + e * kIdxHeads;
-            // Four independent chains: a quarter of the dependent FMA latency.
-            float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-            for (int h = 0; h < kIdxHeads; ++h) s4[h & 3] = fmaf(relu_nan(__uint_as_float(v[h])), w[h], s4[h & 3]);
-            const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-            const uint32_t j = tile * kTileKeys + quarter * 32 + lane;
-            if (j < p.kv_len[e]) {
-                const bool fin = finite_f(s);
-                st_global_hint(p.scores + (size_t)e * p.score_stride + j, fin ? s : -INFINITY, keep);
-                if (want_hist && fin) atomicAdd(&hist_s[score_key(s) >> 21], 1u);
+            for (int k = 0; k < S::kQPerWarp; ++k) {
+                if (k >= nk) break;
+                const int vr = G == 1 ? sg : p.seg_vrow[sg] + q0 + k;
+                const float sc = head_sum(v[k], G == 1 ? wr : nullptr, w_s + (q0 + k) * kIdxHeads);
+                if (j < p.valid[vr]) {
+                    const bool fin = finite_f(sc);
+                    st_global_hint(p.scores + (size_t)vr * p.score_stride + j, fin ? sc : -INFINITY, keep);
+                    if (want_hist && fin) {
+                        const uint32_t bin = score_key(sc) >> 21;
+                        if (G == 1) atomicAdd(&hist_s[bin], 1u);
+                        else atomicAdd(&hist_s[(q0 + k) * (kHistBins / 2) + (bin >> 1)], (bin & 1) ? 0x10000u : 1u);
+                    }
+                }
             }
         }
         if (want_hist && cur >= 0) {
-            named_bar(1, 128);
-            for (int b = ep_tid; b < kHistBins; b += 128) {
-                const uint32_t v = hist_s[b];
-                if (v) atomicAdd(&p.hist[(size_t)cur * kHistBins + b], v);
-            }
+            named_bar(1, kEpiThreads);
+            flush(cur);
         }
     }
 
@@ -284,23 +405,44 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_score_kernel(const __grid
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        tmem_dealloc(tmem_base, S::kTmemCols);
     }
 }
 
-size_t indexer_smem_bytes() { return kSmemBytes; }
+// One query per entry (decode) and up to kIndexerGroup queries per segment.
+__global__ void __launch_bounds__(Shape<1>::kThreads, 1) indexer_score_kernel(const __grid_constant__ IndexerParams1 p) {
+    indexer_score_body<1>(p);
+}
 
-cudaError_t launch_indexer(const IndexerParams& p, int num_sms, cudaStream_t stream, bool pdl) {
+__global__ void __launch_bounds__(Shape<kIndexerGroup>::kThreads, 1)
+    indexer_score_group_kernel(const __grid_constant__ IndexerParamsG p) {
+    indexer_score_body<kIndexerGroup>(p);
+}
+
+template <int G, class K>
+static cudaError_t launch_group(K kernel, const ParamsOf<G>& p, int num_sms, cudaStream_t stream, bool pdl) {
     static bool configured = false;
+    constexpr size_t bytes = smem_bytes<G>();
     if (!configured) {
-        cudaError_t err = cudaFuncSetAttribute(indexer_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)kSmemBytes);
+        cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
         if (err != cudaSuccess) return err;
         configured = true;
     }
-    if (p.total_tiles == 0) return cudaSuccess;
     const uint32_t grid = p.total_tiles < (uint32_t)num_sms ? p.total_tiles : (uint32_t)num_sms;
-    return launch_kernel(indexer_score_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, pdl, p);
+    return launch_kernel(kernel, dim3(grid), dim3(Shape<G>::kThreads), bytes, stream, pdl, p);
+}
+
+static_assert(std::is_same<ParamsOf<1>, IndexerParams1>::value, "one-query table");
+static_assert(std::is_same<ParamsOf<kIndexerGroup>, IndexerParamsG>::value, "grouped table");
+
+cudaError_t launch_indexer(const IndexerParams1& p, int num_sms, cudaStream_t stream, bool pdl) {
+    if (p.total_tiles == 0) return cudaSuccess;
+    return launch_group<1>(indexer_score_kernel, p, num_sms, stream, pdl);
+}
+
+cudaError_t launch_indexer(const IndexerParamsG& p, int num_sms, cudaStream_t stream, bool pdl) {
+    if (p.total_tiles == 0) return cudaSuccess;
+    return launch_group<kIndexerGroup>(indexer_score_group_kernel, p, num_sms, stream, pdl);
 }
 
 uint32_t indexer_tile_keys() { return kTileKeys; }

@@ -10,23 +10,39 @@
 
 namespace dsrows {
 
-// Indexer score: one TMA tensor map per row's key cache, one for the queries.
-struct IndexerParams {
+// Indexer score. A virtual row is one (entry, query) pair with its own query
+// row and number of scored keys; a segment is one entry with a run of up to
+// kIndexerGroup consecutive virtual rows that share each key tile.
+constexpr int kSegMax = 32;
+constexpr int kVRowsMax = DS_INDEX_VROWS_MAX;
+constexpr int kIndexerGroup = 4;  // queries per key tile in the multi-query kernel
+
+// Arrays sized for the kernel that takes them: SEGS segments, VROWS virtual
+// rows (the one-query kernel takes the smaller table: a shorter launch).
+template <int SEGS, int VROWS>
+struct IndexerParamsT {
     CUtensorMap kmap[DS_ROWS_MAX];  // bf16 [kv_len, 128], box {64, 128}, 128-B swizzle
     CUtensorMap qmap;               // bf16 [Q*64, 128], box {64, 64}, 128-B swizzle
     const float* w;                 // [Q, 64]
-    float* scores;                  // entry e at e * score_stride
-    uint32_t* hist;                 // optional [8][2048] score-key histogram
+    float* scores;                  // virtual row v at v * score_stride
+    uint32_t* hist;                 // optional [vrows][2048] score-key histogram
     uint32_t* status;               // device status word
     uint32_t inputs_ready;          // 1: every input was complete when the launch began (it follows an
                                     // ordinary launch), so loads may start before griddepcontrol.wait
     uint64_t score_stride;
-    uint32_t rows;
+    uint32_t rows;                  // entries (key caches)
+    uint32_t segs;
+    uint32_t vrows;
     uint32_t total_tiles;
-    uint32_t kv_len[DS_ROWS_MAX];
-    uint32_t q_row[DS_ROWS_MAX];
-    uint32_t tile_begin[DS_ROWS_MAX];
+    uint32_t tile_begin[SEGS];      // first 128-key tile of each segment
+    uint8_t seg_entry[SEGS];
+    uint8_t seg_vrow[SEGS];         // the segment's first virtual row
+    uint8_t seg_queries[SEGS];      // its virtual rows: 1..group
+    uint32_t valid[VROWS];          // keys j < valid[v] are scored
+    uint32_t q_row[VROWS];          // query and head-weight row of each virtual row
 };
+using IndexerParams1 = IndexerParamsT<DS_ROWS_MAX, DS_ROWS_MAX>;  // one query per entry
+using IndexerParamsG = IndexerParamsT<kSegMax, kVRowsMax>;        // up to kIndexerGroup per segment
 
 // Top-k: level-0 histogram, then one 8-CTA cluster per row for the selection.
 struct TopkParams {
@@ -38,11 +54,11 @@ struct TopkParams {
     uint32_t rows;
     uint32_t order_by_index;  // 0: best first; 1: ascending index (the decode's canonical order)
     uint32_t total_chunks;    // histogram CTAs (chunks of topk_chunk() scores)
-    uint32_t kv_len[DS_ROWS_MAX];
-    uint32_t width[DS_ROWS_MAX];
-    uint32_t out_offset[DS_ROWS_MAX];
-    uint32_t chunk_begin[DS_ROWS_MAX];
-    int32_t offset[DS_ROWS_MAX];   // added to every emitted index (positioned indexer)
+    uint32_t kv_len[kVRowsMax];
+    uint32_t width[kVRowsMax];
+    uint32_t out_offset[kVRowsMax];
+    uint32_t chunk_begin[kVRowsMax];
+    int32_t offset[kVRowsMax];   // added to every emitted index (positioned indexer)
 };
 
 // Selection (decode) and attention, one 8-CTA cluster per row; with `given`,
@@ -91,9 +107,10 @@ struct CompressorParams {
 
 cudaError_t launch_compressor(const CompressorParams& p, cudaStream_t stream, bool pdl);
 
-size_t indexer_smem_bytes();
 uint32_t indexer_tile_keys();
-cudaError_t launch_indexer(const IndexerParams& p, int num_sms, cudaStream_t stream, bool pdl);
+// One query per key tile (decode), or up to kIndexerGroup.
+cudaError_t launch_indexer(const IndexerParams1& p, int num_sms, cudaStream_t stream, bool pdl);
+cudaError_t launch_indexer(const IndexerParamsG& p, int num_sms, cudaStream_t stream, bool pdl);
 
 uint32_t topk_chunk();  // scores per histogram / collection CTA
 cudaError_t launch_topk_hist(const TopkParams& p, cudaStream_t stream, bool pdl);

@@ -40,9 +40,8 @@ constexpr size_t kSelectSmemBytes = sizeof(SelectSmem) + kTopK * sizeof(uint64_t
 
 __device__ __forceinline__ int entry_of_chunk(const TopkParams& p, uint32_t c) {
     int e = 0;
-#pragma unroll
-    for (int i = 1; i < kRowsMax; ++i)
-        if (i < (int)p.rows && c >= p.chunk_begin[i]) e = i;
+    for (int i = 1; i < (int)p.rows; ++i)
+        if (c >= p.chunk_begin[i]) e = i;
     return e;
 }
 

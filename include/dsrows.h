@@ -43,6 +43,7 @@ extern "C" {
 #define DS_ROWS_MAX 8     /* rows per call (binding slots per cache family) */
 #define DS_INDEX_HEADS 64 /* indexer query heads */
 #define DS_INDEX_DIM 128  /* indexer key / query width */
+#define DS_INDEX_VROWS_MAX 64 /* rows x queries of one multi-query indexer call */
 #define DS_TOPK 512       /* most selected KV rows per row */
 #define DS_HEADS 64       /* attention heads */
 #define DS_DIM 512        /* shared-KV row width (K and V) */
@@ -230,6 +231,35 @@ size_t ds_rows_indexer_topk_workspace_bytes(int rows, const ds_indexer_row_t* ta
 int ds_rows_indexer_topk(int rows, const ds_indexer_row_t* table, const ds_bf16* const* index_keys,
                          const ds_bf16* q_index, const float* w_index, int32_t* indices,
                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes for ds_rows_indexer_topk_queries; 0 when the arguments are
+ * invalid. ds_rows_indexer_topk_workspace_bytes(r, t) equals this with
+ * query_len 1. */
+size_t ds_rows_indexer_topk_queries_workspace_bytes(int rows, const ds_indexer_row_t* table, uint32_t query_len);
+
+/*
+ * (1)+(2) with query_len consecutive queries per entry (the query loop of
+ * `deepseek_indexer_score_mma_rows_bf16`, whose query j sits at position
+ * start_pos + j; its valid_count = min(kv_len, (start_pos + j + 1) / 4)). For
+ * each entry e and query j < query_len, exactly ds_rows_indexer_topk of the
+ * entry with start_pos + j, q_row + j and output_offset + 512 j. (The pages'
+ * top-k kernels take the first query only; each query's own list is the
+ * reading taken here.)
+ *   query_len   1 .. 64 with rows * query_len <= DS_INDEX_VROWS_MAX.
+ *   table       as for ds_rows_indexer_topk, except: kv_len must be at least
+ *               the last query's count (start_pos + query_len) / 4,
+ *               start_pos + query_len must fit u32, offset + that count - 1
+ *               must fit int32, q_row .. q_row + query_len - 1 are the
+ *               entry's query rows, and the output ranges are
+ *               [output_offset, output_offset + 512 query_len).
+ *   indices     int32, 512 per (entry, query) at output_offset + 512 j.
+ *   workspace   at least ds_rows_indexer_topk_queries_workspace_bytes(...) bytes.
+ * Up to four queries of an entry share each key tile on the tensor cores, so
+ * the keys are read once for them. Errors as ds_rows_indexer_topk.
+ */
+int ds_rows_indexer_topk_queries(int rows, const ds_indexer_row_t* table, uint32_t query_len,
+                                 const ds_bf16* const* index_keys, const ds_bf16* q_index, const float* w_index,
+                                 int32_t* indices, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * One row of a KV compressor call (`DeepSeekCompressorRow`): the row's

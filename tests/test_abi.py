@@ -216,6 +216,35 @@ def test_indexer_rows_pointers_and_workspace(lib):
     assert _indexer_topk(lib, rows, ws=FAKE + 16) == -3
 
 
+def _queries(lib, rows, query_len, ws_bytes=1 << 30, ws=FAKE):
+    tab, n = ds._indexer_table(rows)
+    ptrs = (ctypes.c_void_p * max(1, n))(*[FAKE + 4096 * i for i in range(n)])
+    return lib.ds_rows_indexer_topk_queries(n, tab, query_len, ptrs, FAKE, FAKE, FAKE, ws, ws_bytes, None)
+
+
+def test_indexer_queries_checks(lib):
+    # The last query's count decides: start_pos 35, 4 queries -> (35 + 4) / 4 = 9.
+    assert _queries(lib, [(8, 35, 0, 0, 0)], 4) == -1 and "shorter than 9 causal" in _err(lib)
+    tab, n = ds._indexer_table([(9, 35, 0, 0, 0)])
+    assert lib.ds_rows_indexer_topk_queries_workspace_bytes(n, tab, 4) > 0, _err(lib)
+    # Output ranges span 512 x query_len.
+    assert _queries(lib, [(600, 2399, 0, 0, 0), (600, 2399, 0, 1, 1024)], 3) == -1 and "overlap" in _err(lib)
+    tab, n = ds._indexer_table([(600, 2399, 0, 0, 0), (600, 2399, 0, 3, 1536)])
+    assert lib.ds_rows_indexer_topk_queries_workspace_bytes(n, tab, 3) > 0, _err(lib)
+    # rows x query_len is bounded; query_len 0 is rejected.
+    assert _queries(lib, [(600, 2399, 0, 0, 0)] * 2, 33) == -1 and "rows x query_len" in _err(lib)
+    assert _queries(lib, [(600, 2399, 0, 0, 0)], 0) == -1 and "rows x query_len" in _err(lib)
+    assert _queries(lib, [(600, 0xFFFFFFFF - 2, 0, 0, 0)], 4) == -1 and "position overflows" in _err(lib)
+    # One query is the positioned indexer: the same workspace.
+    rows = [(700, 2399, 0, 0, 0), (70000, 9999, 5, 8, 4096)]
+    tab, n = ds._indexer_table(rows)
+    assert lib.ds_rows_indexer_topk_queries_workspace_bytes(n, tab, 1) == lib.ds_rows_indexer_topk_workspace_bytes(n, tab)
+    assert (lib.ds_rows_indexer_topk_queries_workspace_bytes(n, tab, 8)
+            > lib.ds_rows_indexer_topk_workspace_bytes(n, tab))
+    need = ds.ds_rows_indexer_topk_queries_workspace_bytes([(600, 2399, 0, 0, 0)], 4)
+    assert _queries(lib, [(600, 2399, 0, 0, 0)], 4, ws_bytes=need - 1) == -2 and "workspace holds" in _err(lib)
+
+
 # ---------------------------------------------------------------------------
 # KV compressor rows (dispatch_deepseek_compressor_rows checks)
 # ---------------------------------------------------------------------------

@@ -235,6 +235,20 @@ def draw_queries(wl: Workload, seed: int):
     return qI, wI, qA
 
 
+def draw_index_queries(wl: Workload, seed: int, count: int):
+    """`count` indexer queries for the same caches (several consecutive queries
+    per row), drawn with the workload's recipe: (q_index uint16 [count,64,128],
+    w_index float32 [count,64])."""
+    rng = np.random.default_rng(seed)
+    if wl.integer_valued:
+        qI = _int_bf16(rng, (count, HEADS, INDEX_DIM))
+        wI = rng.integers(-3, 3, endpoint=True, size=(count, HEADS)).astype(np.float32)
+    else:
+        qI = _normal_bf16(rng, (count, HEADS, INDEX_DIM))
+        wI = rng.standard_normal(size=(count, HEADS), dtype=np.float32) / np.float32(8.0)
+    return qI, wI
+
+
 # ---------------------------------------------------------------------------
 # Stand-alone stage inputs (scores for the top-k stage, indices for attention)
 # ---------------------------------------------------------------------------
