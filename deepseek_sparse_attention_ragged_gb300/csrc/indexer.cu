@@ -219,7 +219,7 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
                     cur = sg;
                     const uint32_t qb = q_uses % S::kQBufs, use = q_uses / S::kQBufs;
                     if (!mbar_wait(&bar->q_empty[qb], (use & 1) ^ 1, p.status)) { ok = false; break; }
-                    const int nq = p.seg_queries[sg];
+                    const int nq = G == 1 ? 1 : p.seg_queries[sg];
                     mbar_arrive_expect_tx(&bar->q_full[qb], (uint32_t)nq * 2 * kQBoxBytes);
                     uint8_t* dst = q_s + (size_t)qb * S::kQBytes;
                     for (int i = 0; i < nq; ++i) {
@@ -260,7 +260,7 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
                     ++q_uses;
                     cur = sg;
                     // D[128 keys x 64 nq] = K_tile . [q_0; ...; q_{nq-1}]^T
-                    idesc = idesc_bf16_f32(128, 64 * (G == 1 ? 1 : (int)p.seg_queries[sg]));
+                    if (G != 1) idesc = idesc_bf16_f32(128, 64 * (int)p.seg_queries[sg]);
                 }
                 const uint32_t s = it % S::kStages;
                 const uint32_t ph = (it / S::kStages) & 1;
@@ -277,7 +277,7 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
                     const uint32_t koff = (uint32_t)(kk & 3) * 32;  // 16 bf16 = 32 B inside the 128-B row
                     const uint64_t adesc = smem_desc_sw128_kmajor(a_base + (kk >> 2) * kHalfBytes + koff);
                     const uint64_t bdesc = smem_desc_sw128_kmajor(b_base + (kk >> 2) * S::kQHalfBytes + koff);
-                    umma_bf16(d_tmem, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+                    umma_bf16(d_tmem, adesc, bdesc, G == 1 ? idesc_bf16_f32(128, 64) : idesc, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&bar->k_empty[s]);
                 umma_commit(&bar->acc_full[a]);
