@@ -258,6 +258,48 @@ def compressor_timings(ds, device, stream, calls=50):
     return res
 
 
+def indexer_queries_timings(ds, workloads, wl, dev, device, stream, counts=(2, 4, 8), calls=10):
+    """ds_rows_indexer_topk_queries on the same caches with Q consecutive queries
+    per row (every key valid for the last query): microseconds per call, the
+    algorithmic bytes (each key once, plus Q query rows, weights and 512 indices
+    per row) and the indexer's tensor flops (2 x 64 x 128 per key and query)."""
+    import torch
+    from workloads.device import bf16_tensor
+    R = len(wl.rows)
+    keys_total = sum(r.kv_len for r in wl.rows)
+    res = {}
+    for Q in counts:
+        qI, wI = workloads.draw_index_queries(wl, 900 + Q, R * Q)
+        q = bf16_tensor(qI, device)
+        w = torch.from_numpy(wI).to(device)
+        rows = [ds.IndexerRow(r.kv_len, 4 * r.kv_len - Q, 0, e * Q, 512 * Q * e) for e, r in enumerate(wl.rows)]
+        out = torch.empty((512 * Q * R,), dtype=torch.int32, device=device)
+        ws = ds.indexer_topk_workspace(rows, device, Q)
+        call = lambda: ds.ds_rows_indexer_topk_queries(rows, Q, q, w, dev.keys, out, workspace_t=ws, stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                call()
+        torch.cuda.synchronize(device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(calls):
+                call()
+        with torch.cuda.stream(stream):
+            graph.replay()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+        torch.cuda.synchronize(device)
+        us = a.elapsed_time(b) / calls * 1e3
+        nbytes = 256 * keys_total + R * Q * (16384 + 256 + 2048)
+        flops = 2 * 64 * 128 * Q * keys_total
+        res[str(Q)] = {"us_per_call": us, "us_per_query_row": us / Q, "bytes_per_call": nbytes,
+                       "gbs": nbytes / (us / 1e6) / 1e9, "tflops": flops / (us / 1e6) / 1e12}
+    return res
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -456,9 +498,11 @@ def main():
 
     per_config = None
     compressor = None
+    queries = None
     if rank == 0 and world == 1 and not args.no_per_config:
         per_config = other_configs(ds, workloads, to_device, device, stream, flush_l2, skip=args.config)
         compressor = compressor_timings(ds, device, stream)
+        queries = indexer_queries_timings(ds, workloads, wl, dev, device, stream)
 
     if rank == 0:
         cb = None
@@ -488,6 +532,7 @@ def main():
                              "frac": pidx_bytes / (pidx_ms / 1e3) / 1e9 / peak},
             "per_config": per_config,
             "compressor": compressor,
+            "indexer_queries": queries,
             "clocks": clocks.summary(),
             "cpu_baseline": cb,
         }
