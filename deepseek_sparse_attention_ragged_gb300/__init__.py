@@ -24,6 +24,7 @@ __all__ = [
     "DsRowsError", "Row", "load", "build", "library_path",
     "ds_rows_workspace_bytes", "workspace", "ds_rows_indexer_score", "ds_rows_topk", "ds_rows_topk_static",
     "ds_rows_sparse_attn", "ds_rows_decode", "ds_rows_version",
+    "ds_rows_decode_host_workspace_bytes", "host_workspace", "ds_rows_decode_host",
     "IndexerRow", "ds_rows_indexer_topk_workspace_bytes", "indexer_topk_workspace", "ds_rows_indexer_topk",
     "ds_rows_indexer_topk_queries_workspace_bytes", "ds_rows_indexer_topk_queries",
     "CompressorRow", "ds_rows_compress_kv",
@@ -109,6 +110,10 @@ def load():
     lib.ds_rows_sparse_attn.restype = i32
     lib.ds_rows_decode.argtypes = [rs, vp, vp, vp, vp, sz, ctypes.c_float, vp, vp, u32p, vp, sz, vp]
     lib.ds_rows_decode.restype = i32
+    lib.ds_rows_decode_host_workspace_bytes.argtypes = [i32, ctypes.POINTER(Row), sz]
+    lib.ds_rows_decode_host_workspace_bytes.restype = sz
+    lib.ds_rows_decode_host.argtypes = [rs, vp, vp, vp, vp, sz, ctypes.c_float, vp, vp, u32p, vp, sz, vp]
+    lib.ds_rows_decode_host.restype = i32
     lib.ds_rows_indexer_topk_workspace_bytes.argtypes = [i32, ctypes.POINTER(IndexerRow)]
     lib.ds_rows_indexer_topk_workspace_bytes.restype = sz
     lib.ds_rows_indexer_topk.argtypes = [i32, ctypes.POINTER(IndexerRow), ctypes.POINTER(vp), vp, vp, vp, vp, sz, vp]
@@ -320,6 +325,67 @@ def ds_rows_decode(rows, q_index, w_index, index_keys, q_attn, kv, sinks, sinks_
     _check(lib, lib.ds_rows_decode(ctypes.byref(rs), _ptr(q_index), _ptr(w_index), _ptr(q_attn), _ptr(sinks),
                                    int(sinks_row_stride), float(scale), _ptr(out), _ptr(indices), _ptr(invalid),
                                    _ptr(workspace_t), workspace_t.numel(), _stream(stream)))
+
+
+def _require_host(t: Optional[torch.Tensor], name: str, dtype, numel: int, *, optional=False):
+    """`t` must be a contiguous CPU tensor of `dtype` holding >= numel elements
+    (pinned, for the library's copies to be asynchronous)."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, needs {numel}")
+
+
+def ds_rows_decode_host_workspace_bytes(rows, sinks_row_stride=0) -> int:
+    lib = load()
+    tab, n = _table(_rows_list(rows))
+    b = lib.ds_rows_decode_host_workspace_bytes(n, tab, int(sinks_row_stride))
+    if b == 0:
+        raise DsRowsError(-1, lib.ds_rows_last_error().decode() or "invalid row table")
+    return int(b)
+
+
+def host_workspace(rows, sinks_row_stride=0, device=None) -> torch.Tensor:
+    """A workspace tensor for ds_rows_decode_host (uint8, 256-byte aligned)."""
+    return torch.empty(ds_rows_decode_host_workspace_bytes(rows, sinks_row_stride), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def ds_rows_decode_host(rows, q_index, w_index, index_keys, q_attn, kv, sinks, sinks_row_stride, scale, out,
+                        indices=None, invalid=None, workspace_t=None, stream=None):
+    """ds_rows_decode with the step's inputs and outputs in host memory (pinned
+    CPU tensors); the caches stay on the device. Asynchronous on `stream`:
+    synchronise it before reading `out`."""
+    lib = load()
+    rl = _rows_list(rows)
+    q_rows = max(r[3] for r in rl) + 1
+    _require_host(q_index, "q_index", torch.bfloat16, q_rows * INDEX_HEADS * INDEX_DIM)
+    _require_host(w_index, "w_index", torch.float32, q_rows * INDEX_HEADS)
+    _require_host(q_attn, "q_attn", torch.bfloat16, q_rows * HEADS * DIM)
+    _require_host(sinks, "sinks", torch.float32, HEADS if sinks_row_stride == 0 else
+                  (q_rows - 1) * sinks_row_stride + HEADS)
+    _require_host(out, "out", torch.bfloat16, q_rows * HEADS * DIM)
+    _require_host(indices, "indices", torch.int32, max(r[2] + r[1] for r in rl), optional=True)
+    _require_host(invalid, "invalid", torch.int32, q_rows * HEADS, optional=True)
+    _check_caches(index_keys, rl, INDEX_DIM, "index_keys")
+    _check_caches(kv, rl, DIM, "kv")
+    if workspace_t is None:
+        workspace_t = host_workspace(rl, sinks_row_stride, kv[0].device)
+    tab, n = _table(rl)
+    rs, keep = _rowset(tab, n, keys=index_keys, kv=kv)
+    _check(lib, lib.ds_rows_decode_host(ctypes.byref(rs), _ptr(q_index), _ptr(w_index), _ptr(q_attn), _ptr(sinks),
+                                        int(sinks_row_stride), float(scale), _ptr(out), _ptr(indices),
+                                        _ptr(invalid), _ptr(workspace_t), workspace_t.numel(), _stream(stream)))
 
 
 # ---------------------------------------------------------------------------

@@ -230,13 +230,14 @@ int check_workspace(const ds_row_set_t* set, void* ws, size_t bytes, const Layou
 // scores only its keys j < valid[v] (the tensor map still spans the entry's
 // kv_len keys), else every key. One query per entry runs the one-query kernel;
 // more run the grouped kernel, up to kIndexerGroup queries per key tile.
-// `inputs_ready`: the launch follows an ordinary launch (the clear kernel), so
-// every input is complete and the key stream may start before the programmatic
-// wait.
+// `inputs_ready` (see IndexerParams): 1 when the launch follows an ordinary
+// launch (the clear kernel), so every input is complete and the key stream may
+// start before the programmatic wait; 2 when the previous kernel writes the
+// query and weights; 0 when it may write anything.
 template <class P>
 int fill_and_launch_indexer(P& p, int group, const ds_row_set_t* set, uint32_t query_len, const ds_bf16* q_index,
                             const float* w_index, float* scores, uint64_t stride, uint32_t* hist, uint32_t* status,
-                            cudaStream_t stream, bool inputs_ready, const uint32_t* valid) {
+                            cudaStream_t stream, uint32_t inputs_ready, const uint32_t* valid) {
     int rc = get_encoder();
     if (rc) return rc;
     std::memset(&p, 0, sizeof(p));
@@ -276,7 +277,7 @@ int fill_and_launch_indexer(P& p, int group, const ds_row_set_t* set, uint32_t q
     p.hist = hist;
     p.status = status;
     p.score_stride = stride;
-    p.inputs_ready = inputs_ready ? 1u : 0u;
+    p.inputs_ready = inputs_ready;
     p.rows = (uint32_t)set->rows;
     p.segs = segs;
     p.vrows = (uint32_t)set->rows * query_len;
@@ -289,7 +290,7 @@ int fill_and_launch_indexer(P& p, int group, const ds_row_set_t* set, uint32_t q
 
 int run_indexer(const ds_row_set_t* set, uint32_t query_len, const ds_bf16* q_index, const float* w_index,
                 float* scores, uint64_t stride, uint32_t* hist, uint32_t* status, cudaStream_t stream,
-                bool inputs_ready, const uint32_t* valid = nullptr) {
+                uint32_t inputs_ready, const uint32_t* valid = nullptr) {
     // The tables hold CUtensorMaps (~1.3-2.2 KB); built per call on the host.
     if (query_len == 1) {
         IndexerParams1 p;
@@ -430,6 +431,58 @@ int topk_scratch(uint8_t** out) {
     return DS_OK;
 }
 
+// ---- the host-buffer decode ----------------------------------------------------
+// Device staging of the step's inputs and outputs, after the decode workspace.
+struct Staging {
+    size_t q_index, w_index, q_attn, sinks, out, indices, invalid, total;
+    uint32_t nq;          // query rows: max q_row + 1
+    size_t sinks_floats;  // floats of sinks the entries read
+    uint64_t index_elems; // max index_offset + width
+};
+
+Staging make_staging(const ds_row_set_t* set, size_t base, size_t sinks_row_stride) {
+    Staging S{};
+    uint32_t nq = 0;
+    uint64_t ie = 0;
+    for (int e = 0; e < set->rows; ++e) {
+        const ds_row_t& r = set->table[e];
+        nq = r.q_row + 1 > nq ? r.q_row + 1 : nq;
+        const uint64_t end = (uint64_t)r.index_offset + r.width;
+        ie = end > ie ? end : ie;
+    }
+    S.nq = nq;
+    S.index_elems = ie;
+    S.sinks_floats = sinks_row_stride ? (size_t)(nq - 1) * sinks_row_stride + DS_HEADS : DS_HEADS;
+    S.q_index = align256(base);
+    S.w_index = align256(S.q_index + (size_t)nq * DS_INDEX_HEADS * DS_INDEX_DIM * 2);
+    S.q_attn = align256(S.w_index + (size_t)nq * DS_INDEX_HEADS * 4);
+    S.sinks = align256(S.q_attn + (size_t)nq * DS_HEADS * DS_DIM * 2);
+    S.out = align256(S.sinks + S.sinks_floats * 4);
+    S.indices = align256(S.out + (size_t)nq * DS_HEADS * DS_DIM * 2);
+    S.invalid = align256(S.indices + (size_t)ie * 4);
+    S.total = align256(S.invalid + (size_t)nq * DS_HEADS * 4);
+    return S;
+}
+
+// The device address of pinned (page-locked) host memory, which kernels may
+// read and write directly; null for any other memory (pageable or device).
+template <class T>
+T* mapped_host(T* p) {
+    if (!p) return nullptr;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost && a.devicePointer ? static_cast<T*>(a.devicePointer) : nullptr;
+}
+
+int copy_async(void* dst, const void* src, size_t bytes, cudaMemcpyKind kind, cudaStream_t s, const char* what) {
+    if (bytes == 0) return DS_OK;
+    cudaError_t err = cudaMemcpyAsync(dst, src, bytes, kind, s);
+    return err == cudaSuccess ? DS_OK : cuda_fail(err, what);
+}
+
 }  // namespace
 
 extern "C" {
@@ -450,7 +503,7 @@ int ds_rows_indexer_score(const ds_row_set_t* set, const ds_bf16* q_index, const
         if (score_stride < set->table[e].kv_len)
             return fail(DS_EINVAL, "score_stride %zu is shorter than row %d (kv_len %u)", score_stride, e,
                         set->table[e].kv_len);
-    return run_indexer(set, 1, q_index, w_index, scores, score_stride, nullptr, nullptr, (cudaStream_t)stream, false);
+    return run_indexer(set, 1, q_index, w_index, scores, score_stride, nullptr, nullptr, (cudaStream_t)stream, 0);
 }
 
 int ds_rows_topk(const ds_row_set_t* set, const float* scores, size_t score_stride, int32_t* indices,
@@ -511,13 +564,128 @@ int ds_rows_decode(const ds_row_set_t* set, const ds_bf16* q_index, const float*
     float* scores = reinterpret_cast<float*>(ws + L.scores);
     uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
     uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
-    rc = run_indexer(set, 1, q_index, w_index, scores, L.score_stride, hist, status, s, true);
+    rc = run_indexer(set, 1, q_index, w_index, scores, L.score_stride, hist, status, s, 1);
     if (rc) return rc;
     // Selection and attention in one kernel: one 8-CTA cluster per row keeps the
     // selection on chip and attends over it in best-first order, the order of
     // the indices it writes for the caller.
     return run_tail(set, q_attn, sinks, sinks_row_stride, scale, out, invalid, scores, L.score_stride, nullptr,
                     indices, ws, L, s);
+}
+
+size_t ds_rows_decode_host_workspace_bytes(int rows, const ds_row_t* table, size_t sinks_row_stride) {
+    if (check_table(rows, table)) return 0;
+    if (sinks_row_stride != 0 && sinks_row_stride < DS_HEADS) return 0;
+    const ds_row_set_t set = {rows, table, nullptr, nullptr};
+    return make_staging(&set, make_layout(rows, table).total, sinks_row_stride).total;
+}
+
+int ds_rows_decode_host(const ds_row_set_t* set, const ds_bf16* h_q_index, const float* h_w_index,
+                        const ds_bf16* h_q_attn, const float* h_sinks, size_t sinks_row_stride, float scale,
+                        ds_bf16* h_out, int32_t* h_indices, uint32_t* h_invalid, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+    int rc = check_set(set, kNeedKeys | kNeedKv | kUniqueQ | (h_indices ? kDisjointOut : 0u));
+    if (rc) return rc;
+    if (!h_q_index || !h_w_index || !h_q_attn || !h_sinks || !h_out)
+        return fail(DS_EINVAL, "host q_index, w_index, q_attn, sinks and out must be non-NULL");
+    if (!aligned16(h_q_index) || !aligned16(h_q_attn) || !aligned16(h_out))
+        return fail(DS_EALIGN, "host q_index, q_attn and out must be 16-B aligned");
+    if (sinks_row_stride != 0 && sinks_row_stride < DS_HEADS)
+        return fail(DS_EINVAL, "sinks_row_stride must be 0 or >= %d, got %zu", DS_HEADS, sinks_row_stride);
+    if (!(scale > 0.0f) || !(scale < __builtin_huge_valf())) return fail(DS_EINVAL, "scale must be finite and positive");
+    const Layout L = make_layout(set->rows, set->table);
+    const Staging S = make_staging(set, L.total, sinks_row_stride);
+    if (!workspace) return fail(DS_EINVAL, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(DS_EALIGN, "workspace must be 256-byte aligned");
+    if (workspace_bytes < S.total)
+        return fail(DS_ESIZE, "workspace holds %zu bytes, needs %zu", workspace_bytes, S.total);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaStream_t s = (cudaStream_t)stream;
+    const uint32_t nq = S.nq;
+    const bool dense = nq == (uint32_t)set->rows;  // every query row 0..nq-1 is an entry's
+    const size_t qI_row = (size_t)DS_INDEX_HEADS * DS_INDEX_DIM, wI_row = DS_INDEX_HEADS;
+    const size_t qA_row = (size_t)DS_HEADS * DS_DIM;
+    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+
+    // The indexer's query and weights go to device staging (its query is a
+    // TMA operand). Pinned and dense: the workspace-clear kernel copies them
+    // (no copy engine round trip); else copies, whole arrays or entry by entry.
+    auto* d_qI = reinterpret_cast<ds_bf16*>(ws + S.q_index);
+    auto* d_wI = reinterpret_cast<float*>(ws + S.w_index);
+    const ds_bf16* m_qI = dense ? mapped_host(h_q_index) : nullptr;
+    const float* m_wI = dense && aligned16(h_w_index) ? mapped_host(h_w_index) : nullptr;
+    const bool kernel_copy = m_qI && m_wI;
+    if (kernel_copy) {
+    } else if (dense) {
+        rc = copy_async(d_qI, h_q_index, nq * qI_row * 2, h2d, s, "q_index copy");
+        if (!rc) rc = copy_async(d_wI, h_w_index, nq * wI_row * 4, h2d, s, "w_index copy");
+    } else {
+        for (int e = 0; e < set->rows && !rc; ++e) {
+            const size_t r = set->table[e].q_row;
+            rc = copy_async(d_qI + r * qI_row, h_q_index + r * qI_row, qI_row * 2, h2d, s, "q_index copy");
+            if (!rc) rc = copy_async(d_wI + r * wI_row, h_w_index + r * wI_row, wI_row * 4, h2d, s, "w_index copy");
+        }
+    }
+    if (rc) return rc;
+    // The attention reads q_attn and the sinks, and writes its outputs, in
+    // pinned host memory directly; other host memory goes through staging.
+    const ds_bf16* d_qA = mapped_host(h_q_attn);
+    const float* d_sk = mapped_host(h_sinks);
+    ds_bf16* d_out = mapped_host(h_out);
+    int32_t* d_idx = h_indices ? mapped_host(h_indices) : nullptr;
+    uint32_t* d_inv = h_invalid ? mapped_host(h_invalid) : nullptr;
+    const bool stage_out = !d_out, stage_idx = h_indices && !d_idx, stage_inv = h_invalid && !d_inv;
+    if (!d_qA) {
+        auto* st = reinterpret_cast<ds_bf16*>(ws + S.q_attn);
+        if (dense) {
+            rc = copy_async(st, h_q_attn, nq * qA_row * 2, h2d, s, "q_attn copy");
+        } else {
+            for (int e = 0; e < set->rows && !rc; ++e) {
+                const size_t o = (size_t)set->table[e].q_row * qA_row;
+                rc = copy_async(st + o, h_q_attn + o, qA_row * 2, h2d, s, "q_attn copy");
+            }
+        }
+        d_qA = st;
+    }
+    if (!rc && !d_sk) {
+        auto* st = reinterpret_cast<float*>(ws + S.sinks);
+        rc = copy_async(st, h_sinks, S.sinks_floats * 4, h2d, s, "sinks copy");
+        d_sk = st;
+    }
+    if (rc) return rc;
+    if (stage_out) d_out = reinterpret_cast<ds_bf16*>(ws + S.out);
+    if (stage_idx) d_idx = reinterpret_cast<int32_t*>(ws + S.indices);
+    if (stage_inv) d_inv = reinterpret_cast<uint32_t*>(ws + S.invalid);
+
+    cudaError_t err =
+        kernel_copy ? launch_clear_copy(reinterpret_cast<uint32_t*>(ws), (uint32_t)(L.ctl_end / 4), m_qI, d_qI,
+                                        nq * qI_row * 2, m_wI, d_wI, nq * wI_row * 4, s)
+                    : launch_clear(reinterpret_cast<uint32_t*>(ws), (uint32_t)(L.ctl_end / 4), s);
+    if (err != cudaSuccess) return cuda_fail(err, "workspace clear");
+    float* scores = reinterpret_cast<float*>(ws + L.scores);
+    // With the kernel copy the indexer streams keys at once but waits for that
+    // kernel (griddepcontrol.wait) before it reads the query and weights.
+    rc = run_indexer(set, 1, d_qI, d_wI, scores, L.score_stride, reinterpret_cast<uint32_t*>(ws + L.hist),
+                     reinterpret_cast<uint32_t*>(ws + L.status), s, kernel_copy ? 2u : 1u);
+    if (rc) return rc;
+    rc = run_tail(set, d_qA, d_sk, sinks_row_stride, scale, d_out, d_inv, scores, L.score_stride, nullptr, d_idx, ws,
+                  L, s);
+    if (rc) return rc;
+
+    // Staged outputs come back by copy.
+    for (int e = 0; e < set->rows && !rc; ++e) {
+        const ds_row_t& r = set->table[e];
+        const size_t q = r.q_row;
+        if (stage_out && (!dense || e == 0))
+            rc = dense ? copy_async(h_out, d_out, nq * qA_row * 2, d2h, s, "out copy")
+                       : copy_async(h_out + q * qA_row, d_out + q * qA_row, qA_row * 2, d2h, s, "out copy");
+        if (!rc && stage_inv)
+            rc = copy_async(h_invalid + q * DS_HEADS, d_inv + q * DS_HEADS, DS_HEADS * 4, d2h, s, "invalid copy");
+        if (!rc && stage_idx)
+            rc = copy_async(h_indices + r.index_offset, d_idx + r.index_offset, (size_t)r.width * 4, d2h, s,
+                            "indices copy");
+    }
+    return rc;
 }
 
 int ds_rows_topk_static(const ds_row_set_t* set, const float* scores, size_t score_stride, int32_t* indices,
@@ -592,7 +760,7 @@ int ds_rows_indexer_topk_queries(int rows, const ds_indexer_row_t* table, uint32
     if (err != cudaSuccess) return cuda_fail(err, "workspace clear");
     float* scores = reinterpret_cast<float*>(ws + L.scores);
     rc = run_indexer(&kset, query_len, q_index, w_index, scores, L.score_stride,
-                     reinterpret_cast<uint32_t*>(ws + L.hist), reinterpret_cast<uint32_t*>(ws + L.status), s, true,
+                     reinterpret_cast<uint32_t*>(ws + L.hist), reinterpret_cast<uint32_t*>(ws + L.status), s, 1,
                      valid);
     if (rc) return rc;
     // The indexer built the level-0 histogram of each query's valid scores.

@@ -56,6 +56,7 @@ namespace cg = cooperative_groups;
 using attend::CombineSmem;
 using attend::combine_slice;
 using attend::cp_async16;
+using attend::cp_async4;
 using attend::cp_async_commit;
 using attend::cp_async_wait_all;
 using namespace rowsel;
@@ -84,7 +85,8 @@ struct TailLayout {
     static constexpr size_t sel = idx + (size_t)kChunkSlots * 4;       // u64 [512] winners (leader)
     static constexpr size_t red = sel + (size_t)kTopK * 8;             // [4 quarters][32 heads] max, sum, bad
     static constexpr size_t misc = red + 3 * 4 * (size_t)kHalfHeads * 4;
-    static constexpr size_t cs = misc + 64;                            // CombineSmem<32>
+    static constexpr size_t sinks = misc + 64;                         // f32 [32] this head half's sinks
+    static constexpr size_t cs = sinks + (size_t)kHalfHeads * 4;       // CombineSmem<32>
     static constexpr size_t total = cs + sizeof(CombineSmem<kHalfHeads>);
     // Aliases of the KV rows' space, used before the rows are gathered.
     static constexpr size_t select = g;                                // SelectSmem (select phase)
@@ -121,6 +123,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t* tmem_s = nsel_s + 1;
     uint64_t* mma_bar = reinterpret_cast<uint64_t*>(smem + T::misc + 8);
     CombineSmem<kHalfHeads>& cs = *reinterpret_cast<CombineSmem<kHalfHeads>*>(smem + T::cs);
+    float* sinks_s = reinterpret_cast<float*>(smem + T::sinks);
     SelectSmem& sm = *reinterpret_cast<SelectSmem*>(smem + T::select);
 
     cg::cluster_group cluster = cg::this_cluster();
@@ -153,6 +156,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
             const int h = k >> 6, ch = k & 63;
             cp_async16(q_s + sw128_chunk(h, ch, kQBlock), qh + (size_t)h * kDim + ch * 8);
         }
+        // The sinks too (an input, possibly in host memory): the combine uses them last.
+        if (t < kHalfHeads) cp_async4(sinks_s + t, p.sinks + (size_t)q_row * p.sinks_row_stride + head0 + t);
         cp_async_commit();
     }
     tc_fence_before();
@@ -358,7 +363,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     const bool row_bad = __ldcg(p.flags + kRowsMax * kHeads + e) != 0;
     combine_slice<kHalfHeads, kThreads, 128>(
         p.part + part0_off, kPartFloats, (int)nchunks, (int)(128 * c),
-        p.sinks + (size_t)q_row * p.sinks_row_stride + head0, row_bad, p.flags + e * kHeads + head0,
+        sinks_s, row_bad, p.flags + e * kHeads + head0,
         p.out + ((size_t)q_row * kHeads + head0) * kDim,
         p.invalid && c == 0 ? p.invalid + (size_t)q_row * kHeads + head0 : nullptr, cs);
 

@@ -158,7 +158,9 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
     const uint32_t g_end = (uint32_t)(((uint64_t)(blockIdx.x + 1) * T) / NB);
 
     // Inputs may still be in flight from the previous kernel (programmatic
-    // launch): then nothing is read before it completes.
+    // launch): then nothing is read before it completes. With inputs_ready 2
+    // only the query and head weights are: the keys stream from the start, the
+    // query and weight loads wait.
     if (!p.inputs_ready) pdl_wait();
 
     // ---- setup -------------------------------------------------------------
@@ -186,7 +188,7 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
         tmem_alloc(&bar->tmem_base, S::kTmemCols);
         tmem_relinquish();
     }
-    if (G == 1)
+    if (G == 1 && p.inputs_ready != 2)
         for (int i = threadIdx.x; i < (int)p.vrows * kIdxHeads; i += S::kThreads) {
             const int v = i / kIdxHeads, h = i % kIdxHeads;
             w_s[i] = p.w[(size_t)p.q_row[v] * kIdxHeads + h];
@@ -217,6 +219,7 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
                 const uint32_t tile = g - p.tile_begin[sg];
                 if (sg != cur) {
                     cur = sg;
+                    if (p.inputs_ready == 2 && q_uses == 0) pdl_wait();
                     const uint32_t qb = q_uses % S::kQBufs, use = q_uses / S::kQBufs;
                     if (!mbar_wait(&bar->q_empty[qb], (use & 1) ^ 1, p.status)) { ok = false; break; }
                     const int nq = G == 1 ? 1 : p.seg_queries[sg];
@@ -295,6 +298,13 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
         // The histogram may still be being cleared by the previous kernel (PDL):
         // the producer and MMA warps start streaming, the epilogue waits here.
         pdl_wait();
+        if (G == 1 && p.inputs_ready == 2) {
+            for (int i = ep_tid; i < (int)p.vrows * kIdxHeads; i += kEpiThreads) {
+                const int v = i / kIdxHeads, h = i % kIdxHeads;
+                w_s[i] = p.w[(size_t)p.q_row[v] * kIdxHeads + h];
+            }
+            named_bar(1, kEpiThreads);
+        }
         // The scores are read back by the next kernel: keep them in L2 while the
         // key stream (evict-first) passes through.
         const uint64_t keep = l2_policy_evict_last();

@@ -28,7 +28,9 @@ struct IndexerParamsT {
     uint32_t* hist;                 // optional [vrows][2048] score-key histogram
     uint32_t* status;               // device status word
     uint32_t inputs_ready;          // 1: every input was complete when the launch began (it follows an
-                                    // ordinary launch), so loads may start before griddepcontrol.wait
+                                    // ordinary launch), so loads may start before griddepcontrol.wait;
+                                    // 2: the keys were, the query and head weights come from the
+                                    // previous kernel; 0: nothing is read before the wait
     uint64_t score_stride;
     uint32_t rows;                  // entries (key caches)
     uint32_t segs;
@@ -118,6 +120,10 @@ cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t stream, bool pd
 
 // Zero `words` 32-bit words (the workspace control region); an ordinary launch.
 cudaError_t launch_clear(uint32_t* p, uint32_t words, cudaStream_t stream);
+// The same, and copies a_bytes and b_bytes (multiples of 16; 16-byte aligned)
+// from a_src and b_src to a_dst and b_dst before it completes.
+cudaError_t launch_clear_copy(uint32_t* p, uint32_t words, const void* a_src, void* a_dst, size_t a_bytes,
+                              const void* b_src, void* b_dst, size_t b_bytes, cudaStream_t stream);
 
 size_t decode_tail_smem_bytes();
 cudaError_t launch_decode_tail(const TailParams& p, cudaStream_t stream, bool pdl);

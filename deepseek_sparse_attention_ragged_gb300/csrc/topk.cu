@@ -130,4 +130,27 @@ cudaError_t launch_clear(uint32_t* p, uint32_t words, cudaStream_t stream) {
     return launch_kernel(clear_kernel, dim3(16), dim3(1024), 0, stream, false, p, words);
 }
 
+// clear_kernel plus two 16-byte-granular copies (the indexer's query and head
+// weights, from pinned host memory into device staging). The next kernel may
+// start early; it waits for this one (griddepcontrol.wait) before it reads
+// the copies.
+__global__ void __launch_bounds__(1024) clear_copy_kernel(uint32_t* __restrict__ p, uint32_t words,
+                                                          const uint4* __restrict__ a_src, uint4* __restrict__ a_dst,
+                                                          uint32_t a_n, const uint4* __restrict__ b_src,
+                                                          uint4* __restrict__ b_dst, uint32_t b_n) {
+    pdl_trigger();
+    const uint32_t stride = gridDim.x * blockDim.x;
+    const uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x;
+    for (uint32_t i = i0; i < a_n; i += stride) a_dst[i] = a_src[i];
+    for (uint32_t i = i0; i < b_n; i += stride) b_dst[i] = b_src[i];
+    for (uint32_t i = i0; i < words; i += stride) p[i] = 0;
+}
+
+cudaError_t launch_clear_copy(uint32_t* p, uint32_t words, const void* a_src, void* a_dst, size_t a_bytes,
+                              const void* b_src, void* b_dst, size_t b_bytes, cudaStream_t stream) {
+    return launch_kernel(clear_copy_kernel, dim3(16), dim3(1024), 0, stream, false, p, words,
+                         static_cast<const uint4*>(a_src), static_cast<uint4*>(a_dst), (uint32_t)(a_bytes / 16),
+                         static_cast<const uint4*>(b_src), static_cast<uint4*>(b_dst), (uint32_t)(b_bytes / 16));
+}
+
 }  // namespace dsrows

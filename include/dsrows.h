@@ -188,6 +188,38 @@ int ds_rows_decode(const ds_row_set_t* set, const ds_bf16* q_index, const float*
                    float scale, ds_bf16* out, int32_t* indices, uint32_t* invalid,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* Workspace bytes for ds_rows_decode_host: the decode workspace plus device
+ * staging for the step's inputs and outputs; 0 when the table is invalid. */
+size_t ds_rows_decode_host_workspace_bytes(int rows, const ds_row_t* table, size_t sinks_row_stride);
+
+/*
+ * ds_rows_decode with the step's inputs and outputs in HOST memory. The
+ * caches stay on the device (`set`). Everything is ordered on `stream`, and
+ * the call returns before the step completes: synchronise `stream` before
+ * reading h_out. Results are bitwise those of ds_rows_decode.
+ *   - h_q_index and h_w_index are copied into device staging inside the
+ *     workspace (the indexer's query is a tensor-core operand).
+ *   - The attention reads h_q_attn and h_sinks, and writes h_out, h_indices
+ *     and h_invalid, in place when they are pinned (page-locked) host
+ *     memory: no copy. Any other host memory goes through staging, with
+ *     copies before and after the kernels.
+ * The call may be captured in a CUDA graph.
+ *   h_q_index   bf16 [Q, 64, 128] (16-B aligned); h_w_index fp32 [Q, 64]
+ *   h_q_attn    bf16 [Q, 64, 512] (16-B aligned); h_sinks as for ds_rows_decode
+ *   h_out       bf16 [Q, 64, 512] (16-B aligned): the entries' q_rows are
+ *               written, no others.
+ *   h_indices   optional int32 (as ds_rows_decode's indices).
+ *   h_invalid   optional uint32 [Q, 64]: the entries' q_rows are written.
+ *   Q = max q_row + 1. When the entries use every q_row 0..Q-1, a staged array
+ *   travels as one copy, else one copy per entry.
+ *   workspace   at least ds_rows_decode_host_workspace_bytes(...) bytes.
+ * Errors as ds_rows_decode, plus DS_EINVAL for a NULL host array.
+ */
+int ds_rows_decode_host(const ds_row_set_t* set, const ds_bf16* h_q_index, const float* h_w_index,
+                        const ds_bf16* h_q_attn, const float* h_sinks, size_t sinks_row_stride, float scale,
+                        ds_bf16* h_out, int32_t* h_indices, uint32_t* h_invalid, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
 /*
  * One row of a positioned indexer call (`DeepSeekIndexerRow`; compression
  * ratio 4, one query per row):

@@ -216,6 +216,22 @@ def test_indexer_rows_pointers_and_workspace(lib):
     assert _indexer_topk(lib, rows, ws=FAKE + 16) == -3
 
 
+def test_decode_host_checks(lib):
+    rows = [(600, 512, 0, 0), (300, 300, 512, 1)]
+    tab, n = ds._table(rows)
+    rs, keep = _set(rows)
+    call = lambda *a, ws_bytes=1 << 30: lib.ds_rows_decode_host(ctypes.byref(rs), *a, 0, ctypes.c_float(0.05),
+                                                                  FAKE, None, None, FAKE, ws_bytes, None)
+    assert call(None, FAKE, FAKE, FAKE) == -1 and "host q_index" in _err(lib)
+    assert call(FAKE, FAKE, FAKE, None) == -1 and "host q_index" in _err(lib)
+    need = lib.ds_rows_decode_host_workspace_bytes(n, tab, 0)
+    assert need > lib.ds_rows_workspace_bytes(n, tab)
+    assert call(FAKE, FAKE, FAKE, FAKE, ws_bytes=need - 1) == -2 and "workspace holds" in _err(lib)
+    assert lib.ds_rows_decode_host_workspace_bytes(n, tab, 32) == 0  # stride below 64
+    # Per-row sinks make the staging larger.
+    assert lib.ds_rows_decode_host_workspace_bytes(n, tab, 64) > need
+
+
 def _queries(lib, rows, query_len, ws_bytes=1 << 30, ws=FAKE):
     tab, n = ds._indexer_table(rows)
     ptrs = (ctypes.c_void_p * max(1, n))(*[FAKE + 4096 * i for i in range(n)])
