@@ -4,7 +4,7 @@
 //
 // GB300 design. The work is a stream of 128-key tiles over all rows (a row's
 // tile t covers keys [128 t, 128 t + 128) of that row). A persistent CTA takes
-// a contiguous range of tiles. Per tile, one tcgen05.mma chain computes
+// every NB-th tile of the stream (one query per row) or a contiguous range. Per tile, one tcgen05.mma chain computes
 // D[128 keys x 64 heads] = K_tile[128 x 128] * Q[64 x 128]^T into TMEM
 // (M=128, N=64, K=128 as 8 steps of 16). Operands sit in shared memory in the
 // 128-byte-swizzled K-major layout written by TMA. The epilogue gives each
@@ -154,8 +154,17 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
     const int lane = threadIdx.x & 31;
     const uint32_t NB = gridDim.x;
     const uint32_t T = p.total_tiles;
+    // This CTA's k-th tile. One query per entry: every NB-th tile, so all CTAs
+    // sweep the caches side by side and finish together (measured: 0.5 us
+    // faster than contiguous ranges, whose CTAs end up to 4 us apart). Grouped:
+    // a contiguous range, since its single query buffer reloads at every entry.
     const uint32_t g_begin = (uint32_t)(((uint64_t)blockIdx.x * T) / NB);
     const uint32_t g_end = (uint32_t)(((uint64_t)(blockIdx.x + 1) * T) / NB);
+    auto tile_of = [&](uint32_t k) -> uint32_t {
+        if (G == 1) return blockIdx.x + k * NB;
+        const uint32_t g = g_begin + k;
+        return g < g_end ? g : T;
+    };
 
     // Inputs may still be in flight from the previous kernel (programmatic
     // launch): then nothing is read before it completes. With inputs_ready 2
@@ -213,7 +222,9 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
             bool used[S::kStages];
             for (int s = 0; s < S::kStages; ++s) used[s] = false;
             bool ok = true;
-            for (uint32_t g = g_begin; g < g_end && ok; ++g, ++it) {
+            for (;; ++it) {
+                const uint32_t g = tile_of(it);
+                if (g >= T || !ok) break;
                 const int sg = segment_of_tile(p, g);
                 const int e = G == 1 ? sg : p.seg_entry[sg];  // one segment per entry with one query
                 const uint32_t tile = g - p.tile_begin[sg];
@@ -253,7 +264,9 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
         if (lane == 0) {
             int cur = -1;
             uint32_t q_uses = 0, qb = 0, it = 0, idesc = 0;
-            for (uint32_t g = g_begin; g < g_end; ++g, ++it) {
+            for (;; ++it) {
+                const uint32_t g = tile_of(it);
+                if (g >= T) break;
                 if (*(volatile uint32_t*)&bar->abort_flag) break;
                 const int sg = segment_of_tile(p, g);
                 if (sg != cur) {
@@ -338,7 +351,9 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
         uint32_t it = 0, since_flush = 0;
         // One query: the row's head weights stay in registers.
         float wr[G == 1 ? kIdxHeads : 4];
-        for (uint32_t g = g_begin; g < g_end; ++g, ++it) {
+        for (;; ++it) {
+            const uint32_t g = tile_of(it);
+            if (g >= T) break;
             const int sg = segment_of_tile(p, g);
             const uint32_t tile = g - p.tile_begin[sg];
             if (G == 1) {
