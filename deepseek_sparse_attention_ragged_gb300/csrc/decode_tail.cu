@@ -98,6 +98,14 @@ static_assert(TailLayout::misc % 8 == 0, "alignment");
 constexpr size_t kTailSmem = TailLayout::total + 1024;  // + slack to align the swizzled buffers to 1 KiB
 static_assert(kTailSmem <= 227 * 1024, "shared memory");
 
+// Maximum over the warp, in the integer reduction unit: finite values and
+// -inf map order-preservingly to int (no NaN reaches here).
+__device__ __forceinline__ float warp_max(float x) {
+    const int i = __float_as_int(x);
+    const int r = __reduce_max_sync(0xFFFFFFFFu, i >= 0 ? i : i ^ 0x7FFFFFFF);
+    return __int_as_float(r >= 0 ? r : r ^ 0x7FFFFFFF);
+}
+
 // Byte offset of 16-byte chunk ch (0..63) of row r in a K-major SW128 buffer of
 // 64-column blocks `block` bytes apart (rows of 128 B per block).
 __device__ __forceinline__ uint32_t sw128_chunk(int r, int ch, int block) {
@@ -281,9 +289,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
             if (lane == 0) red_bad[qt * kHalfHeads + 8 * hg + i] = bad ? 1u : 0u;
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) m[i] = fmaxf(m[i], __shfl_xor_sync(0xFFFFFFFFu, m[i], o));
+        for (int i = 0; i < 8; ++i) m[i] = warp_max(m[i]);
         if (lane == 0)
 #pragma unroll
             for (int i = 0; i < 8; ++i) red_max[qt * kHalfHeads + 8 * hg + i] = m[i];
