@@ -237,7 +237,8 @@ int check_workspace(const ds_row_set_t* set, void* ws, size_t bytes, const Layou
 template <class P>
 int fill_and_launch_indexer(P& p, int group, const ds_row_set_t* set, uint32_t query_len, const ds_bf16* q_index,
                             const float* w_index, float* scores, uint64_t stride, uint32_t* hist, uint32_t* status,
-                            cudaStream_t stream, uint32_t inputs_ready, const uint32_t* valid) {
+                            cudaStream_t stream, uint32_t inputs_ready, const uint32_t* valid, const void* side_src,
+                            void* side_dst, size_t side_bytes) {
     int rc = get_encoder();
     if (rc) return rc;
     std::memset(&p, 0, sizeof(p));
@@ -278,6 +279,9 @@ int fill_and_launch_indexer(P& p, int group, const ds_row_set_t* set, uint32_t q
     p.status = status;
     p.score_stride = stride;
     p.inputs_ready = inputs_ready;
+    p.side_src = static_cast<const uint4*>(side_src);
+    p.side_dst = static_cast<uint4*>(side_dst);
+    p.side_n16 = (uint32_t)(side_bytes / 16);
     p.rows = (uint32_t)set->rows;
     p.segs = segs;
     p.vrows = (uint32_t)set->rows * query_len;
@@ -288,18 +292,20 @@ int fill_and_launch_indexer(P& p, int group, const ds_row_set_t* set, uint32_t q
     return err == cudaSuccess ? DS_OK : cuda_fail(err, "indexer launch");
 }
 
+// `side_*`: an optional copy the indexer makes for the attention (see IndexerParamsT).
 int run_indexer(const ds_row_set_t* set, uint32_t query_len, const ds_bf16* q_index, const float* w_index,
                 float* scores, uint64_t stride, uint32_t* hist, uint32_t* status, cudaStream_t stream,
-                uint32_t inputs_ready, const uint32_t* valid = nullptr) {
+                uint32_t inputs_ready, const uint32_t* valid = nullptr, const void* side_src = nullptr,
+                void* side_dst = nullptr, size_t side_bytes = 0) {
     // The tables hold CUtensorMaps (~1.3-2.2 KB); built per call on the host.
     if (query_len == 1) {
         IndexerParams1 p;
         return fill_and_launch_indexer(p, 1, set, query_len, q_index, w_index, scores, stride, hist, status, stream,
-                                       inputs_ready, valid);
+                                       inputs_ready, valid, side_src, side_dst, side_bytes);
     }
     IndexerParamsG p;
     return fill_and_launch_indexer(p, kIndexerGroup, set, query_len, q_index, w_index, scores, stride, hist, status,
-                                   stream, inputs_ready, valid);
+                                   stream, inputs_ready, valid, side_src, side_dst, side_bytes);
 }
 
 int run_topk(const ds_row_set_t* set, const float* scores, uint64_t stride, int32_t* out, const uint32_t* out_offset,
@@ -339,7 +345,8 @@ int run_topk(const ds_row_set_t* set, const float* scores, uint64_t stride, int3
 // attention: one 8-CTA cluster per row.
 int run_tail(const ds_row_set_t* set, const ds_bf16* q_attn, const float* sinks, size_t sinks_row_stride,
              float scale, ds_bf16* out, uint32_t* invalid, const float* scores, uint64_t score_stride,
-             const int32_t* given, int32_t* indices, uint8_t* ws, const Layout& L, cudaStream_t stream) {
+             const int32_t* given, int32_t* indices, uint8_t* ws, const Layout& L, cudaStream_t stream,
+             bool q_after_wait = false) {
     TailParams tp;
     std::memset(&tp, 0, sizeof(tp));
     uint32_t chunks = 0;
@@ -358,6 +365,7 @@ int run_tail(const ds_row_set_t* set, const ds_bf16* q_attn, const float* sinks,
     tp.hist = reinterpret_cast<const uint32_t*>(ws + L.hist);
     tp.status = reinterpret_cast<uint32_t*>(ws + L.status);
     tp.q = reinterpret_cast<const __nv_bfloat16*>(q_attn);
+    tp.q_after_wait = q_after_wait ? 1u : 0u;
     tp.sinks = sinks;
     tp.sinks_row_stride = sinks_row_stride;
     tp.part = reinterpret_cast<float*>(ws + L.part);
@@ -629,7 +637,12 @@ int ds_rows_decode_host(const ds_row_set_t* set, const ds_bf16* h_q_index, const
     if (rc) return rc;
     // The attention reads q_attn and the sinks, and writes its outputs, in
     // pinned host memory directly; other host memory goes through staging.
-    const ds_bf16* d_qA = mapped_host(h_q_attn);
+    // A pinned q_attn is copied into staging by the indexer's epilogue warps
+    // while they wait for the first scores (the attention would otherwise
+    // fetch it from host memory on its critical path); the attention then
+    // fetches it after its wait.
+    const ds_bf16* m_qA = mapped_host(h_q_attn);
+    const ds_bf16* d_qA = m_qA ? reinterpret_cast<const ds_bf16*>(ws + S.q_attn) : nullptr;
     const float* d_sk = mapped_host(h_sinks);
     ds_bf16* d_out = mapped_host(h_out);
     int32_t* d_idx = h_indices ? mapped_host(h_indices) : nullptr;
@@ -666,10 +679,11 @@ int ds_rows_decode_host(const ds_row_set_t* set, const ds_bf16* h_q_index, const
     // With the kernel copy the indexer streams keys at once but waits for that
     // kernel (griddepcontrol.wait) before it reads the query and weights.
     rc = run_indexer(set, 1, d_qI, d_wI, scores, L.score_stride, reinterpret_cast<uint32_t*>(ws + L.hist),
-                     reinterpret_cast<uint32_t*>(ws + L.status), s, kernel_copy ? 2u : 1u);
+                     reinterpret_cast<uint32_t*>(ws + L.status), s, kernel_copy ? 2u : 1u, nullptr, m_qA,
+                     ws + S.q_attn, m_qA ? nq * qA_row * 2 : 0);
     if (rc) return rc;
     rc = run_tail(set, d_qA, d_sk, sinks_row_stride, scale, d_out, d_inv, scores, L.score_stride, nullptr, d_idx, ws,
-                  L, s);
+                  L, s, m_qA != nullptr);
     if (rc) return rc;
 
     // Staged outputs come back by copy.

@@ -158,21 +158,24 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_alloc(tmem_s, kTmemCols);
         tmem_relinquish();
     }
-    {
+    // The query half (cp.async into the swizzled layout; waited for before the
+    // logits) and the sinks (possibly in host memory; the combine uses them last).
+    auto fetch_inputs = [&]() {
         const __nv_bfloat16* qh = p.q + ((size_t)q_row * kHeads + head0) * kDim;
         for (int k = t; k < kHalfHeads * (kDim / 8); k += kThreads) {
             const int h = k >> 6, ch = k & 63;
             cp_async16(q_s + sw128_chunk(h, ch, kQBlock), qh + (size_t)h * kDim + ch * 8);
         }
-        // The sinks too (an input, possibly in host memory): the combine uses them last.
         if (t < kHalfHeads) cp_async4(sinks_s + t, p.sinks + (size_t)q_row * p.sinks_row_stride + head0 + t);
         cp_async_commit();
-    }
+    };
+    if (!p.q_after_wait) fetch_inputs();
     tc_fence_before();
     cluster.sync();  // the leader's counters are zero before anyone appends
     tc_fence_after();
     const uint32_t tmem = *tmem_s;
     pdl_wait();  // scores and histogram (decode) or indices (caller) come from earlier work
+    if (p.q_after_wait) fetch_inputs();
 
     if (p.given == nullptr) {
         // ---- select -------------------------------------------------------------

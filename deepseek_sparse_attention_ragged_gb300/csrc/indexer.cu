@@ -311,6 +311,8 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
         // The histogram may still be being cleared by the previous kernel (PDL):
         // the producer and MMA warps start streaming, the epilogue waits here.
         pdl_wait();
+        for (uint32_t i = blockIdx.x * kEpiThreads + ep_tid; i < p.side_n16; i += NB * kEpiThreads)
+            p.side_dst[i] = p.side_src[i];
         if (G == 1 && p.inputs_ready == 2) {
             for (int i = ep_tid; i < (int)p.vrows * kIdxHeads; i += kEpiThreads) {
                 const int v = i / kIdxHeads, h = i % kIdxHeads;

@@ -42,6 +42,12 @@ struct IndexerParamsT {
     uint8_t seg_queries[SEGS];      // its virtual rows: 1..group
     uint32_t valid[VROWS];          // keys j < valid[v] are scored
     uint32_t q_row[VROWS];          // query and head-weight row of each virtual row
+    // Optional copy for the next kernel, done by the epilogue warps while they
+    // wait for the first scores: side_n16 16-byte words from side_src (pinned
+    // host memory) to side_dst.
+    const uint4* side_src;
+    uint4* side_dst;
+    uint32_t side_n16;
 };
 using IndexerParams1 = IndexerParamsT<DS_ROWS_MAX, DS_ROWS_MAX>;  // one query per entry
 using IndexerParamsG = IndexerParamsT<kSegMax, kVRowsMax>;        // up to kIndexerGroup per segment
@@ -74,6 +80,7 @@ struct TailParams {
     uint32_t* status;
     const __nv_bfloat16* kv[DS_ROWS_MAX];
     const __nv_bfloat16* q;       // [Q, 64, 512]
+    uint32_t q_after_wait;        // 1: q is written by the previous kernel (fetch it after the wait)
     const float* sinks;
     uint64_t sinks_row_stride;
     float* part;                  // partials: m[32], l[32], acc[32][512] per (chunk, head half)

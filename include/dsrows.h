@@ -198,11 +198,13 @@ size_t ds_rows_decode_host_workspace_bytes(int rows, const ds_row_t* table, size
  * the call returns before the step completes: synchronise `stream` before
  * reading h_out. Results are bitwise those of ds_rows_decode.
  *   - h_q_index and h_w_index are copied into device staging inside the
- *     workspace (the indexer's query is a tensor-core operand).
- *   - The attention reads h_q_attn and h_sinks, and writes h_out, h_indices
- *     and h_invalid, in place when they are pinned (page-locked) host
- *     memory: no copy. Any other host memory goes through staging, with
- *     copies before and after the kernels.
+ *     workspace (the indexer's query is a tensor-core operand); when pinned,
+ *     by the workspace-clear kernel itself.
+ *   - A pinned h_q_attn is copied into staging by the indexer while it waits
+ *     for its first scores; the attention reads h_sinks, and writes h_out,
+ *     h_indices and h_invalid, in place when they are pinned (page-locked)
+ *     host memory. Any other host memory goes through staging, with
+ *     cudaMemcpyAsync before and after the kernels.
  * The call may be captured in a CUDA graph.
  *   h_q_index   bf16 [Q, 64, 128] (16-B aligned); h_w_index fp32 [Q, 64]
  *   h_q_attn    bf16 [Q, 64, 512] (16-B aligned); h_sinks as for ds_rows_decode
