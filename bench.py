@@ -317,6 +317,7 @@ def main():
     device = torch.device("cuda", torch.cuda.current_device() if world == 1 else local)
 
     import deepseek_sparse_attention_ragged_gb300 as ds
+    from deepseek_sparse_attention_ragged_gb300.replicas import job_rate, max_over_ranks
     import workloads
     from workloads.device import to_device
 
@@ -415,12 +416,9 @@ def main():
 
     latency_graph_ms = flushed(lambda i: graphs[i].replay())
     latency_eager_ms = flushed(step)
-    if world > 1:
-        t = torch.tensor([total_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, device)
     ms_per_step = total_ms / args.steps
-    value = world * R * args.steps / (total_ms / 1e3)
+    value = job_rate(world, R, args.steps, total_ms)
     alg_bytes = wl.algorithmic_bytes()
     step_gbs = alg_bytes / (ms_per_step / 1e3) / 1e9
 
@@ -488,10 +486,7 @@ def main():
         t1.record(stream)
     barrier()
     e2e_ms = t0.elapsed_time(t1) / (4 * e2e_graphs)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, device)
 
     # The positioned indexer with its causal top-512 (every key valid, offset 0)
     # on the same caches: 20 calls back to back.
@@ -538,7 +533,7 @@ def main():
             "roofline": {"kernel": "indexer_score_kernel", "bound": "hbm", "achieved": idx_gbs, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": idx_gbs / peak, "traffic": idx_traffic,
                          "bytes_per_launch": idx_bytes, "ms_per_launch": idx_ms},
-            "e2e": {"value": world * R / (e2e_ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": job_rate(world, R, 1, e2e_ms), "unit": "rows/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": 3 * args.steps,
             "indexer_topk": {"entry": "ds_rows_indexer_topk", "workload": "same caches, every key valid, offset 0",
