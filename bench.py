@@ -426,19 +426,31 @@ def main():
     # its entry point; 20 launches back to back (keys larger than L2), timed as a batch.
     stride = max(r.kv_len for r in wl.rows)
     scores = torch.empty((R, stride), dtype=torch.float32, device=device)
-    n_idx = 20
-    a_ev = torch.cuda.Event(enable_timing=True)
-    b_ev = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            ds.ds_rows_indexer_score(dev.rows, dev.q_index, dev.w_index, dev.keys, scores, stride, stream=stream)
-        a_ev.record(stream)
-        for i in range(n_idx):
-            qI, wI, _ = qsets[i % 4]
-            ds.ds_rows_indexer_score(dev.rows, qI, wI, dev.keys, scores, stride, stream=stream)
-        b_ev.record(stream)
-    torch.cuda.synchronize(device)
-    idx_ms = a_ev.elapsed_time(b_ev) / n_idx
+    def graph_ms_per_call(call, reps=5):
+        """Mean device time of call(i) for the four query sets i, captured in one
+        CUDA graph and replayed `reps` times (no host marshalling in the timing)."""
+        with torch.cuda.stream(stream):
+            for i in range(4):
+                call(i)
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(4):
+                call(i)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+        torch.cuda.synchronize(device)
+        return a.elapsed_time(b) / (4 * reps)
+
+    # The indexer alone, 20 launches back to back (keys larger than L2).
+    idx_ms = graph_ms_per_call(lambda i: ds.ds_rows_indexer_score(dev.rows, qsets[i][0], qsets[i][1], dev.keys,
+                                                                  scores, stride, stream=stream))
     idx_bytes = sum(256 * r.kv_len + 4 * r.kv_len + 16384 + 256 for r in wl.rows)
     peak, peak_kind = peaks()
     idx_gbs = idx_bytes / (idx_ms / 1e3) / 1e9
@@ -493,16 +505,8 @@ def main():
     prow = [ds.IndexerRow(r.kv_len, 4 * r.kv_len - 1, 0, r.q_row, 512 * e) for e, r in enumerate(wl.rows)]
     pidx = torch.empty((512 * R,), dtype=torch.int32, device=device)
     pws = ds.indexer_topk_workspace(prow, device)
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            ds.ds_rows_indexer_topk(prow, dev.q_index, dev.w_index, dev.keys, pidx, workspace_t=pws, stream=stream)
-        a_ev.record(stream)
-        for i in range(n_idx):
-            qI, wI, _ = qsets[i % 4]
-            ds.ds_rows_indexer_topk(prow, qI, wI, dev.keys, pidx, workspace_t=pws, stream=stream)
-        b_ev.record(stream)
-    torch.cuda.synchronize(device)
-    pidx_ms = a_ev.elapsed_time(b_ev) / n_idx
+    pidx_ms = graph_ms_per_call(lambda i: ds.ds_rows_indexer_topk(prow, qsets[i][0], qsets[i][1], dev.keys, pidx,
+                                                                  workspace_t=pws, stream=stream))
     pidx_bytes = sum(256 * r.kv_len + 16384 + 256 + 4 * 512 for r in wl.rows)
 
     per_config = None
