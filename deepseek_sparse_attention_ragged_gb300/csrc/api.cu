@@ -346,13 +346,13 @@ int run_topk(const ds_row_set_t* set, const float* scores, uint64_t stride, int3
 int run_tail(const ds_row_set_t* set, const ds_bf16* q_attn, const float* sinks, size_t sinks_row_stride,
              float scale, ds_bf16* out, uint32_t* invalid, const float* scores, uint64_t score_stride,
              const int32_t* given, int32_t* indices, uint8_t* ws, const Layout& L, cudaStream_t stream,
-             bool q_after_wait = false) {
+             bool q_after_wait = false, bool attend = true, const int32_t* offsets = nullptr) {
     TailParams tp;
     std::memset(&tp, 0, sizeof(tp));
     uint32_t chunks = 0;
     for (int e = 0; e < set->rows; ++e) {
         const ds_row_t& r = set->table[e];
-        tp.kv[e] = reinterpret_cast<const __nv_bfloat16*>(set->kv[e]);
+        tp.kv[e] = set->kv ? reinterpret_cast<const __nv_bfloat16*>(set->kv[e]) : nullptr;
         tp.kv_len[e] = r.kv_len;
         tp.width[e] = r.width;
         tp.index_offset[e] = r.index_offset;
@@ -366,6 +366,8 @@ int run_tail(const ds_row_set_t* set, const ds_bf16* q_attn, const float* sinks,
     tp.status = reinterpret_cast<uint32_t*>(ws + L.status);
     tp.q = reinterpret_cast<const __nv_bfloat16*>(q_attn);
     tp.q_after_wait = q_after_wait ? 1u : 0u;
+    tp.attend = attend ? 1u : 0u;
+    for (int e = 0; e < set->rows; ++e) tp.offset[e] = offsets ? offsets[e] : 0;
     tp.sinks = sinks;
     tp.sinks_row_stride = sinks_row_stride;
     tp.part = reinterpret_cast<float*>(ws + L.part);
@@ -777,7 +779,12 @@ int ds_rows_indexer_topk_queries(int rows, const ds_indexer_row_t* table, uint32
                      reinterpret_cast<uint32_t*>(ws + L.hist), reinterpret_cast<uint32_t*>(ws + L.status), s, 1,
                      valid);
     if (rc) return rc;
-    // The indexer built the level-0 histogram of each query's valid scores.
+    // The indexer built the level-0 histogram of each query's valid scores. One
+    // query per row: the decode's selection (the tail kernel, selection only),
+    // which places the winners by distributed ranking; else the top-k kernel.
+    if (query_len == 1)
+        return run_tail(&sset, nullptr, nullptr, 0, 1.0f, nullptr, nullptr, scores, L.score_stride, nullptr, indices,
+                        ws, L, s, false, false, offsets);
     return run_topk(&sset, scores, L.score_stride, indices, out_off, ws, L, false, false, s, offsets);
 }
 

@@ -154,7 +154,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(mma_bar, kIssuers);
         fence_barrier_init();
     }
-    if (warp == 0) {
+    if (warp == 0 && p.attend) {
         tmem_alloc(tmem_s, kTmemCols);
         tmem_relinquish();
     }
@@ -169,13 +169,13 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         if (t < kHalfHeads) cp_async4(sinks_s + t, p.sinks + (size_t)q_row * p.sinks_row_stride + head0 + t);
         cp_async_commit();
     };
-    if (!p.q_after_wait) fetch_inputs();
+    if (p.attend && !p.q_after_wait) fetch_inputs();
     tc_fence_before();
     cluster.sync();  // the leader's counters are zero before anyone appends
     tc_fence_after();
-    const uint32_t tmem = *tmem_s;
+    const uint32_t tmem = p.attend ? *tmem_s : 0u;
     pdl_wait();  // scores and histogram (decode) or indices (caller) come from earlier work
-    if (p.q_after_wait) fetch_inputs();
+    if (p.attend && p.q_after_wait) fetch_inputs();
 
     if (p.given == nullptr) {
         // ---- select -------------------------------------------------------------
@@ -218,14 +218,19 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
             if (k < nsel) {
                 const uint32_t pos = rk[t];
                 const int32_t j = (int32_t)(~(uint32_t)ck);
-                if (out) out[pos] = j;
-                const uint32_t owner = 2 * (pos / kChunkSlots);
-                cluster.map_shared_rank(idx_s, owner)[pos % kChunkSlots] = j;
-                cluster.map_shared_rank(idx_s, owner + 1)[pos % kChunkSlots] = j;
+                if (out) out[pos] = j + p.offset[e];
+                if (p.attend) {
+                    const uint32_t owner = 2 * (pos / kChunkSlots);
+                    cluster.map_shared_rank(idx_s, owner)[pos % kChunkSlots] = j;
+                    cluster.map_shared_rank(idx_s, owner + 1)[pos % kChunkSlots] = j;
+                }
             } else if (out && k < W) {
                 out[k] = -1;
             }
         }
+        // Selection only: the indices are out; no CTA touches another's shared
+        // memory after the winners' barrier, so the cluster may leave.
+        if (!p.attend) return;
     } else if (t < kChunkSlots) {
         // ---- the caller's indices: -1 for sentinels, bad indices and slots past the width
         const uint32_t slot = c * kChunkSlots + (uint32_t)t;

@@ -81,6 +81,7 @@ struct TailParams {
     const __nv_bfloat16* kv[DS_ROWS_MAX];
     const __nv_bfloat16* q;       // [Q, 64, 512]
     uint32_t q_after_wait;        // 1: q is written by the previous kernel (fetch it after the wait)
+    uint32_t attend;              // 0: selection only (decode mode): write the indices and stop
     const float* sinks;
     uint64_t sinks_row_stride;
     float* part;                  // partials: m[32], l[32], acc[32][512] per (chunk, head half)
@@ -96,6 +97,7 @@ struct TailParams {
     uint32_t index_offset[DS_ROWS_MAX];
     uint32_t q_row[DS_ROWS_MAX];
     uint32_t chunk_begin[DS_ROWS_MAX];  // first 128-slot chunk of each row
+    int32_t offset[DS_ROWS_MAX];        // added to the selected indices written out
 };
 
 // Learned KV compressor, one decode token per row: one 8-CTA cluster per row.
