@@ -309,7 +309,7 @@ int run_indexer(const ds_row_set_t* set, uint32_t query_len, const ds_bf16* q_in
 }
 
 int run_topk(const ds_row_set_t* set, const float* scores, uint64_t stride, int32_t* out, const uint32_t* out_offset,
-             uint8_t* ws, const Layout& L, bool with_hist, bool by_index, cudaStream_t stream,
+             uint8_t* ws, const Layout& L, bool with_hist, cudaStream_t stream,
              const int32_t* offsets = nullptr) {
     if (set->rows > kVRowsMax) return fail(DS_EINVAL, "too many top-k rows");
     TopkParams p;
@@ -330,7 +330,6 @@ int run_topk(const ds_row_set_t* set, const float* scores, uint64_t stride, int3
     p.hist = reinterpret_cast<uint32_t*>(ws + L.hist);
     p.status = reinterpret_cast<uint32_t*>(ws + L.status);
     p.rows = (uint32_t)set->rows;
-    p.order_by_index = by_index ? 1u : 0u;
     p.total_chunks = chunks;
     cudaError_t err = cudaSuccess;
     if (with_hist) {
@@ -534,7 +533,7 @@ int ds_rows_topk(const ds_row_set_t* set, const float* scores, size_t score_stri
     if (err != cudaSuccess) return cuda_fail(err, "workspace clear");
     uint32_t off[DS_ROWS_MAX];
     for (int e = 0; e < set->rows; ++e) off[e] = set->table[e].index_offset;
-    return run_topk(set, scores, score_stride, indices, off, ws, L, true, false, s);
+    return run_topk(set, scores, score_stride, indices, off, ws, L, true, s);
 }
 
 int ds_rows_sparse_attn(const ds_row_set_t* set, const ds_bf16* q_attn, const float* sinks,
@@ -728,7 +727,7 @@ int ds_rows_topk_static(const ds_row_set_t* set, const float* scores, size_t sco
     if (err != cudaSuccess) return cuda_fail(err, "scratch clear");
     uint32_t off[DS_ROWS_MAX];
     for (int e = 0; e < set->rows; ++e) off[e] = set->table[e].index_offset;
-    return run_topk(set, scores, score_stride, indices, off, ws, L, true, false, s);
+    return run_topk(set, scores, score_stride, indices, off, ws, L, true, s);
 }
 
 size_t ds_rows_indexer_topk_queries_workspace_bytes(int rows, const ds_indexer_row_t* table, uint32_t query_len) {
@@ -785,7 +784,7 @@ int ds_rows_indexer_topk_queries(int rows, const ds_indexer_row_t* table, uint32
     if (query_len == 1)
         return run_tail(&sset, nullptr, nullptr, 0, 1.0f, nullptr, nullptr, scores, L.score_stride, nullptr, indices,
                         ws, L, s, false, false, offsets);
-    return run_topk(&sset, scores, L.score_stride, indices, out_off, ws, L, false, false, s, offsets);
+    return run_topk(&sset, scores, L.score_stride, indices, out_off, ws, L, false, s, offsets);
 }
 
 int ds_rows_indexer_topk(int rows, const ds_indexer_row_t* table, const ds_bf16* const* index_keys,

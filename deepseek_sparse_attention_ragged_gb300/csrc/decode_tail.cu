@@ -186,7 +186,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         if (rank == 0) {
             // The leader refines, then pushes the winners (zero past the last) and
             // their number into every CTA's shared memory.
-            const uint32_t n = select_finish(col, s, L, W, false, nullptr, sm, sel, p.status);
+            const uint32_t n = select_finish(col, s, L, W, nullptr, sm, sel, p.status);
             const uint64_t wv = (uint32_t)t < n ? sel[t] : 0ull;
 #pragma unroll
             for (int r = 0; r < kCluster; ++r) {

@@ -60,7 +60,6 @@ struct TopkParams {
     uint32_t* hist;        // [8][2048] level 0 (top 11 key bits), zero before it is built
     uint32_t* status;
     uint32_t rows;
-    uint32_t order_by_index;  // 0: best first; 1: ascending index (the decode's canonical order)
     uint32_t total_chunks;    // histogram CTAs (chunks of topk_chunk() scores)
     uint32_t kv_len[kVRowsMax];
     uint32_t width[kVRowsMax];

@@ -104,7 +104,6 @@ struct RowSource {
 
 constexpr int kCluster = 8;        // CTAs per row in the select kernel
 constexpr int kLeaderCap = 8192;   // candidates the leader CTA holds in shared memory
-constexpr int kBitmapWords = kLeaderCap * 2;  // the candidate space as a bitmap: rows up to 524288 keys
 
 constexpr uint32_t kRankDirect = 128;  // a threshold bin this small is ranked element by element
 
@@ -141,59 +140,16 @@ __device__ __forceinline__ Refine refine_from_level0(const BinPick& l0, uint32_t
 }
 
 // Write the nsel winners of sel (composites), as index + offset, to
-// out[0, width), then -1; `out` may point to global or shared memory, and sel
-// is left unchanged.
-// Best first: sorted by composite. Index order (ascending): through a bitmap of
-// the row's L positions in the candidate space when it fits, else sorted by index.
+// out[0, width) best first (sorted by composite), then -1; `out` may point to
+// global or shared memory, and sel is left unchanged.
 __device__ __forceinline__ void write_winners(SelectSmem& sm, const uint64_t* sel, uint32_t nsel, uint32_t width,
-                                              uint32_t L, bool by_index, int32_t* out, int32_t offset) {
-    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const uint32_t words = (L + 31) / 32;
-    if (!by_index || words > (uint32_t)kBitmapWords) {
-        const uint64_t c = sel[t];
-        // Best first: the composite. Index order: its low word ~index, larger for a
-        // lower index (zero stays the padding). Either way ~(low word) is the index.
-        uint64_t x[1] = {by_index ? (uint64_t)(uint32_t)c : c};
-        __syncthreads();  // every thread holds its element before the buffer is reused
-        sort512_desc<kThreads>(x, sm.cand);  // the candidates are consumed
-        if ((uint32_t)t < width) out[t] = (uint32_t)t < nsel ? (int32_t)(~(uint32_t)x[0]) + offset : -1;
-        return;
-    }
-    uint32_t* bm = reinterpret_cast<uint32_t*>(sm.cand);  // the candidates are consumed
-    for (uint32_t w = t; w < words; w += kThreads) bm[w] = 0;
-    __syncthreads();
-    if ((uint32_t)t < nsel) {
-        const uint32_t j = ~(uint32_t)sel[t];
-        atomicOr(&bm[j >> 5], 1u << (j & 31));
-    }
-    __syncthreads();
-    // Each thread owns a contiguous run of words; a block scan of the run
-    // popcounts gives every set bit its place.
-    const uint32_t per = (words + kThreads - 1) / kThreads;
-    const uint32_t w0 = min(words, t * per), w1 = min(words, w0 + per);
-    uint32_t cnt = 0;
-    for (uint32_t w = w0; w < w1; ++w) cnt += __popc(bm[w]);
-    uint32_t incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) sm.scratch[warp] = incl;
-    __syncthreads();
-    uint32_t before = 0;
-    for (int w = 0; w < warp; ++w) before += sm.scratch[w];
-    uint32_t at = before + incl - cnt;
-    for (uint32_t w = w0; w < w1; ++w) {
-        uint32_t bits = bm[w];
-        while (bits) {
-            const int b = __ffs(bits) - 1;
-            bits &= bits - 1;
-            if (at < width) out[at] = (int32_t)(32 * w + b) + offset;
-            ++at;
-        }
-    }
-    for (uint32_t k = nsel + t; k < width; k += kThreads) out[k] = -1;
+                                              int32_t* out, int32_t offset) {
+    const int t = threadIdx.x;
+    uint64_t x[1] = {sel[t]};
+    __syncthreads();  // every thread holds its element before the buffer is reused
+    sort512_desc<kThreads>(x, sm.cand);  // the candidates are consumed
+    // ~(low word) of a composite is its index.
+    if ((uint32_t)t < width) out[t] = (uint32_t)t < nsel ? (int32_t)(~(uint32_t)x[0]) + offset : -1;
 }
 
 // Refine digit by digit until the threshold bin is taken whole or holds at
@@ -202,7 +158,7 @@ __device__ __forceinline__ void write_winners(SelectSmem& sm, const uint64_t* se
 // the bin's elements, found by counting for each how many of them are better.
 // Writes their indices to out (unless out is null). Returns the number of winners.
 template <class Src>
-__device__ inline uint32_t finish_row(const Src& src, Refine st, uint32_t width, uint32_t L, bool by_index, int32_t* out,
+__device__ inline uint32_t finish_row(const Src& src, Refine st, uint32_t width, uint32_t L, int32_t* out,
                                       SelectSmem& sm, uint64_t* sel, uint32_t* status, int32_t offset = 0) {
     const int t = threadIdx.x, lane = t & 31;
     const bool take_all = st.take_all;
@@ -286,7 +242,7 @@ __device__ inline uint32_t finish_row(const Src& src, Refine st, uint32_t width,
     const uint32_t got = sm.nsel;
     const uint32_t nsel = got < width ? got : width;
     if (got > width && t == 0) atomicOr(status, kStatusCandOverflow);
-    if (out) write_winners(sm, sel, nsel, width, L, by_index, out, offset);
+    if (out) write_winners(sm, sel, nsel, width, out, offset);
     return nsel;
 }
 
@@ -386,7 +342,7 @@ __device__ __forceinline__ Collected select_collect(const float* s, uint32_t L, 
 // The leader's half of a row's selection, after the collection phase and a
 // cluster barrier: refine, keep the winners in sel and write their indices.
 __device__ __forceinline__ uint32_t select_finish(const Collected& c, const float* s, uint32_t L, uint32_t width,
-                                                  bool by_index, int32_t* out, SelectSmem& sm, uint64_t* sel,
+                                                  int32_t* out, SelectSmem& sm, uint64_t* sel,
                                                   uint32_t* status, int32_t offset = 0) {
     if (c.fast) {
         const uint32_t got = sm.ncand;
@@ -396,9 +352,9 @@ __device__ __forceinline__ uint32_t select_finish(const Collected& c, const floa
         l0f.bin = (int)c.b0;
         const Refine st = refine_from_level0(l0f, width);
         return finish_row(SmemCandSource{sm.cand, got < (uint32_t)kLeaderCap ? got : (uint32_t)kLeaderCap}, st, width,
-                          L, by_index, out, sm, sel, status, offset);
+                          L, out, sm, sel, status, offset);
     }
-    return finish_row(RowSource{s, L}, refine_from_level0(c.l0, width), width, L, by_index, out, sm, sel, status,
+    return finish_row(RowSource{s, L}, refine_from_level0(c.l0, width), width, L, out, sm, sel, status,
                       offset);
 }
 

@@ -99,7 +99,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
     const Collected c = select_collect(s, L, width, p.hist + (size_t)e * kHistBins, rank, sm, leader);
     cluster.sync();  // every append into the leader is visible to it
     if (rank != 0) return;
-    select_finish(c, s, L, width, p.order_by_index != 0, p.out + p.out_offset[e], sm, sel, p.status, p.offset[e]);
+    select_finish(c, s, L, width, p.out + p.out_offset[e], sm, sel, p.status, p.offset[e]);
 }
 
 uint32_t topk_chunk() { return kChunk; }
