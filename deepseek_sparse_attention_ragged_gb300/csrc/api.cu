@@ -308,9 +308,11 @@ int run_indexer(const ds_row_set_t* set, uint32_t query_len, const ds_bf16* q_in
                                    stream, inputs_ready, valid, side_src, side_dst, side_bytes);
 }
 
+// The level-0 histogram (with_hist) and the top-k kernel's selection
+// (select), one 8-CTA cluster per row.
 int run_topk(const ds_row_set_t* set, const float* scores, uint64_t stride, int32_t* out, const uint32_t* out_offset,
              uint8_t* ws, const Layout& L, bool with_hist, cudaStream_t stream,
-             const int32_t* offsets = nullptr) {
+             const int32_t* offsets = nullptr, bool select = true) {
     if (set->rows > kVRowsMax) return fail(DS_EINVAL, "too many top-k rows");
     TopkParams p;
     std::memset(&p, 0, sizeof(p));
@@ -336,6 +338,7 @@ int run_topk(const ds_row_set_t* set, const float* scores, uint64_t stride, int3
         err = launch_topk_hist(p, stream, true);
         if (err != cudaSuccess) return cuda_fail(err, "top-k histogram launch");
     }
+    if (!select) return DS_OK;
     err = launch_topk_select(p, stream, true);
     return err == cudaSuccess ? DS_OK : cuda_fail(err, "top-k select launch");
 }
@@ -379,6 +382,24 @@ int run_tail(const ds_row_set_t* set, const ds_bf16* q_attn, const float* sinks,
     tp.rows = (uint32_t)set->rows;
     cudaError_t err = launch_decode_tail(tp, stream, true);
     return err == cudaSuccess ? DS_OK : cuda_fail(err, given ? "attention launch" : "decode select + attention launch");
+}
+
+// Best-first top-k of the set's rows into indices (+ offsets), after the
+// level-0 histogram (built here with with_hist, else already in the
+// workspace). Up to 8 rows: the decode's tail kernel in selection-only mode
+// (its placement by distributed ranking is faster than the top-k kernel's
+// leader-only sort); more: the top-k kernel.
+int run_select(const ds_row_set_t* set, const float* scores, uint64_t stride, int32_t* indices, uint8_t* ws,
+               const Layout& L, bool with_hist, cudaStream_t s, const int32_t* offsets = nullptr) {
+    uint32_t off[kVRowsMax];
+    for (int e = 0; e < set->rows; ++e) off[e] = set->table[e].index_offset;
+    if (set->rows > kRowsMax) return run_topk(set, scores, stride, indices, off, ws, L, with_hist, s, offsets);
+    if (with_hist) {
+        const int rc = run_topk(set, scores, stride, indices, off, ws, L, true, s, offsets, false);
+        if (rc) return rc;
+    }
+    return run_tail(set, nullptr, nullptr, 0, 1.0f, nullptr, nullptr, scores, stride, nullptr, indices, ws, L, s,
+                    false, false, offsets);
 }
 
 int check_attn_args(const ds_bf16* q_attn, const float* sinks, size_t sinks_row_stride, float scale, ds_bf16* out) {
@@ -531,9 +552,7 @@ int ds_rows_topk(const ds_row_set_t* set, const float* scores, size_t score_stri
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t err = launch_clear(reinterpret_cast<uint32_t*>(ws), (uint32_t)(L.ctl_end / 4), s);
     if (err != cudaSuccess) return cuda_fail(err, "workspace clear");
-    uint32_t off[DS_ROWS_MAX];
-    for (int e = 0; e < set->rows; ++e) off[e] = set->table[e].index_offset;
-    return run_topk(set, scores, score_stride, indices, off, ws, L, true, s);
+    return run_select(set, scores, score_stride, indices, ws, L, true, s);
 }
 
 int ds_rows_sparse_attn(const ds_row_set_t* set, const ds_bf16* q_attn, const float* sinks,
@@ -725,9 +744,7 @@ int ds_rows_topk_static(const ds_row_set_t* set, const float* scores, size_t sco
     // the histograms before they are rebuilt.
     cudaError_t err = launch_clear(reinterpret_cast<uint32_t*>(ws), (uint32_t)(kStaticBytes / 4), s);
     if (err != cudaSuccess) return cuda_fail(err, "scratch clear");
-    uint32_t off[DS_ROWS_MAX];
-    for (int e = 0; e < set->rows; ++e) off[e] = set->table[e].index_offset;
-    return run_topk(set, scores, score_stride, indices, off, ws, L, true, s);
+    return run_select(set, scores, score_stride, indices, ws, L, true, s);
 }
 
 size_t ds_rows_indexer_topk_queries_workspace_bytes(int rows, const ds_indexer_row_t* table, uint32_t query_len) {
@@ -751,7 +768,7 @@ int ds_rows_indexer_topk_queries(int rows, const ds_indexer_row_t* table, uint32
     if (!indices) return fail(DS_EINVAL, "indices is NULL");
     const int vrows = rows * (int)query_len;
     ds_row_t keys_tab[DS_ROWS_MAX], sel_tab[DS_INDEX_VROWS_MAX];
-    uint32_t valid[DS_INDEX_VROWS_MAX], out_off[DS_INDEX_VROWS_MAX];
+    uint32_t valid[DS_INDEX_VROWS_MAX];
     int32_t offsets[DS_INDEX_VROWS_MAX];
     indexer_selection_table(rows, table, query_len, sel_tab);
     for (int e = 0; e < rows; ++e) {
@@ -761,7 +778,6 @@ int ds_rows_indexer_topk_queries(int rows, const ds_indexer_row_t* table, uint32
     }
     for (int v = 0; v < vrows; ++v) {
         valid[v] = sel_tab[v].kv_len;
-        out_off[v] = sel_tab[v].index_offset;
         offsets[v] = table[v / query_len].offset;
     }
     const Layout L = make_layout(vrows, sel_tab, false);
@@ -778,13 +794,8 @@ int ds_rows_indexer_topk_queries(int rows, const ds_indexer_row_t* table, uint32
                      reinterpret_cast<uint32_t*>(ws + L.hist), reinterpret_cast<uint32_t*>(ws + L.status), s, 1,
                      valid);
     if (rc) return rc;
-    // The indexer built the level-0 histogram of each query's valid scores. One
-    // query per row: the decode's selection (the tail kernel, selection only),
-    // which places the winners by distributed ranking; else the top-k kernel.
-    if (query_len == 1)
-        return run_tail(&sset, nullptr, nullptr, 0, 1.0f, nullptr, nullptr, scores, L.score_stride, nullptr, indices,
-                        ws, L, s, false, false, offsets);
-    return run_topk(&sset, scores, L.score_stride, indices, out_off, ws, L, false, s, offsets);
+    // The indexer built the level-0 histogram of each query's valid scores.
+    return run_select(&sset, scores, L.score_stride, indices, ws, L, false, s, offsets);
 }
 
 int ds_rows_indexer_topk(int rows, const ds_indexer_row_t* table, const ds_bf16* const* index_keys,
