@@ -234,6 +234,49 @@ int check_workspace(const ds_row_set_t* set, void* ws, size_t bytes, const Layou
 // launch (the clear kernel), so every input is complete and the key stream may
 // start before the programmatic wait; 2 when the previous kernel writes the
 // query and weights; 0 when it may write anything.
+// Split `grid` CTAs over `segs` segments of tiles (segment s: tiles
+// [tile_begin[s], tile_begin[s+1]), the last one up to `tiles`) in proportion to
+// their tiles, every nonempty segment at least one CTA and none more CTAs than
+// tiles; cta_begin[s] is the first CTA of segment s, cta_begin[segs] = grid.
+// grid <= tiles, and grid >= the nonempty segments (grid = min(tiles, SMs)).
+void split_ctas(const uint32_t* tile_begin, uint32_t* cta_begin, uint32_t segs, uint32_t tiles, uint32_t grid) {
+    uint32_t ts[kSegMax], n[kSegMax];
+    double rem[kSegMax];
+    uint32_t used = 0;
+    for (uint32_t s = 0; s < segs; ++s) {
+        ts[s] = (s + 1 < segs ? tile_begin[s + 1] : tiles) - tile_begin[s];
+        const double want = tiles ? (double)grid * ts[s] / tiles : 0.0;
+        n[s] = (uint32_t)want;
+        if (ts[s] > 0 && n[s] == 0) n[s] = 1;
+        if (n[s] > ts[s]) n[s] = ts[s];
+        rem[s] = want - n[s];
+        used += n[s];
+    }
+    while (used > grid) {  // the minimum of one CTA took too many: shrink the largest
+        uint32_t best = 0;
+        for (uint32_t s = 1; s < segs; ++s)
+            if (n[s] > n[best]) best = s;
+        --n[best];
+        rem[best] += 1.0;
+        --used;
+    }
+    while (used < grid) {  // largest remainders first
+        int best = -1;
+        for (uint32_t s = 0; s < segs; ++s)
+            if (n[s] < ts[s] && (best < 0 || rem[s] > rem[best])) best = (int)s;
+        if (best < 0) break;
+        ++n[best];
+        rem[best] -= 1.0;
+        ++used;
+    }
+    uint32_t c = 0;
+    for (uint32_t s = 0; s < segs; ++s) {
+        cta_begin[s] = c;
+        c += n[s];
+    }
+    cta_begin[segs] = c;
+}
+
 template <class P>
 int fill_and_launch_indexer(P& p, int group, const ds_row_set_t* set, uint32_t query_len, const ds_bf16* q_index,
                             const float* w_index, float* scores, uint64_t stride, uint32_t* hist, uint32_t* status,
@@ -288,6 +331,7 @@ int fill_and_launch_indexer(P& p, int group, const ds_row_set_t* set, uint32_t q
     p.total_tiles = tiles;
     const int sms = num_sms();
     if (sms <= 0) return fail(DS_ECUDA, "no CUDA device");
+    if (group == 1) split_ctas(p.tile_begin, p.cta_begin, segs, tiles, tiles < (uint32_t)sms ? tiles : (uint32_t)sms);
     cudaError_t err = launch_indexer(p, sms, stream, true);
     return err == cudaSuccess ? DS_OK : cuda_fail(err, "indexer launch");
 }

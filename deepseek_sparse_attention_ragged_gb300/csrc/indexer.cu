@@ -4,7 +4,8 @@
 //
 // GB300 design. The work is a stream of 128-key tiles over all rows (a row's
 // tile t covers keys [128 t, 128 t + 128) of that row). A persistent CTA takes
-// every NB-th tile of the stream (one query per row) or a contiguous range. Per tile, one tcgen05.mma chain computes
+// every n-th tile of one row (one query per row: n CTAs per row, in proportion
+// to the row's tiles) or a contiguous range of the stream. Per tile, one tcgen05.mma chain computes
 // D[128 keys x 64 heads] = K_tile[128 x 128] * Q[64 x 128]^T into TMEM
 // (M=128, N=64, K=128 as 8 steps of 16). Operands sit in shared memory in the
 // 128-byte-swizzled K-major layout written by TMA. The epilogue gives each
@@ -154,16 +155,23 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
     const int lane = threadIdx.x & 31;
     const uint32_t NB = gridDim.x;
     const uint32_t T = p.total_tiles;
-    // This CTA's k-th tile. One query per entry: every NB-th tile, so all CTAs
-    // sweep the caches side by side and finish together (measured: 0.5 us
-    // faster than contiguous ranges, whose CTAs end up to 4 us apart). Grouped:
-    // a contiguous range, since its single query buffer reloads at every entry.
+    // This CTA's k-th tile. One query per entry: the CTAs are split over the
+    // entries in proportion to their tiles, and an entry's CTAs take every n-th
+    // of its tiles, so they sweep the cache side by side and finish together
+    // (contiguous ranges ended up to 4 us apart) while each CTA keeps one query
+    // and one histogram. Grouped: a contiguous range of the whole stream.
     const uint32_t g_begin = (uint32_t)(((uint64_t)blockIdx.x * T) / NB);
     const uint32_t g_end = (uint32_t)(((uint64_t)(blockIdx.x + 1) * T) / NB);
+    int my_seg = 0;
+    if (G == 1)
+        for (int i = 1; i < (int)p.segs; ++i)
+            if (blockIdx.x >= p.cta_begin[i]) my_seg = i;
+    const uint32_t seg_j = blockIdx.x - p.cta_begin[my_seg];
+    const uint32_t seg_n = p.cta_begin[my_seg + 1] - p.cta_begin[my_seg];
+    const uint32_t seg_end = my_seg + 1 < (int)p.segs ? p.tile_begin[my_seg + 1] : T;
     auto tile_of = [&](uint32_t k) -> uint32_t {
-        if (G == 1) return blockIdx.x + k * NB;
-        const uint32_t g = g_begin + k;
-        return g < g_end ? g : T;
+        const uint32_t g = G == 1 ? p.tile_begin[my_seg] + seg_j + k * seg_n : g_begin + k;
+        return g < (G == 1 ? seg_end : g_end) ? g : T;
     };
 
     // Inputs may still be in flight from the previous kernel (programmatic

@@ -37,6 +37,7 @@ struct IndexerParamsT {
     uint32_t vrows;
     uint32_t total_tiles;
     uint32_t tile_begin[SEGS];      // first 128-key tile of each segment
+    uint32_t cta_begin[SEGS + 1];   // one query per entry: the first CTA of each segment
     uint8_t seg_entry[SEGS];
     uint8_t seg_vrow[SEGS];         // the segment's first virtual row
     uint8_t seg_queries[SEGS];      // its virtual rows: 1..group
