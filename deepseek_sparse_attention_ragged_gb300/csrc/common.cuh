@@ -83,6 +83,43 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same, acquiring at cluster scope: what the arrivals of other CTAs of the
+// cluster released (their writes to this CTA's or global memory) is visible.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* status) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t start = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (global_timer_ns() - start > kWaitBudgetNs) {
+            if (status) atomicOr(status, kStatusWaitTimeout);
+            return false;
+        }
+    }
+}
+
+// Store `v` to the word at the same offset as `dst` in CTA `rank` of the
+// cluster, completing 4 bytes of transaction on that CTA's mbarrier at the same
+// offset as `bar`.
+__device__ __forceinline__ void st_async_remote(uint32_t* dst, uint32_t v, uint64_t* bar, uint32_t rank) {
+    uint32_t d, b;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_u32(dst)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(b) : "r"(smem_u32(bar)), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(d), "r"(v), "r"(b)
+                 : "memory");
+}
+
 // Wait for the phase of `parity` to complete, for at most kWaitBudgetNs.
 // Returns false (and records kStatusWaitTimeout) when the budget runs out.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {

@@ -18,8 +18,9 @@
 //      composite (score descending, lower index first): that rank is the
 //      winner's slot, both in the caller's best-first index list and in the
 //      attention, and the CTA stores the index into the shared memory of the
-//      two CTAs that own the slot. With indices given by the caller, each CTA
-//      reads its chunk's slots instead;
+//      two CTAs that own the slot (st.async, counted on the owner's mbarrier,
+//      so each CTA waits only for its own slots). With indices given by the
+//      caller, each CTA reads its chunk's slots instead;
 //   3. attend, on tcgen05 tensor cores with fp32 accumulators in TMEM: gather
 //      the chunk's 128 KV rows into the 128-byte-swizzled K-major layout, then
 //        logits  D[128 slots x 32 heads] = KV_chunk . Q_half^T   (K = 512,
@@ -130,6 +131,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t* nsel_s = reinterpret_cast<uint32_t*>(smem + T::misc);
     uint32_t* tmem_s = nsel_s + 1;
     uint64_t* mma_bar = reinterpret_cast<uint64_t*>(smem + T::misc + 8);
+    // This CTA's slots arrive (st.async, 4 bytes each) on slots_bar.
+    uint64_t* slots_bar = reinterpret_cast<uint64_t*>(smem + T::misc + 16);
     CombineSmem<kHalfHeads>& cs = *reinterpret_cast<CombineSmem<kHalfHeads>*>(smem + T::cs);
     float* sinks_s = reinterpret_cast<float*>(smem + T::sinks);
     SelectSmem& sm = *reinterpret_cast<SelectSmem*>(smem + T::select);
@@ -152,6 +155,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     if (t == 0) {
         sm.ncand = 0;
         mbar_init(mma_bar, kIssuers);
+        mbar_init(slots_bar, 1);
         fence_barrier_init();
     }
     if (warp == 0 && p.attend) {
@@ -198,6 +202,12 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
 
         // ---- place: rank 64 winners, store them in their slots -------------------
         const uint32_t nsel = *nsel_s;
+        if (t == 0) {
+            // The slots of this CTA's chunk that get a winner, 4 bytes each.
+            const uint32_t first = c * kChunkSlots;
+            const uint32_t n_here = nsel > first ? (nsel - first < kChunkSlots ? nsel - first : kChunkSlots) : 0u;
+            mbar_arrive_expect_tx(slots_bar, 4u * n_here);
+        }
         uint32_t* rk = reinterpret_cast<uint32_t*>(smem + T::ranks);
         if (t < 64) rk[t] = 0;
         // Slots of this chunk past the last winner are empty.
@@ -221,8 +231,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
                 if (out) out[pos] = j + p.offset[e];
                 if (p.attend) {
                     const uint32_t owner = 2 * (pos / kChunkSlots);
-                    cluster.map_shared_rank(idx_s, owner)[pos % kChunkSlots] = j;
-                    cluster.map_shared_rank(idx_s, owner + 1)[pos % kChunkSlots] = j;
+                    uint32_t* slot_word = reinterpret_cast<uint32_t*>(idx_s + pos % kChunkSlots);
+                    st_async_remote(slot_word, (uint32_t)j, slots_bar, owner);
+                    st_async_remote(slot_word, (uint32_t)j, slots_bar, owner + 1);
                 }
             } else if (out && k < W) {
                 out[k] = -1;
@@ -242,7 +253,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         }
         idx_s[t] = i;
     }
-    cluster.sync();  // every CTA's slots are in place
+    // Every slot of this CTA's chunk is in place: the winners placed by the
+    // cluster (decode) have arrived; the local writes are ordered by the barrier.
+    if (p.given == nullptr) mbar_wait_cluster(slots_bar, 0, p.status);
+    __syncthreads();
 
     // ---- attend: 128 slots x 32 heads on the tensor cores ------------------------
     const size_t part0_off = ((size_t)2 * p.chunk_begin[e] + (size_t)half * nchunks) * kPartFloats;
