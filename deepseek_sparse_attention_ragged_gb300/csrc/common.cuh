@@ -120,6 +120,15 @@ __device__ __forceinline__ void st_async_remote(uint32_t* dst, uint32_t v, uint6
                  : "memory");
 }
 
+// The same for an 8-byte value.
+__device__ __forceinline__ void st_async_remote_u64(uint64_t* dst, uint64_t v, uint64_t* bar, uint32_t rank) {
+    uint32_t d, b;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_u32(dst)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(b) : "r"(smem_u32(bar)), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(d), "l"(v), "r"(b)
+                 : "memory");
+}
+
 // Wait for the phase of `parity` to complete, for at most kWaitBudgetNs.
 // Returns false (and records kStatusWaitTimeout) when the budget runs out.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {

@@ -131,8 +131,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t* nsel_s = reinterpret_cast<uint32_t*>(smem + T::misc);
     uint32_t* tmem_s = nsel_s + 1;
     uint64_t* mma_bar = reinterpret_cast<uint64_t*>(smem + T::misc + 8);
-    // This CTA's slots arrive (st.async, 4 bytes each) on slots_bar.
+    // This CTA's slots arrive (st.async, 4 bytes each) on slots_bar, the
+    // leader's winners and their number (4,100 bytes) on winners_bar.
     uint64_t* slots_bar = reinterpret_cast<uint64_t*>(smem + T::misc + 16);
+    uint64_t* winners_bar = reinterpret_cast<uint64_t*>(smem + T::misc + 24);
     CombineSmem<kHalfHeads>& cs = *reinterpret_cast<CombineSmem<kHalfHeads>*>(smem + T::cs);
     float* sinks_s = reinterpret_cast<float*>(smem + T::sinks);
     SelectSmem& sm = *reinterpret_cast<SelectSmem*>(smem + T::select);
@@ -156,6 +158,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         sm.ncand = 0;
         mbar_init(mma_bar, kIssuers);
         mbar_init(slots_bar, 1);
+        mbar_init(winners_bar, 1);
         fence_barrier_init();
     }
     if (warp == 0 && p.attend) {
@@ -187,18 +190,20 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         const Collected col = select_collect(s, L, W, p.hist + (size_t)e * kHistBins, rank, sm, leader);
         cluster.sync();  // every append into the leader is visible to it
         uint64_t* sc = reinterpret_cast<uint64_t*>(smem + T::selcopy);
+        if (t == 0) mbar_arrive_expect_tx(winners_bar, kTopK * 8 + 4);
         if (rank == 0) {
             // The leader refines, then pushes the winners (zero past the last) and
-            // their number into every CTA's shared memory.
+            // their number into every CTA's shared memory (st.async on each CTA's
+            // winners_bar).
             const uint32_t n = select_finish(col, s, L, W, nullptr, sm, sel, p.status);
             const uint64_t wv = (uint32_t)t < n ? sel[t] : 0ull;
 #pragma unroll
             for (int r = 0; r < kCluster; ++r) {
-                cluster.map_shared_rank(sc, (unsigned)r)[t] = wv;
-                if (t == 0) *cluster.map_shared_rank(nsel_s, (unsigned)r) = n;
+                st_async_remote_u64(sc + t, wv, winners_bar, (uint32_t)r);
+                if (t == 0) st_async_remote(nsel_s, n, winners_bar, (uint32_t)r);
             }
         }
-        cluster.sync();  // the winners are visible to the cluster
+        mbar_wait_cluster(winners_bar, 0, p.status);  // the winners are here
 
         // ---- place: rank 64 winners, store them in their slots -------------------
         const uint32_t nsel = *nsel_s;
