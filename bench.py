@@ -31,7 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-INDEXER_DRAM_BYTES_8x131072 = 268_653_824 + 3_011_328
+INDEXER_DRAM_BYTES_8x131072 = 268_662_784 + 2_829_824
 CONFIG_INDEX = 3
 METRIC = "decode rows/s (8 rows, 128K ctx) and achieved HBM GB/s vs GB300 peak"
 
