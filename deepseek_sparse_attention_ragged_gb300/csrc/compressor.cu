@@ -78,6 +78,9 @@ __global__ void __cluster_dims__(kCompCluster, 1, 1) __launch_bounds__(kCompThre
     float* scs = p.score_state[row];
 
     pdl_wait();  // inputs and states may come from the previous kernel
+    // The next kernel may start launching; it waits for this grid to complete
+    // before it reads anything (griddepcontrol.wait).
+    pdl_trigger();
 
     // ---- 1. the token's state row, for this column's features ----------------
     if (active && sub < coff) {
