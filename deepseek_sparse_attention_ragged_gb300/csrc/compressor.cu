@@ -21,7 +21,8 @@
 // its whole share of the window in flight. Each thread owns its features in
 // every state row, so the token write, the pooling and the shift need no
 // barrier beyond the block's; the RMS sum and the fail-closed flags cross the
-// cluster through distributed shared memory in rank order.
+// cluster as st.async pushes into every CTA (counted on mbarriers) and are
+// added in rank order.
 
 #include <cooperative_groups.h>
 
@@ -45,12 +46,15 @@ __device__ __forceinline__ float comp(const float4& v, int k) {
 }
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
-struct CompSmem {
+struct __align__(8) CompSmem {
+    uint64_t bar_sq;           // the cluster's shares arrive here (st.async)
+    uint64_t bar_yb;           // ... and their output flags
     float col_sq[kSplit];      // per float4 column: sum of c^2
     uint32_t col_bad[kSplit];
-    float cta_sq;              // this CTA's share, read by the cluster
-    uint32_t cta_bad;
     uint32_t cta_ybad;
+    uint32_t sq_all[kCompCluster];   // every CTA's sum of c^2 (fp32 bits), by rank
+    uint32_t bad_all[kCompCluster];  // every CTA's bad flag, by rank
+    uint32_t yb_all[kCompCluster];   // every CTA's output flag, by rank
 };
 
 }  // namespace
@@ -77,6 +81,14 @@ __global__ void __cluster_dims__(kCompCluster, 1, 1) __launch_bounds__(kCompThre
     float* kvs = p.kv_state[row];
     float* scs = p.score_state[row];
 
+    // The exchange barriers, visible to the cluster before any CTA stores into
+    // another (this overlaps the previous kernel).
+    if (t == 0) {
+        mbar_init(&sm.bar_sq, 1);
+        mbar_init(&sm.bar_yb, 1);
+        fence_barrier_init();
+    }
+    cluster.sync();
     pdl_wait();  // inputs and states may come from the previous kernel
     // The next kernel may start launching; it waits for this grid to complete
     // before it reads anything (griddepcontrol.wait).
@@ -180,15 +192,20 @@ __global__ void __cluster_dims__(kCompCluster, 1, 1) __launch_bounds__(kCompThre
             s += sm.col_sq[j];
             b |= sm.col_bad[j];
         }
-        sm.cta_sq = s;
-        sm.cta_bad = b;
+        // Push this CTA's share into every CTA (itself too): 8 bytes each, counted
+        // on the receiver's bar_sq, which expects 8 bytes from every rank.
+        mbar_arrive_expect_tx(&sm.bar_sq, 8 * kCompCluster);
+        for (int r = 0; r < kCompCluster; ++r) {
+            st_async_remote(&sm.sq_all[rank], __float_as_uint(s), &sm.bar_sq, (uint32_t)r);
+            st_async_remote(&sm.bad_all[rank], b, &sm.bar_sq, (uint32_t)r);
+        }
     }
-    cluster.sync();
+    mbar_wait_cluster(&sm.bar_sq, 0, nullptr);
     float total = 0.0f;
     uint32_t any_bad = 0;
-    for (int r = 0; r < kCompCluster; ++r) {
-        total += cluster.map_shared_rank(&sm, (unsigned)r)->cta_sq;
-        any_bad |= cluster.map_shared_rank(&sm, (unsigned)r)->cta_bad;
+    for (int r = 0; r < kCompCluster; ++r) {  // rank order
+        total += __uint_as_float(sm.sq_all[r]);
+        any_bad |= sm.bad_all[r];
     }
     bool invalid = any_bad != 0 || !finite_f(total);
     const float scale = invalid ? 0.0f : 1.0f / sqrtf(total / (float)D + p.eps);
@@ -203,8 +220,13 @@ __global__ void __cluster_dims__(kCompCluster, 1, 1) __launch_bounds__(kCompThre
     if (t == 0) sm.cta_ybad = 0;
     __syncthreads();
     if (active && sub == 0 && ybad) atomicOr(&sm.cta_ybad, 1u);
-    cluster.sync();
-    for (int r = 0; r < kCompCluster; ++r) invalid = invalid || cluster.map_shared_rank(&sm, (unsigned)r)->cta_ybad;
+    __syncthreads();
+    if (t == 0) {
+        mbar_arrive_expect_tx(&sm.bar_yb, 4 * kCompCluster);
+        for (int r = 0; r < kCompCluster; ++r) st_async_remote(&sm.yb_all[rank], sm.cta_ybad, &sm.bar_yb, (uint32_t)r);
+    }
+    mbar_wait_cluster(&sm.bar_yb, 0, nullptr);
+    for (int r = 0; r < kCompCluster; ++r) invalid = invalid || sm.yb_all[r];
 
     if (active && sub == 0) {
         __align__(8) __nv_bfloat16 o[4];
@@ -220,7 +242,8 @@ __global__ void __cluster_dims__(kCompCluster, 1, 1) __launch_bounds__(kCompThre
         st4(kvs + dst, ld4(kvs + src));
         st4(scs + dst, ld4(scs + src));
     }
-    cluster.sync();  // no CTA leaves while the others may still read its shared memory
+    // No CTA reads another's shared memory, and every store into this CTA's
+    // has landed (both barriers completed): the CTAs leave independently.
 }
 
 cudaError_t launch_compressor(const CompressorParams& p, cudaStream_t stream, bool pdl) {
