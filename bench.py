@@ -131,11 +131,12 @@ import numpy as np, oracle, workloads
 wl = workloads.config({cfg})
 budget = {budget}
 t0 = time.perf_counter(); rows = 0
-for e in range(wl.num_rows):
-    oracle.decode(wl, entries=[e]); rows += 1
+while True:
+    oracle.decode(wl, entries=[rows % wl.num_rows]); rows += 1
     if time.perf_counter() - t0 > budget: break
 dt = time.perf_counter() - t0
-print(json.dumps({{"rows": rows, "seconds": dt}}))
+print(json.dumps({{"rows": rows, "distinct": min(rows, wl.num_rows), "of": wl.num_rows,
+                  "kv_lens": sorted({{int(r.kv_len) for r in wl.rows}}), "seconds": dt}}))
 """
 
 
@@ -150,8 +151,9 @@ def cpu_baseline(cfg: int, budget_s: float = 12.0):
         return {"value": None, "unit": "rows/s", "cores": 1, "kind": "oracle", "error": r.stderr[-300:]}
     d = json.loads(r.stdout.strip().splitlines()[-1])
     return {"value": d["rows"] / d["seconds"], "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": f"{d['rows']} of the 8 rows (131072 keys each), numpy float64 oracle, "
-                      f"single-threaded BLAS, {d['seconds']:.1f} s"}
+            "sample": f"{d['rows']} row decodes cycling over {d['distinct']} of the {d['of']} rows "
+                      f"(kv_len {'/'.join(map(str, d['kv_lens']))}), numpy float64 oracle, single-threaded BLAS, "
+                      f"{d['seconds']:.1f} s"}
 
 
 def run_reference(args):
