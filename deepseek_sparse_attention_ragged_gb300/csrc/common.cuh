@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "dsrows.h"
@@ -323,6 +324,21 @@ inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block
     cfg.attrs = pdl ? attr : nullptr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device. The attribute belongs to the device's context, so it is set once per
+// device (bit d of `done`); threads that race here only repeat the same call.
+template <typename... KArgs>
+inline cudaError_t set_smem_limit_once(void (*kernel)(KArgs...), size_t bytes, std::atomic<uint64_t>& done) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t)1 << dev : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (err == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return err;
 }
 
 // Programmatic dependent launch controls (no-ops for a launch without PDL).

@@ -411,13 +411,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
 size_t decode_tail_smem_bytes() { return kTailSmem; }
 
 cudaError_t launch_decode_tail(const TailParams& p, cudaStream_t stream, bool pdl) {
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t err =
-            cudaFuncSetAttribute(decode_tail_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTailSmem);
-        if (err != cudaSuccess) return err;
-        configured = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    const cudaError_t err = set_smem_limit_once(decode_tail_kernel, kTailSmem, smem_set);
+    if (err != cudaSuccess) return err;
     if (p.rows == 0) return cudaSuccess;
     return launch_kernel(decode_tail_kernel, dim3(p.rows * kCluster), dim3(kThreads), kTailSmem, stream, pdl, p);
 }

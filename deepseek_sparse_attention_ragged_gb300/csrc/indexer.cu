@@ -456,13 +456,10 @@ __global__ void __launch_bounds__(Shape<kIndexerGroup>::kThreads, 1)
 
 template <int G, class K>
 static cudaError_t launch_group(K kernel, const ParamsOf<G>& p, int num_sms, cudaStream_t stream, bool pdl) {
-    static bool configured = false;
+    static std::atomic<uint64_t> smem_set{0};
     constexpr size_t bytes = smem_bytes<G>();
-    if (!configured) {
-        cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-        if (err != cudaSuccess) return err;
-        configured = true;
-    }
+    const cudaError_t err = set_smem_limit_once(kernel, bytes, smem_set);
+    if (err != cudaSuccess) return err;
     const uint32_t grid = p.total_tiles < (uint32_t)num_sms ? p.total_tiles : (uint32_t)num_sms;
     return launch_kernel(kernel, dim3(grid), dim3(Shape<G>::kThreads), bytes, stream, pdl, p);
 }

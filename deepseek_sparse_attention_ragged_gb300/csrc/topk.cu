@@ -110,13 +110,9 @@ cudaError_t launch_topk_hist(const TopkParams& p, cudaStream_t stream, bool pdl)
 }
 
 cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t stream, bool pdl) {
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t err = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)kSelectSmemBytes);
-        if (err != cudaSuccess) return err;
-        configured = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    const cudaError_t err = set_smem_limit_once(topk_select_kernel, kSelectSmemBytes, smem_set);
+    if (err != cudaSuccess) return err;
     return launch_kernel(topk_select_kernel, dim3(p.rows * kCluster), dim3(kThreads), kSelectSmemBytes, stream,
                          pdl, p);
 }
