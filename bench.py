@@ -64,6 +64,93 @@ def peaks():
     return 6800.0, "fallback"
 
 
+REASON_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+def clock_summary(samples, source):
+    """Median SM clock under load, the maximum SM clock and every clock-event
+    reason seen, from (sm_mhz, max_mhz, reasons) samples."""
+    if not samples:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": source}
+    reasons = set()
+    for _, _, r in samples:
+        reasons |= set(r)
+    return {"sm_mhz": statistics.median(x[0] for x in samples), "sm_max_mhz": max(x[1] for x in samples),
+            "reasons": sorted(reasons), "samples": len(samples), "source": source}
+
+
+class NvmlClockSampler:
+    """SM clock and clock-event reasons read through NVML (read-only queries)
+    every `period_s` seconds by a thread while the timed region runs."""
+
+    # nvmlClocksEventReason* bits
+    BITS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
+
+    def __init__(self, device, period_s: float = 0.002, lib=None):
+        import ctypes
+        self.ct = ctypes
+        self.period_s = period_s
+        self.samples = []
+        self.stop = threading.Event()
+        self.nvml = lib if lib is not None else ctypes.CDLL("libnvidia-ml.so.1")
+        if self.nvml.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.handle = self._handle(device)
+        self.max_mhz = self._clock(self.nvml.nvmlDeviceGetMaxClockInfo)
+        fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = fn if fn is not None else self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _handle(self, device):
+        ct, h = self.ct, self.ct.c_void_p()
+        uuid = None
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            pass
+        if uuid:
+            for u in (uuid, "GPU-" + uuid):
+                if self.nvml.nvmlDeviceGetHandleByUUID(ct.c_char_p(u.encode()), ct.byref(h)) == 0:
+                    return h
+        index = device.index if getattr(device, "index", None) is not None else 0
+        if self.nvml.nvmlDeviceGetHandleByIndex_v2(ct.c_uint(index), ct.byref(h)) != 0:
+            raise OSError("no NVML handle for the device")
+        return h
+
+    def _clock(self, fn):
+        v = self.ct.c_uint()
+        if fn(self.handle, self.ct.c_int(1), self.ct.byref(v)) != 0:  # NVML_CLOCK_SM
+            raise OSError("NVML clock query failed")
+        return float(v.value)
+
+    def _sample(self):
+        r = self.ct.c_ulonglong()
+        bits = r.value if self.reasons_fn(self.handle, self.ct.byref(r)) == 0 else 0
+        sm = self._clock(self.nvml.nvmlDeviceGetClockInfo)
+        self.samples.append((sm, self.max_mhz, [n for b, n in self.BITS.items() if bits & b]))
+
+    def _run(self):
+        while not self.stop.is_set():
+            try:
+                self._sample()
+            except OSError:
+                return
+            self.stop.wait(self.period_s)
+
+    def __enter__(self):
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        self.stop.set()
+        self.thread.join(timeout=5)
+        self.nvml.nvmlShutdown()
+
+    def summary(self):
+        return clock_summary(self.samples, "nvml")
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
 
@@ -99,25 +186,25 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx = [], []
-        reasons = set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        samples = []
         for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 6:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                sm, mx = float(parts[0]), float(parts[1])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[2:6]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+            samples.append((sm, mx, [n for n, v in zip(REASON_NAMES, parts[2:6]) if v.lower() == "active"]))
+        return clock_summary(samples, "nvidia-smi")
+
+
+def clock_sampler(device):
+    """NVML polling (every 2 ms) when the library loads, else nvidia-smi (every 100 ms)."""
+    try:
+        return NvmlClockSampler(device)
+    except (OSError, AttributeError):
+        return ClockSampler(device.index or 0)
 
 
 # ---------------------------------------------------------------------------
@@ -390,7 +477,7 @@ def main():
     # are far larger than L2, and the queries rotate, so no flush is needed.
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(device.index or 0) as clocks:
+    with clock_sampler(device) as clocks:
         barrier()
         with torch.cuda.stream(stream):
             t_start.record(stream)
