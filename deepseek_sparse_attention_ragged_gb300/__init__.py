@@ -28,6 +28,7 @@ __all__ = [
     "IndexerRow", "ds_rows_indexer_topk_workspace_bytes", "indexer_topk_workspace", "ds_rows_indexer_topk",
     "ds_rows_indexer_topk_queries_workspace_bytes", "ds_rows_indexer_topk_queries",
     "CompressorRow", "ds_rows_compress_kv",
+    "STATUS_WAIT_TIMEOUT", "STATUS_OVERFLOW", "workspace_status", "ds_rows_selftest_bounded_wait",
     "ROWS_MAX", "INDEX_HEADS", "INDEX_DIM", "TOP_K", "HEADS", "DIM",
 ]
 
@@ -39,6 +40,8 @@ HEADS = 64
 DIM = 512
 
 DS_OK = 0
+STATUS_WAIT_TIMEOUT = 1  # DS_STATUS_WAIT_TIMEOUT: a bounded device wait gave up
+STATUS_OVERFLOW = 2      # DS_STATUS_OVERFLOW: an internal selection check failed
 
 
 class DsRowsError(RuntimeError):
@@ -126,6 +129,8 @@ def load():
     lib.ds_rows_compress_kv.argtypes = [i32, ctypes.POINTER(CompressorRow), vp, vp, vp, vp, ctypes.c_uint32,
                                          ctypes.c_uint32, ctypes.c_float, vp, vp]
     lib.ds_rows_compress_kv.restype = i32
+    lib.ds_rows_selftest_bounded_wait.argtypes = [vp, vp, ctypes.c_uint64, vp]
+    lib.ds_rows_selftest_bounded_wait.restype = i32
     lib.ds_rows_last_error.argtypes = []
     lib.ds_rows_last_error.restype = ctypes.c_char_p
     lib.ds_rows_version.argtypes = []
@@ -236,6 +241,29 @@ def workspace(rows, device=None) -> torch.Tensor:
     """A workspace tensor (uint8, 256-byte aligned by the caching allocator)."""
     return torch.empty(ds_rows_workspace_bytes(rows), dtype=torch.uint8,
                        device=device if device is not None else "cuda")
+
+
+def workspace_status(workspace_t: torch.Tensor) -> int:
+    """The device status word at the head of a workspace (the STATUS_* bits of
+    the last call that used it). Reads 4 bytes back to the host, so it waits
+    for the work queued on the workspace's device."""
+    if workspace_t.dtype != torch.uint8 or workspace_t.numel() < 4:
+        raise DsRowsError(-1, "workspace_status: a uint8 workspace tensor is required")
+    return int(workspace_t[:4].view(torch.int32).item()) & 0xFFFFFFFF
+
+
+def ds_rows_selftest_bounded_wait(budget_ns: int = 1_000_000, device=None, stream=None):
+    """Run the library's bounded mbarrier wait on a phase that completes and on
+    one that nothing completes (giving up after budget_ns); returns
+    (status, completed_wait_ok, abandoned_wait_gave_up)."""
+    lib = load()
+    dev = torch.device(device if device is not None else "cuda")
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    result = torch.full((2,), 7, dtype=torch.int32, device=dev)
+    _check(lib, lib.ds_rows_selftest_bounded_wait(status.data_ptr(), result.data_ptr(), int(budget_ns),
+                                                  _stream(stream)))
+    r = result.cpu().tolist()
+    return int(status.item()) & 0xFFFFFFFF, r[0] == 1, r[1] == 1
 
 
 def ds_rows_indexer_score(rows, q_index, w_index, index_keys, scores, score_stride=None, stream=None):

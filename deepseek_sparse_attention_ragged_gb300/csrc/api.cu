@@ -902,6 +902,14 @@ int ds_rows_compress_kv(int rows, const ds_compressor_row_t* table, const float*
     return err == cudaSuccess ? DS_OK : cuda_fail(err, "compressor launch");
 }
 
+int ds_rows_selftest_bounded_wait(uint32_t* status, uint32_t* result, uint64_t budget_ns, void* stream) {
+    if (!status || !result) return fail(DS_EINVAL, "status and result must be non-NULL");
+    if (budget_ns < 1000ull || budget_ns > 10000000000ull)
+        return fail(DS_EINVAL, "budget_ns must be 1e3..1e10, got %llu", (unsigned long long)budget_ns);
+    const cudaError_t err = launch_wait_selftest(status, result, budget_ns, (cudaStream_t)stream);
+    return err == cudaSuccess ? DS_OK : cuda_fail(err, "bounded-wait self-test launch");
+}
+
 const char* ds_rows_last_error(void) { return g_error.c_str(); }
 
 const char* ds_rows_version(void) { return "dsrows 0.1.0 (sm_103a)"; }

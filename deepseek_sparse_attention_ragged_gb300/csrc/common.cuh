@@ -21,8 +21,8 @@ constexpr int kHeads = DS_HEADS;
 constexpr int kDim = DS_DIM;
 
 // Device-side status bits written into the workspace control header.
-constexpr uint32_t kStatusWaitTimeout = 1u;      // a bounded wait gave up
-constexpr uint32_t kStatusCandOverflow = 2u;     // internal: candidate buffer clipped
+constexpr uint32_t kStatusWaitTimeout = DS_STATUS_WAIT_TIMEOUT;  // a bounded wait gave up
+constexpr uint32_t kStatusCandOverflow = DS_STATUS_OVERFLOW;      // internal: counts disagreed
 
 // Time budget of every spin-wait on an mbarrier (nanoseconds of %globaltimer).
 constexpr uint64_t kWaitBudgetNs = 2000000000ull;
@@ -130,14 +130,15 @@ __device__ __forceinline__ void st_async_remote_u64(uint64_t* dst, uint64_t v, u
                  : "memory");
 }
 
-// Wait for the phase of `parity` to complete, for at most kWaitBudgetNs.
+// Wait for the phase of `parity` to complete, for at most `budget_ns`.
 // Returns false (and records kStatusWaitTimeout) when the budget runs out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                          uint64_t budget_ns = kWaitBudgetNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t start = global_timer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_timer_ns() - start > kWaitBudgetNs) {
+        if (global_timer_ns() - start > budget_ns) {
             if (status) atomicOr(status, kStatusWaitTimeout);
             return false;
         }

@@ -129,6 +129,10 @@ cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t stream, bool pd
 
 // Zero `words` 32-bit words (the workspace control region); an ordinary launch.
 cudaError_t launch_clear(uint32_t* p, uint32_t words, cudaStream_t stream);
+
+// The bounded-wait self-test (one CTA): result[0] = a completed wait succeeded,
+// result[1] = a wait on a phase nothing completes gave up after budget_ns.
+cudaError_t launch_wait_selftest(uint32_t* status, uint32_t* result, uint64_t budget_ns, cudaStream_t stream);
 // The same, and copies a_bytes and b_bytes (multiples of 16; 16-byte aligned)
 // from a_src and b_src to a_dst and b_dst before it completes.
 cudaError_t launch_clear_copy(uint32_t* p, uint32_t words, const void* a_src, void* a_dst, size_t a_bytes,

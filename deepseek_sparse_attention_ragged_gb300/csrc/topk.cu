@@ -126,6 +126,24 @@ cudaError_t launch_clear(uint32_t* p, uint32_t words, cudaStream_t stream) {
     return launch_kernel(clear_kernel, dim3(16), dim3(1024), 0, stream, false, p, words);
 }
 
+// The library's bounded mbarrier wait on two phases of a shared-memory barrier
+// with one expected arrival: phase 0, which this thread completes, and phase 1,
+// which nothing completes (the wait must give up after budget_ns).
+__global__ void wait_selftest_kernel(uint32_t* __restrict__ status, uint32_t* __restrict__ result,
+                                     uint64_t budget_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    mbar_arrive(&bar);
+    result[0] = mbar_wait(&bar, 0, status, budget_ns) ? 1u : 0u;
+    result[1] = mbar_wait(&bar, 1, status, budget_ns) ? 0u : 1u;
+}
+
+cudaError_t launch_wait_selftest(uint32_t* status, uint32_t* result, uint64_t budget_ns, cudaStream_t stream) {
+    return launch_kernel(wait_selftest_kernel, dim3(1), dim3(32), 0, stream, false, status, result, budget_ns);
+}
+
 // clear_kernel plus two 16-byte-granular copies (the indexer's query and head
 // weights, from pinned host memory into device staging). The next kernel may
 // start early; it waits for this one (griddepcontrol.wait) before it reads

@@ -90,6 +90,23 @@ typedef struct {
 } ds_row_set_t;
 
 /*
+ * Device status. The first 4 bytes of a workspace hold a uint32 status word.
+ * Every call that takes a workspace zeroes it when it starts, and its kernels
+ * OR these bits into it:
+ *   DS_STATUS_WAIT_TIMEOUT  a bounded device-side wait (2 s of %globaltimer)
+ *                           gave up; the kernel unwound without finishing and
+ *                           the call's outputs are not valid.
+ *   DS_STATUS_OVERFLOW      an internal consistency check of the selection
+ *                           failed (candidate counts disagreed); its indices
+ *                           may be incomplete. Not expected in any input.
+ * Read the word once the call has completed (for example a 4-byte
+ * cudaMemcpyAsync on the same stream); the next call on the workspace clears
+ * it. 0: neither happened. ds_rows_topk_static keeps its word internally.
+ */
+#define DS_STATUS_WAIT_TIMEOUT 1u
+#define DS_STATUS_OVERFLOW 2u
+
+/*
  * Workspace bytes that every entry point below needs for this row table
  * (the largest need over the entry points). 0 when the table is invalid
  * (see ds_rows_last_error). The workspace must be 256-byte aligned; its
@@ -331,6 +348,20 @@ typedef struct {
 int ds_rows_compress_kv(int rows, const ds_compressor_row_t* table, const float* kv, const float* score,
                         const float* ape, const float* norm, uint32_t ratio, uint32_t head_dim,
                         float epsilon, ds_bf16* out, void* stream);
+
+/*
+ * Self-test of the device-side failure detection, on the current device. One
+ * CTA runs the library's bounded mbarrier wait twice on a shared-memory
+ * barrier: on a phase that completes, and on a phase that nothing completes,
+ * each with a budget of `budget_ns` nanoseconds of %globaltimer (1,000 to
+ * 10,000,000,000). It writes result[0] = 1 if the first wait succeeded and
+ * result[1] = 1 if the second gave up, and ORs DS_STATUS_WAIT_TIMEOUT into
+ * *status when it gives up, as the library's kernels do. Nothing faults and
+ * the device stays usable. Takes about budget_ns on the GPU.
+ *   status   device uint32 (zeroed by the caller beforehand)
+ *   result   device uint32 [2]
+ */
+int ds_rows_selftest_bounded_wait(uint32_t* status, uint32_t* result, uint64_t budget_ns, void* stream);
 
 /* Message of the last failed call on this host thread ("" if none). */
 const char* ds_rows_last_error(void);

@@ -291,3 +291,20 @@ def test_compressor_argument_checks(lib):
     assert _compress(lib, [ok_row, (FAKE + STATE, FAKE + 2 * STATE, 3)]) == -1 and "overlap" in _err(lib)
     assert _compress(lib, [ok_row, (FAKE + 2 * STATE, FAKE + 3 * STATE, 3)]) != -1 or "overlap" not in _err(lib)
     assert _compress(lib, [(FAKE, FAKE + STATE, 3)] * 9) == -1 and "rows must be 1..=8" in _err(lib)
+
+
+def test_selftest_bounded_wait_validation(lib):
+    # Rejected on the host: nothing is launched.
+    assert lib.ds_rows_selftest_bounded_wait(None, FAKE, 1_000_000, None) == -1
+    assert "non-NULL" in _err(lib)
+    assert lib.ds_rows_selftest_bounded_wait(FAKE, None, 1_000_000, None) == -1
+    assert lib.ds_rows_selftest_bounded_wait(FAKE, FAKE, 999, None) == -1
+    assert "budget_ns" in _err(lib)
+    assert lib.ds_rows_selftest_bounded_wait(FAKE, FAKE, 10_000_000_001, None) == -1
+
+
+def test_status_bits_match_the_binding():
+    text = open(HEADER).read()
+    assert re.search(r"#define DS_STATUS_WAIT_TIMEOUT 1u", text)
+    assert re.search(r"#define DS_STATUS_OVERFLOW 2u", text)
+    assert ds.STATUS_WAIT_TIMEOUT == 1 and ds.STATUS_OVERFLOW == 2
