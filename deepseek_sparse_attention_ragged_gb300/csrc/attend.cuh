@@ -53,12 +53,12 @@ struct CombineSmem {
 // Combine feature columns [f0, f0 + F) of H heads over the n chunk partials of
 // one row (or head half) with NT threads (thread -> one head, F H / NT
 // features). A partial is m[H], l[H], acc[H][512] (fp32), `stride` floats apart
-// from part0; flags[h] marks a head with a non-finite logit, row_bad the whole
-// row; the heads' outputs start at out (rows of 512 bf16), and invalid
+// from part0; flags[h] marks a head with a non-finite logit, *row_flag the
+// whole row; the heads' outputs start at out (rows of 512 bf16), and invalid
 // (optional) receives each head's flag.
 template <int H, int NT, int F = 64>
 __device__ __forceinline__ void combine_slice(const float* part0, size_t stride, int n, int f0, const float* sinks,
-                                              bool row_bad, const uint32_t* flags, __nv_bfloat16* out,
+                                              const uint32_t* row_flag, const uint32_t* flags, __nv_bfloat16* out,
                                               uint32_t* invalid, CombineSmem<H>& cs) {
     constexpr int FPT = F * H / NT;  // features per thread
     static_assert(FPT == 4 || FPT == 8, "4 or 8 features per thread");
@@ -75,6 +75,9 @@ __device__ __forceinline__ void combine_slice(const float* part0, size_t stride,
 #pragma unroll
             for (int u = 0; u < FPT / 4; ++u) v[c][u] = __ldcg(reinterpret_cast<const float4*>(src + 4 * u));
         }
+    // The flags travel with the partials' statistics: one round trip to L2.
+    uint32_t flagged = 0;
+    if (t < H) flagged = __ldcg(flags + t) | __ldcg(row_flag);
     if (t < n * H) {
         const int c = t / H, hh = t % H;
         cs.mc[c][hh] = __ldcg(part0 + (size_t)c * stride + hh);
@@ -82,7 +85,7 @@ __device__ __forceinline__ void combine_slice(const float* part0, size_t stride,
     }
     __syncthreads();
     if (t < H) {
-        bool b = row_bad || __ldcg(flags + t) != 0;
+        bool b = flagged != 0;
         cs.inv_den[t] = combine_factors(
             sinks[t], n, [&](int c) { return cs.mc[c][t]; }, [&](int c) { return cs.lc[c][t]; }, cs.fac[t], b);
         cs.bad[t] = b ? 1u : 0u;

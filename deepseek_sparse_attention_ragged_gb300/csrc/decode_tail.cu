@@ -393,10 +393,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
 
     // ---- combine: feature columns [128 c, 128 c + 128) of the 32 heads ----------
-    const bool row_bad = __ldcg(p.flags + kRowsMax * kHeads + e) != 0;
     combine_slice<kHalfHeads, kThreads, 128>(
         p.part + part0_off, kPartFloats, (int)nchunks, (int)(128 * c),
-        sinks_s, row_bad, p.flags + e * kHeads + head0,
+        sinks_s, p.flags + kRowsMax * kHeads + e, p.flags + e * kHeads + head0,
         p.out + ((size_t)q_row * kHeads + head0) * kDim,
         p.invalid && c == 0 ? p.invalid + (size_t)q_row * kHeads + head0 : nullptr, cs);
 
