@@ -48,12 +48,18 @@ class Dev:
     index = 0
 
 
+def _run(sampler, n=3, limit_s=5.0):
+    """Run the sampler until it has n samples (or limit_s passes)."""
+    t0 = time.perf_counter()
+    with sampler:
+        while len(sampler.samples) < n and time.perf_counter() - t0 < limit_s:
+            time.sleep(0.005)
+    return sampler.summary()
+
+
 def test_nvml_sampler_median_and_reasons():
     fake = FakeNvml([2070, 2070, 1980], 0x1 | 0x4)  # GPU idle (ignored) + SW power cap
-    s = bench.NvmlClockSampler(Dev(), period_s=0.001, lib=fake)
-    with s:
-        time.sleep(0.05)
-    out = s.summary()
+    out = _run(bench.NvmlClockSampler(Dev(), period_s=0.001, lib=fake))
     assert fake.shut
     assert out["samples"] >= 3 and out["source"] == "nvml"
     assert out["sm_max_mhz"] == 2070
@@ -63,10 +69,8 @@ def test_nvml_sampler_median_and_reasons():
 
 def test_nvml_sampler_throttle_bits():
     fake = FakeNvml([1200], 0x8 | 0x20 | 0x40)
-    s = bench.NvmlClockSampler(Dev(), period_s=0.001, lib=fake)
-    with s:
-        time.sleep(0.01)
-    assert s.summary()["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
+    out = _run(bench.NvmlClockSampler(Dev(), period_s=0.001, lib=fake), n=1)
+    assert out["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
 
 
 def test_nvidia_smi_parser_and_empty_summary():
