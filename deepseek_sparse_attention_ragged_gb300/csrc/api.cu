@@ -687,11 +687,10 @@ int ds_rows_decode_host(const ds_row_set_t* set, const ds_bf16* h_q_index, const
     const ds_bf16* m_qI = dense ? mapped_host(h_q_index) : nullptr;
     const float* m_wI = dense && aligned16(h_w_index) ? mapped_host(h_w_index) : nullptr;
     const bool kernel_copy = m_qI && m_wI;
-    if (kernel_copy) {
-    } else if (dense) {
+    if (!kernel_copy && dense) {
         rc = copy_async(d_qI, h_q_index, nq * qI_row * 2, h2d, s, "q_index copy");
         if (!rc) rc = copy_async(d_wI, h_w_index, nq * wI_row * 4, h2d, s, "w_index copy");
-    } else {
+    } else if (!kernel_copy) {
         for (int e = 0; e < set->rows && !rc; ++e) {
             const size_t r = set->table[e].q_row;
             rc = copy_async(d_qI + r * qI_row, h_q_index + r * qI_row, qI_row * 2, h2d, s, "q_index copy");
@@ -740,8 +739,9 @@ int ds_rows_decode_host(const ds_row_set_t* set, const ds_bf16* h_q_index, const
                     : launch_clear(reinterpret_cast<uint32_t*>(ws), (uint32_t)(L.ctl_end / 4), s);
     if (err != cudaSuccess) return cuda_fail(err, "workspace clear");
     float* scores = reinterpret_cast<float*>(ws + L.scores);
-    // With the kernel copy the indexer streams keys at once but waits for that
-    // kernel (griddepcontrol.wait) before it reads the query and weights.
+    // With the kernel copy the indexer launches early (programmatic dependent
+    // launch) and waits for that kernel (griddepcontrol.wait) before its first
+    // query and key loads and before it reads the head weights.
     rc = run_indexer(set, 1, d_qI, d_wI, scores, L.score_stride, reinterpret_cast<uint32_t*>(ws + L.hist),
                      reinterpret_cast<uint32_t*>(ws + L.status), s, kernel_copy ? 2u : 1u, nullptr, m_qA,
                      ws + S.q_attn, m_qA ? nq * qA_row * 2 : 0);

@@ -176,8 +176,9 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
 
     // Inputs may still be in flight from the previous kernel (programmatic
     // launch): then nothing is read before it completes. With inputs_ready 2
-    // only the query and head weights are: the keys stream from the start, the
-    // query and weight loads wait.
+    // only the query and head weights are: the CTA sets up at once, and the
+    // producer (before its first query load, ahead of the first key tile) and
+    // the epilogue (before the weights) wait.
     if (!p.inputs_ready) pdl_wait();
 
     // ---- setup -------------------------------------------------------------
