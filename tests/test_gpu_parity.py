@@ -339,3 +339,51 @@ def test_fail_closed_kv_and_keys():
     assert np.all(inv.cpu().numpy()[0] == 1)
     assert np.all(out[0].float().cpu().numpy() == 0)
     check_out(out[1].float().cpu().numpy(), ref[1]["out"], what="row 1")
+
+
+def test_decode_full_size_in_the_bench_launch_configuration():
+    """The bench's launch configuration on the full 8 x 131072 workload: four
+    consecutive decode steps (four query sets) captured in one CUDA graph on a
+    side stream and replayed. Every step's output and indices are bitwise those
+    of the same step run eagerly, and step 0 run eagerly is the decode that
+    test_decode checks against the oracle."""
+    wl, dev = cfg(3), cfg_dev(3)
+    qsets = [(dev.q_index, dev.w_index, dev.q_attn)]
+    for i in range(3):
+        qI, wI, qA = workloads.draw_queries(wl, 1000 + i)
+        qsets.append((bf16_tensor(qI, "cuda"), torch.from_numpy(wI).cuda(), bf16_tensor(qA, "cuda")))
+    n_idx = max(r.index_offset + r.width for r in dev.rows)
+    outs = [torch.full((8, 64, 512), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    idxs = [torch.full((n_idx,), -7, dtype=torch.int32, device="cuda") for _ in range(4)]
+    ws = ds.workspace(dev.rows)
+    s = torch.cuda.Stream()
+
+    def step(i):
+        qI, wI, qA = qsets[i]
+        ds.ds_rows_decode(dev.rows, qI, wI, dev.keys, qA, dev.kv, dev.sinks, dev.sinks_row_stride, dev.scale,
+                          outs[i], indices=idxs[i], workspace_t=ws, stream=s)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for i in range(4):
+            step(i)
+    s.synchronize()
+    eager = [(o.clone(), x.clone()) for o, x in zip(outs, idxs)]
+    for o, x in zip(outs, idxs):
+        o.fill_(float("nan"))
+        x.fill_(-7)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(4):
+            step(i)
+    with torch.cuda.stream(s):
+        g.replay()
+        g.replay()
+    s.synchronize()
+    for i in range(4):
+        assert torch.equal(outs[i].view(torch.int16), eager[i][0].view(torch.int16)), f"step {i} out"
+        assert torch.equal(idxs[i], eager[i][1]), f"step {i} indices"
+    ref0, idx0, _ = run_decode(dev)
+    assert torch.equal(ref0.view(torch.int16), eager[0][0].view(torch.int16))
+    assert torch.equal(idx0, eager[0][1])
