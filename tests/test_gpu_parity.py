@@ -84,21 +84,6 @@ def test_indexer_scores(i):
         assert np.isnan(got[e, r.kv_len:]).all(), "wrote past kv_len"
 
 
-def test_indexer_identical_keys_identical_scores():
-    """Exact duplicate keys at different tile positions give bitwise equal scores."""
-    wl = cfg(4)
-    dev = cfg_dev(4)
-    e = 7  # kv_len 262144, 64 prototypes
-    r = wl.rows[e]
-    scores = torch.empty((1, r.kv_len), dtype=torch.float32, device="cuda")
-    one = [workloads.Row(r.kv_len, r.width, 0, r.q_row)]
-    ds.ds_rows_indexer_score(one, dev.q_index, dev.w_index, [dev.keys[e]], scores, r.kv_len)
-    got = scores.cpu().numpy()[0]
-    keys = wl.keys[e]
-    _, first, inverse = np.unique(keys, axis=0, return_index=True, return_inverse=True)
-    np.testing.assert_array_equal(got, got[first][inverse.ravel()])
-
-
 # ---------------------------------------------------------------------------
 # (2) top-k on generated scores (bit-exact: fp32 inputs, exact comparisons)
 # ---------------------------------------------------------------------------
@@ -387,3 +372,30 @@ def test_decode_full_size_in_the_bench_launch_configuration():
     ref0, idx0, _ = run_decode(dev)
     assert torch.equal(ref0.view(torch.int16), eager[0][0].view(torch.int16))
     assert torch.equal(idx0, eager[0][1])
+
+
+def test_indexer_identical_keys_identical_scores():
+    """Copies of one key placed at other tiles, other lanes of a tile and in a
+    ragged last tile score bitwise the same: a key's score depends only on its
+    data and the query."""
+    wl = cfg(4)
+    dev = cfg_dev(4)
+    copies = {4: {0: [300, 133, 512]},                # kv_len 513: key 512 is alone in the last tile
+              6: {3: [130, 4097, 65535], 1000: [1, 20000, 65408], 40000: [129, 777, 60000]}}  # kv_len 65536
+    rows, keys = [], []
+    for n, (e, moves) in enumerate(copies.items()):
+        r = wl.rows[e]
+        k = wl.keys[e].copy()
+        for src, dsts in moves.items():
+            k[dsts] = k[src]
+        rows.append(workloads.Row(r.kv_len, r.width, 512 * n, r.q_row))
+        keys.append(bf16_tensor(k, "cuda"))
+    stride = max(r.kv_len for r in rows)
+    scores = torch.empty((len(rows), stride), dtype=torch.float32, device="cuda")
+    ds.ds_rows_indexer_score(rows, dev.q_index, dev.w_index, keys, scores, stride)
+    torch.cuda.synchronize()
+    got = scores.cpu().numpy().view(np.uint32)
+    for n, (e, moves) in enumerate(copies.items()):
+        for src, dsts in moves.items():
+            np.testing.assert_array_equal(got[n, dsts], np.full(len(dsts), got[n, src], dtype=np.uint32),
+                                          err_msg=f"row {e}, copies of key {src}")
