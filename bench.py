@@ -34,6 +34,7 @@ if ROOT not in sys.path:
 INDEXER_DRAM_BYTES_8x131072 = 268_662_784 + 2_829_824
 CONFIG_INDEX = 3
 METRIC = "decode rows/s (8 rows, 128K ctx) and achieved HBM GB/s vs GB300 peak"
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 
 
 def parse():
@@ -660,6 +661,7 @@ def main():
                        "latency_ms_flushed_graph": latency_graph_ms, "latency_ms_flushed_eager": latency_eager_ms,
                        "parallelism": f"replicas{world}"},
             "step_gbs": step_gbs, "step_frac_of_peak": step_gbs / peak,
+            "step_frac_of_nominal": step_gbs / NOMINAL_HBM_GBS, "nominal_hbm_gbs": NOMINAL_HBM_GBS,
             "algorithmic_bytes_per_step": alg_bytes,
             "roofline": {"kernel": "indexer_score_kernel", "bound": "hbm", "achieved": idx_gbs, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": idx_gbs / peak, "traffic": idx_traffic,
