@@ -11,17 +11,15 @@
 // One 8-CTA thread-block cluster per row, 512 threads per CTA. CTA r owns the
 // 128-slot chunk c = r / 2 and the head half r % 2 (32 heads).
 //   1. select (decode only): every CTA streams its slice of the row's scores
-//      and appends the candidates at or above the level-0 threshold bin to the
-//      leader's shared memory; the leader refines and keeps the winners'
-//      composites;
-//   2. place: every CTA ranks 64 of the winners against all of them by
-//      composite (score descending, lower index first): that rank is the
-//      winner's slot, both in the caller's best-first index list and in the
-//      attention, and the CTA stores the index into the shared memory of the
-//      two CTAs that own the slot (st.async, counted on the owner's mbarrier,
-//      so each CTA waits only for its own slots). With indices given by the
-//      caller, each CTA reads its chunk's slots instead;
-//   3. attend, on tcgen05 tensor cores with fp32 accumulators in TMEM: gather
+//      and stores the candidates at or above the level-0 threshold bin into
+//      the shared memory of every CTA of the cluster (an all-gather); after one
+//      cluster barrier each CTA refines the threshold over the gathered
+//      candidates, sorts the winners best first and takes its chunk's slots:
+//      slot t holds the t-th best index, both in the caller's best-first index
+//      list and in the attention. Every CTA computes the same selection, so no
+//      winner or slot crosses the cluster. With indices given by the caller,
+//      each CTA reads its chunk's slots instead;
+//   2. attend, on tcgen05 tensor cores with fp32 accumulators in TMEM: gather
 //      the chunk's 128 KV rows into the 128-byte-swizzled K-major layout, then
 //        logits  D[128 slots x 32 heads] = KV_chunk . Q_half^T   (K = 512,
 //                as four accumulators over the K-steps k = a mod 4, added
@@ -31,7 +29,7 @@
 //      for the four 128-feature blocks, where the same KV buffer is the
 //      MN-major operand and P enters as a bf16 hi + lo pair stacked along N
 //      (acc = D[:, h] + D[:, 32 + h]);
-//   4. combine: after a cluster barrier CTA r combines feature columns
+//   3. combine: after a cluster barrier CTA r combines feature columns
 //      [128 c, 128 c + 128) of its 32 heads over the chunks in chunk order:
 //        m = max(sink, m_c), den = exp(sink - m) + sum_c l_c exp(m_c - m),
 //        out = sum_c acc_c exp(m_c - m) / den.
@@ -43,6 +41,12 @@
 // non-finite logit (non-finite q or KV element, or overflow) flags its head;
 // a non-finite sink or denominator flags the head; a flagged head is written
 // as zeros, and any non-finite output element is written as zero.
+//
+// Bounded waits: a wait for the tensor cores that gives up (DS_STATUS_WAIT_TIMEOUT)
+// stops the CTA's attention work (no further MMA, no TMEM read) and flags the
+// row, so every head of it is written as zeros; the CTA still takes part in
+// every cluster barrier, and before it frees TMEM it waits (bounded) once more
+// for the MMAs it issued.
 
 #include <cooperative_groups.h>
 
@@ -54,7 +58,6 @@
 namespace dsrows {
 
 namespace cg = cooperative_groups;
-using attend::CombineSmem;
 using attend::combine_slice;
 using attend::cp_async16;
 using attend::cp_async4;
@@ -83,18 +86,19 @@ struct TailLayout {
     static constexpr size_t q = g + 8 * (size_t)kGBlock;               // query half [32][512], K-major SW128
     static constexpr size_t pmat = q + 8 * (size_t)kQBlock;            // [P_hi; P_lo] [64][128 slots], K-major SW128
     static constexpr size_t idx = pmat + 2 * (size_t)kPBlock;          // i32 [128] this chunk's slots
-    static constexpr size_t sel = idx + (size_t)kChunkSlots * 4;       // u64 [512] winners (leader)
+    static constexpr size_t sel = idx + (size_t)kChunkSlots * 4;       // u64 [512] the row's winners
     static constexpr size_t red = sel + (size_t)kTopK * 8;             // [4 quarters][32 heads] max, sum, bad
     static constexpr size_t misc = red + 3 * 4 * (size_t)kHalfHeads * 4;
     static constexpr size_t sinks = misc + 64;                         // f32 [32] this head half's sinks
-    static constexpr size_t cs = sinks + (size_t)kHalfHeads * 4;       // CombineSmem<32>
-    static constexpr size_t total = cs + sizeof(CombineSmem<kHalfHeads>);
-    // Aliases of the KV rows' space, used before the rows are gathered.
-    static constexpr size_t select = g;                                // SelectSmem (select phase)
-    static constexpr size_t selcopy = g;                               // u64 [512] (place phase)
-    static constexpr size_t ranks = g + (size_t)kTopK * 8;             // u32 [64] (place phase)
+    static constexpr size_t ranks = sinks + (size_t)kHalfHeads * 4;    // u32 [64] best-first ranks
+    static constexpr size_t total = ranks + 64 * 4;
+    // Aliases used before the KV rows are gathered and P is written: the
+    // gathered candidates ([8][kCandCap] u64) and the selection state.
+    static constexpr size_t regions = g;
+    static constexpr size_t gather = pmat;
 };
-static_assert(TailLayout::select + sizeof(SelectSmem) <= TailLayout::q, "select state overlaps the query");
+static_assert(TailLayout::regions + (size_t)kCluster * kCandCap * 8 <= TailLayout::q, "candidates overlap the query");
+static_assert(TailLayout::gather + sizeof(GatherSmem) <= TailLayout::idx, "selection state overlaps the slots");
 static_assert(TailLayout::misc % 8 == 0, "alignment");
 constexpr size_t kTailSmem = TailLayout::total + 1024;  // + slack to align the swizzled buffers to 1 KiB
 static_assert(kTailSmem <= 227 * 1024, "shared memory");
@@ -128,39 +132,62 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     float* red_max = reinterpret_cast<float*>(smem + T::red);
     float* red_sum = red_max + 4 * kHalfHeads;
     uint32_t* red_bad = reinterpret_cast<uint32_t*>(red_sum + 4 * kHalfHeads);
-    uint32_t* nsel_s = reinterpret_cast<uint32_t*>(smem + T::misc);
-    uint32_t* tmem_s = nsel_s + 1;
+    uint32_t* tmem_s = reinterpret_cast<uint32_t*>(smem + T::misc);
     uint64_t* mma_bar = reinterpret_cast<uint64_t*>(smem + T::misc + 8);
-    // This CTA's slots arrive (st.async, 4 bytes each) on slots_bar, the
-    // leader's winners and their number (4,100 bytes) on winners_bar.
-    uint64_t* slots_bar = reinterpret_cast<uint64_t*>(smem + T::misc + 16);
-    uint64_t* winners_bar = reinterpret_cast<uint64_t*>(smem + T::misc + 24);
-    CombineSmem<kHalfHeads>& cs = *reinterpret_cast<CombineSmem<kHalfHeads>*>(smem + T::cs);
     float* sinks_s = reinterpret_cast<float*>(smem + T::sinks);
-    SelectSmem& sm = *reinterpret_cast<SelectSmem*>(smem + T::select);
+    uint64_t* regions = reinterpret_cast<uint64_t*>(smem + T::regions);
+    GatherSmem& gs = *reinterpret_cast<GatherSmem*>(smem + T::gather);
 
     cg::cluster_group cluster = cg::this_cluster();
     const uint32_t rank = cluster.block_rank();
     const int e = blockIdx.x / kCluster;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    uint32_t* const pub_flag = p.flags + kRowsMax * kHeads + kRowsMax;  // [8] winners published
+    uint32_t* const pub_n = reinterpret_cast<uint32_t*>(p.pub + (size_t)kRowsMax * kTopK);
+
+    if (e >= (int)p.rows) {
+        // ---- one more cluster ranks the rows' winners (decode with attention):
+        // CTA r waits for row r to publish its winners in index order, sorts
+        // them best first and writes the row's index list. No row waits for it.
+        const uint32_t re = rank;
+        if (re >= p.rows) return;
+        pdl_wait();  // the publish flags were zeroed by earlier work
+        uint32_t ok = 1;
+        if (t == 0) {
+            const uint64_t start = global_timer_ns();
+            while (ld_acquire_gpu(pub_flag + re) == 0)
+                if (global_timer_ns() - start > kWaitBudgetNs) {
+                    atomicOr(p.status, kStatusWaitTimeout);
+                    ok = 0;
+                    break;
+                }
+        }
+        ok = __syncthreads_and(t != 0 || ok);
+        __threadfence();
+        const uint64_t x0 = ok ? __ldcg(p.pub + (size_t)re * kTopK + t) : 0ull;
+        const uint32_t nsel = ok ? __ldcg(pub_n + re) : 0u;
+        const uint64_t x = bitonic512_desc(x0, reinterpret_cast<uint64_t*>(gs.h));
+        if ((uint32_t)t < p.width[re])
+            p.indices[p.index_offset[re] + t] = (uint32_t)t < nsel ? (int32_t)(~(uint32_t)x) + p.offset[re] : -1;
+        return;
+    }
+
     const uint32_t c = rank >> 1;          // chunk: slots [128 c, 128 c + 128)
     const int half = (int)(rank & 1);      // heads [32 half, 32 half + 32)
     const int head0 = half * kHalfHeads;
-    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const uint32_t L = p.kv_len[e];
     const uint32_t W = p.width[e];
     const uint32_t q_row = p.q_row[e];
     const uint32_t nchunks = (W + kChunkSlots - 1) / kChunkSlots;
     const bool has_chunk = c < nchunks;
-    SelectSmem& leader = *cluster.map_shared_rank(&sm, 0);
 
     // ---- setup: counters, barrier, TMEM, and the query (an input of the call) --
     if (t == 0) {
-        sm.ncand = 0;
         mbar_init(mma_bar, kIssuers);
-        mbar_init(slots_bar, 1);
-        mbar_init(winners_bar, 1);
         fence_barrier_init();
     }
+    if (t < kChunkSlots) idx_s[t] = -1;  // slots past the last winner stay empty
+    sel[t] = 0;
     if (warp == 0 && p.attend) {
         tmem_alloc(tmem_s, kTmemCols);
         tmem_relinquish();
@@ -178,109 +205,97 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     };
     if (p.attend && !p.q_after_wait) fetch_inputs();
     tc_fence_before();
-    cluster.sync();  // the leader's counters are zero before anyone appends
+    cluster.sync();  // every CTA's counters are set before anyone stores into them
     tc_fence_after();
     const uint32_t tmem = p.attend ? *tmem_s : 0u;
     pdl_wait();  // scores and histogram (decode) or indices (caller) come from earlier work
     if (p.attend && p.q_after_wait) fetch_inputs();
 
+    const uint32_t first = c * kChunkSlots;
+    uint32_t nsel = 0;
     if (p.given == nullptr) {
-        // ---- select -------------------------------------------------------------
+        // ---- select: gather the candidates, then every CTA selects the same winners
         const float* s = p.scores + (size_t)e * p.score_stride;
-        const Collected col = select_collect(s, L, W, p.hist + (size_t)e * kHistBins, rank, sm, leader);
-        cluster.sync();  // every append into the leader is visible to it
-        uint64_t* sc = reinterpret_cast<uint64_t*>(smem + T::selcopy);
-        if (t == 0) mbar_arrive_expect_tx(winners_bar, kTopK * 8 + 4);
-        if (rank == 0) {
-            // The leader refines, then pushes the winners (zero past the last) and
-            // their number into every CTA's shared memory (st.async on each CTA's
-            // winners_bar).
-            const uint32_t n = select_finish(col, s, L, W, nullptr, sm, sel, p.status);
-            const uint64_t wv = (uint32_t)t < n ? sel[t] : 0ull;
-#pragma unroll
-            for (int r = 0; r < kCluster; ++r) {
-                st_async_remote_u64(sc + t, wv, winners_bar, (uint32_t)r);
-                if (t == 0) st_async_remote(nsel_s, n, winners_bar, (uint32_t)r);
-            }
+        const Gathered gat = select_collect_all(s, L, W, p.hist + (size_t)e * kHistBins,
+                                                p.gmax ? p.gmax + (size_t)e * p.gmax_stride : nullptr, rank, gs,
+                                                regions);
+        cluster.sync();  // every CTA's candidates are in every CTA; no CTA touches
+                         // another's shared memory after this barrier
+        nsel = select_slots(gat, s, L, W, gs, regions, sel, idx_s, first, p.status);
+    } else {
+        // ---- the caller's indices, in ascending order (sentinels last): the
+        // attention is a function of the index multiset. An index < -1 or
+        // >= kv_len flags the row (it is written as zeros) and takes no slot.
+        uint64_t v = 0;
+        if ((uint32_t)t < W) {
+            const int g = __ldcg(p.given + p.index_offset[e] + t);
+            if (g < -1 || g >= (int)L) atomicOr(&p.flags[kRowsMax * kHeads + e], 1u);
+            else if (g >= 0) v = (uint64_t)(~(uint32_t)g);
         }
-        mbar_wait_cluster(winners_bar, 0, p.status);  // the winners are here
-
-        // ---- place: rank 64 winners, store them in their slots -------------------
-        const uint32_t nsel = *nsel_s;
-        if (t == 0) {
-            // The slots of this CTA's chunk that get a winner, 4 bytes each.
-            const uint32_t first = c * kChunkSlots;
-            const uint32_t n_here = nsel > first ? (nsel - first < kChunkSlots ? nsel - first : kChunkSlots) : 0u;
-            mbar_arrive_expect_tx(slots_bar, 4u * n_here);
+        v = bitonic512_desc(v, reinterpret_cast<uint64_t*>(gs.h));
+        if ((uint32_t)t - first < (uint32_t)kChunkSlots && v != 0) idx_s[t - first] = (int32_t)(~(uint32_t)v);
+    }
+    __syncthreads();  // this chunk's slots are in place (and the candidates consumed)
+    if (p.ranker && rank == 0) {
+        // Publish the winners (index order) for the ranking cluster.
+        p.pub[(size_t)e * kTopK + t] = sel[t];
+        if (t == 0) pub_n[e] = nsel;
+        __threadfence();
+        __syncthreads();
+        if (t == 0) st_release_gpu(pub_flag + e, 1u);
+    }
+    // The gather of the chunk's KV rows starts now.
+    const size_t part0_off = ((size_t)2 * p.chunk_begin[e] + (size_t)half * nchunks) * kPartFloats;
+    if (has_chunk && p.attend) {
+        const __nv_bfloat16* kv = p.kv[e];
+        for (int k = t; k < kChunkSlots * (kDim / 8); k += kThreads) {
+            const int r = k >> 6, ch = k & 63;
+            const int i = idx_s[r];
+            uint8_t* dst = g_s + sw128_chunk(r, ch, kGBlock);
+            if (i >= 0 && (uint32_t)i < L) cp_async16(dst, kv + (size_t)i * kDim + ch * 8);
+            else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
         }
+    }
+    // Best-first ranks (decode): CTA `rank` ranks the winners of slots
+    // [64 rank, 64 rank + 64) against all of them (group t / 64 of 64 each) and
+    // writes their indices at their ranks; slots past the last winner (up to
+    // the width) are -1. With attention this runs inside the cluster barrier
+    // that precedes the combine.
+    auto rank_indices = [&]() {
         uint32_t* rk = reinterpret_cast<uint32_t*>(smem + T::ranks);
         if (t < 64) rk[t] = 0;
-        // Slots of this chunk past the last winner are empty.
-        if (t < kChunkSlots && c * kChunkSlots + (uint32_t)t >= nsel) idx_s[t] = -1;
         __syncthreads();
-        // Winner k against the 64 winners of group t / 64: how many are better
-        // (the zero padding never is; composites are distinct).
         const uint32_t k = rank * 64 + (uint32_t)(t & 63);
-        const uint64_t ck = sc[k];
-        const uint64_t* grp = sc + (t >> 6) * 64;
+        const uint64_t ck = sel[k];
+        const uint64_t* grp = sel + (t >> 6) * 64;
         uint32_t nb = 0;
 #pragma unroll 16
         for (int j = 0; j < 64; ++j) nb += grp[j] > ck ? 1u : 0u;
         atomicAdd(&rk[t & 63], nb);
         __syncthreads();
         if (t < 64) {
-            int32_t* out = p.indices ? p.indices + p.index_offset[e] : nullptr;
-            if (k < nsel) {
-                const uint32_t pos = rk[t];
-                const int32_t j = (int32_t)(~(uint32_t)ck);
-                if (out) out[pos] = j + p.offset[e];
-                if (p.attend) {
-                    const uint32_t owner = 2 * (pos / kChunkSlots);
-                    uint32_t* slot_word = reinterpret_cast<uint32_t*>(idx_s + pos % kChunkSlots);
-                    st_async_remote(slot_word, (uint32_t)j, slots_bar, owner);
-                    st_async_remote(slot_word, (uint32_t)j, slots_bar, owner + 1);
-                }
-            } else if (out && k < W) {
-                out[k] = -1;
-            }
+            int32_t* out = p.indices + p.index_offset[e];
+            if (k < nsel) out[rk[t]] = (int32_t)(~(uint32_t)ck) + p.offset[e];
+            else if (k < W) out[k] = -1;
         }
-        // Selection only: the indices are out; no CTA touches another's shared
-        // memory after the winners' barrier, so the cluster may leave.
-        if (!p.attend) return;
-    } else if (t < kChunkSlots) {
-        // ---- the caller's indices: -1 for sentinels, bad indices and slots past the width
-        const uint32_t slot = c * kChunkSlots + (uint32_t)t;
-        int i = -1;
-        if (slot < W) {
-            const int v = __ldcg(p.given + p.index_offset[e] + slot);
-            if (v < -1 || v >= (int)L) atomicOr(&p.flags[kRowsMax * kHeads + e], 1u);
-            else i = v;
-        }
-        idx_s[t] = i;
+    };
+    const bool want_ranks = p.given == nullptr && p.indices != nullptr && !p.ranker;
+    if (!p.attend) {
+        if (want_ranks) rank_indices();
+        return;
     }
-    // Every slot of this CTA's chunk is in place: the winners placed by the
-    // cluster (decode) have arrived; the local writes are ordered by the barrier.
-    if (p.given == nullptr) mbar_wait_cluster(slots_bar, 0, p.status);
-    __syncthreads();
 
     // ---- attend: 128 slots x 32 heads on the tensor cores ------------------------
-    const size_t part0_off = ((size_t)2 * p.chunk_begin[e] + (size_t)half * nchunks) * kPartFloats;
-    if (has_chunk) {
-        const __nv_bfloat16* kv = p.kv[e];
-        for (int k = t; k < kChunkSlots * (kDim / 8); k += kThreads) {
-            const int r = k >> 6, ch = k & 63;
-            const int i = idx_s[r];
-            uint8_t* dst = g_s + sw128_chunk(r, ch, kGBlock);
-            if (i >= 0) cp_async16(dst, kv + (size_t)i * kDim + ch * 8);
-            else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-        }
-    }
     cp_async_wait_all();      // the query and the KV rows
     fence_proxy_async_smem();  // ... are visible to the tensor cores
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
+    // `alive`: every tensor-core wait of this CTA has succeeded (uniform over the
+    // CTA); `pending`: the mma_bar phase of MMAs whose completion was not seen.
+    bool alive = true;
+    int pending = -1;
     if (has_chunk) {
         const uint32_t g_addr = smem_u32(g_s), q_addr = smem_u32(q_s);
         if (lane == 0 && warp < kIssuers) {
@@ -293,9 +308,13 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
                           smem_desc_sw128_kmajor(q_addr + j * kQBlock + koff), idesc, j > 0 ? 1u : 0u);
             umma_commit(mma_bar);
         }
-        mbar_wait(mma_bar, 0, p.status);
+    }
+    if (has_chunk) {
+        alive = __syncthreads_and(mbar_wait(mma_bar, 0, p.status)) != 0;
+        if (!alive) pending = 0;
+    }
+    if (has_chunk && alive) {
         tc_fence_after();
-
         // ---- chunk softmax: warp -> (32 slots, 8 heads), lane -> one slot ----------
         const int qt = warp & 3, hg = warp >> 2;
         const int slot = 32 * qt + lane;
@@ -305,21 +324,23 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         const bool live = idx_s[slot] >= 0;
         float l[8], m[8];
+        uint32_t bad_bits = 0;  // head i of this warp's 8 has a non-finite live logit
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             l[i] = ((__uint_as_float(v[0][i]) + __uint_as_float(v[1][i])) +
                     (__uint_as_float(v[2][i]) + __uint_as_float(v[3][i]))) * p.scale;
             const bool ok = live && finite_f(l[i]);
-            const uint32_t bad = __ballot_sync(0xFFFFFFFFu, live && !ok);
+            bad_bits |= (live && !ok) ? 1u << i : 0u;
             if (!ok) l[i] = -INFINITY;
-            m[i] = l[i];
-            if (lane == 0) red_bad[qt * kHalfHeads + 8 * hg + i] = bad ? 1u : 0u;
+            m[i] = warp_max(l[i]);
         }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) m[i] = warp_max(m[i]);
+        bad_bits = __reduce_or_sync(0xFFFFFFFFu, bad_bits);
         if (lane == 0)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) red_max[qt * kHalfHeads + 8 * hg + i] = m[i];
+            for (int i = 0; i < 8; ++i) {
+                red_max[qt * kHalfHeads + 8 * hg + i] = m[i];
+                red_bad[qt * kHalfHeads + 8 * hg + i] = (bad_bits >> i) & 1u;
+            }
         __syncthreads();
         float sum[8];
 #pragma unroll
@@ -337,28 +358,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
             *reinterpret_cast<__nv_bfloat16*>(p_s + off + kHalfHeads * 128) = lo;
             sum[i] = w;
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) sum[i] += __shfl_xor_sync(0xFFFFFFFFu, sum[i], o);
-        if (lane == 0)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) red_sum[qt * kHalfHeads + 8 * hg + i] = sum[i];
         fence_proxy_async_smem();  // P is visible to the tensor cores
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-
-        float* part = p.part + part0_off + (size_t)c * kPartFloats;
-        if (t < kHalfHeads) {
-            const float mh = fmaxf(fmaxf(red_max[t], red_max[kHalfHeads + t]),
-                                   fmaxf(red_max[2 * kHalfHeads + t], red_max[3 * kHalfHeads + t]));
-            part[t] = mh;
-            part[kHalfHeads + t] = (red_sum[t] + red_sum[kHalfHeads + t]) +
-                                   (red_sum[2 * kHalfHeads + t] + red_sum[3 * kHalfHeads + t]);
-            if (red_bad[t] | red_bad[kHalfHeads + t] | red_bad[2 * kHalfHeads + t] | red_bad[3 * kHalfHeads + t])
-                atomicOr(&p.flags[e * kHeads + head0 + t], 1u);
-        }
+        const uint32_t g_addr = smem_u32(g_s);
         if (lane == 0 && warp < kIssuers) {
             // Feature block b = warp: features [128 b, 128 b + 128).
             constexpr uint32_t idesc = idesc_bf16_f32(128, 2 * kHalfHeads) | kIdescAMnMajor;
@@ -373,32 +377,64 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
             }
             umma_commit(mma_bar);
         }
-        mbar_wait(mma_bar, 1, p.status);
-        tc_fence_after();
-
-        // ---- partial: warp -> (32 features, 32 heads) of block warp / 4 -------------
-        const int b = warp >> 2;
-        uint32_t ahi[32], alo[32];
-        const uint32_t tcol = tmem + ((uint32_t)(32 * qt) << 16) + kPvCol + 64 * b;
-        tmem_ld_x32(tcol, ahi);
-        tmem_ld_x32(tcol + kHalfHeads, alo);
-        tmem_ld_wait();
-        float* pacc = part + 2 * kHalfHeads + 128 * b + 32 * qt + lane;
+        // While the tensor cores run P G: the chunk's sum per head (a fixed warp
+        // tree, then the four quarters) and the head flags.
 #pragma unroll
-        for (int h = 0; h < kHalfHeads; ++h)
-            pacc[(size_t)h * kDim] = __uint_as_float(ahi[h]) + __uint_as_float(alo[h]);
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sum[i] += __shfl_xor_sync(0xFFFFFFFFu, sum[i], o);
+        if (lane == 0)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) red_sum[qt * kHalfHeads + 8 * hg + i] = sum[i];
+        __syncthreads();
+        float* part = p.part + part0_off + (size_t)c * kPartFloats;
+        if (t < kHalfHeads) {
+            const float mh = fmaxf(fmaxf(red_max[t], red_max[kHalfHeads + t]),
+                                   fmaxf(red_max[2 * kHalfHeads + t], red_max[3 * kHalfHeads + t]));
+            part[t] = mh;
+            part[kHalfHeads + t] = (red_sum[t] + red_sum[kHalfHeads + t]) +
+                                   (red_sum[2 * kHalfHeads + t] + red_sum[3 * kHalfHeads + t]);
+            if (red_bad[t] | red_bad[kHalfHeads + t] | red_bad[2 * kHalfHeads + t] | red_bad[3 * kHalfHeads + t])
+                atomicOr(&p.flags[e * kHeads + head0 + t], 1u);
+        }
+        alive = __syncthreads_and(mbar_wait(mma_bar, 1, p.status)) != 0;
+        if (!alive) pending = 1;
+        if (alive) {
+            tc_fence_after();
+            // ---- partial: warp -> (32 features, 32 heads) of block warp / 4 -------------
+            const int b = warp >> 2;
+            uint32_t ahi[32], alo[32];
+            const uint32_t tcol = tmem + ((uint32_t)(32 * qt) << 16) + kPvCol + 64 * b;
+            tmem_ld_x32(tcol, ahi);
+            tmem_ld_x32(tcol + kHalfHeads, alo);
+            tmem_ld_wait();
+            float* pacc = part + 2 * kHalfHeads + 128 * b + 32 * qt + lane;
+#pragma unroll
+            for (int h = 0; h < kHalfHeads; ++h)
+                pacc[(size_t)h * kDim] = __uint_as_float(ahi[h]) + __uint_as_float(alo[h]);
+        }
     }
+    // A CTA whose tensor-core wait gave up has no valid partial: the whole row
+    // is written as zeros.
+    if (!alive && t == 0) atomicOr(&p.flags[kRowsMax * kHeads + e], 1u);
     tc_fence_before();
-    cluster.sync();  // every chunk's partial and head flags are visible to the cluster
+    // Every chunk's partial and flags are visible to the cluster after this
+    // barrier; the best-first ranks are written while it completes.
+    cluster_arrive_release();
+    if (want_ranks) rank_indices();
+    cluster_wait_acquire();
     tc_fence_after();
 
     // ---- combine: feature columns [128 c, 128 c + 128) of the 32 heads ----------
     combine_slice<kHalfHeads, kThreads, 128>(
-        p.part + part0_off, kPartFloats, (int)nchunks, (int)(128 * c),
-        sinks_s, p.flags + kRowsMax * kHeads + e, p.flags + e * kHeads + head0,
+        p.part + part0_off, kPartFloats, (int)nchunks, (int)(128 * c), sinks_s,
+        p.flags + kRowsMax * kHeads + e, p.flags + e * kHeads + head0,
         p.out + ((size_t)q_row * kHeads + head0) * kDim,
-        p.invalid && c == 0 ? p.invalid + (size_t)q_row * kHeads + head0 : nullptr, cs);
+        p.invalid && c == 0 ? p.invalid + (size_t)q_row * kHeads + head0 : nullptr);
 
+    // MMAs whose completion was not seen may still write TMEM: wait once more
+    // (bounded) before it is freed.
+    if (pending >= 0) (void)mbar_wait(mma_bar, (uint32_t)pending, nullptr);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -414,7 +450,8 @@ cudaError_t launch_decode_tail(const TailParams& p, cudaStream_t stream, bool pd
     const cudaError_t err = set_smem_limit_once(decode_tail_kernel, kTailSmem, smem_set);
     if (err != cudaSuccess) return err;
     if (p.rows == 0) return cudaSuccess;
-    return launch_kernel(decode_tail_kernel, dim3(p.rows * kCluster), dim3(kThreads), kTailSmem, stream, pdl, p);
+    const uint32_t clusters = p.rows + (p.ranker ? 1u : 0u);
+    return launch_kernel(decode_tail_kernel, dim3(clusters * kCluster), dim3(kThreads), kTailSmem, stream, pdl, p);
 }
 
 }  // namespace dsrows

@@ -420,14 +420,20 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
                 if (k >= nk) break;
                 const int vr = G == 1 ? sg : p.seg_vrow[sg] + q0 + k;
                 const float sc = head_sum(v[k], G == 1 ? wr : nullptr, w_s + (q0 + k) * kIdxHeads);
-                if (j < p.valid[vr]) {
-                    const bool fin = finite_f(sc);
+                const bool in = j < p.valid[vr];
+                const bool fin = finite_f(sc);
+                if (in) {
                     st_global_hint(p.scores + (size_t)vr * p.score_stride + j, fin ? sc : -INFINITY, keep);
                     if (want_hist && fin) {
                         const uint32_t bin = score_key(sc) >> 21;
                         if (G == 1) atomicAdd(&hist_s[bin], 1u);
                         else atomicAdd(&hist_s[(q0 + k) * (kHistBins / 2) + (bin >> 1)], (bin & 1) ? 0x10000u : 1u);
                     }
+                }
+                if (p.gmax) {
+                    // The warp's 32 keys are one group: its largest score key.
+                    const uint32_t gm = __reduce_max_sync(0xFFFFFFFFu, in && fin ? score_key(sc) : 0u);
+                    if (lane == 0 && j < p.valid[vr]) p.gmax[(size_t)vr * p.gmax_stride + (j >> 5)] = gm;
                 }
             }
         }

@@ -20,12 +20,12 @@ namespace cg = cooperative_groups;
 constexpr int kThreads = 512;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
-struct LevelSpec {
-    int shift;
-    int bits;
-};
-// Digits of the composite, most significant first.
-static __constant__ LevelSpec kLevels[6] = {{53, 11}, {42, 11}, {32, 10}, {21, 11}, {10, 11}, {0, 10}};
+// Digits of the composite, most significant first: level lv covers bits
+// [level_shift(lv), level_shift(lv) + level_bits(lv)).
+__device__ __forceinline__ int level_shift(int lv) {
+    return lv == 0 ? 53 : lv == 1 ? 42 : lv == 2 ? 32 : lv == 3 ? 21 : lv == 4 ? 10 : 0;
+}
+__device__ __forceinline__ int level_bits(int lv) { return (lv == 2 || lv == 5) ? 10 : 11; }
 
 struct BinPick {
     int bin;        // -1 when the histogram holds fewer than `need` elements
@@ -36,10 +36,13 @@ struct BinPick {
 
 // Block-wide (512 threads, 4 bins each): the bin b with
 //   count(bins >= b) >= need > count(bins > b).
-// `scratch` is >= 24 words of shared memory.
-__device__ inline BinPick pick_bin(const uint32_t* h, uint32_t need, uint32_t* scratch) {
+// `scratch` is >= 24 words of shared memory; h is 16-byte aligned. Every
+// thread has read h when the call returns, so h may be overwritten then.
+// Without `sync_after`, the next call must use other scratch words.
+__device__ inline BinPick pick_bin(const uint32_t* h, uint32_t need, uint32_t* scratch, bool sync_after = true) {
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-    const uint32_t v0 = h[4 * t], v1 = h[4 * t + 1], v2 = h[4 * t + 2], v3 = h[4 * t + 3];
+    const uint4 hv = reinterpret_cast<const uint4*>(h)[t];
+    const uint32_t v0 = hv.x, v1 = hv.y, v2 = hv.z, v3 = hv.w;
     const uint32_t tot = v0 + v1 + v2 + v3;
     uint32_t x = tot;
 #pragma unroll
@@ -74,7 +77,7 @@ __device__ inline BinPick pick_bin(const uint32_t* h, uint32_t need, uint32_t* s
     r.eq = scratch[18];
     r.total = scratch[19];
     if (r.bin < 0) r.gt = r.eq = 0;
-    __syncthreads();
+    if (sync_after) __syncthreads();
     return r;
 }
 
@@ -103,12 +106,15 @@ struct RowSource {
 };
 
 constexpr int kCluster = 8;        // CTAs per row in the select kernel
+constexpr uint32_t kChunkSlotsSel = 128;  // attention slots per CTA chunk
 constexpr int kLeaderCap = 8192;   // candidates the leader CTA holds in shared memory
 
 constexpr uint32_t kRankDirect = 128;  // a threshold bin this small is ranked element by element
 
+struct SelectSmem;
+__device__ __forceinline__ uint32_t* pick_scratch(SelectSmem& sm);
 struct SelectSmem {
-    uint32_t h[kHistBins];   // level-0 histogram (each CTA), then refinement levels (leader),
+    __align__(16) uint32_t h[kHistBins];  // level-0 histogram (each CTA), then refinement levels (leader),
                              // then the threshold bin's elements when they are ranked directly
     uint32_t scratch[32];
     uint64_t cand[kLeaderCap];
@@ -116,6 +122,7 @@ struct SelectSmem {
     uint32_t nsel;
     uint32_t nres;
 };
+__device__ __forceinline__ uint32_t* pick_scratch(SelectSmem& sm) { return sm.scratch; }
 
 // Where the refinement stands: the last digit level fixed, the composite
 // prefix through that level, and how many elements of that prefix are needed.
@@ -156,10 +163,11 @@ __device__ __forceinline__ void write_winners(SelectSmem& sm, const uint64_t* se
 // most kRankDirect elements, then keep the winners' composites in sel[0, 512)
 // (zero past the last): every element above the bin, and the `need` best of
 // the bin's elements, found by counting for each how many of them are better.
-// Writes their indices to out (unless out is null). Returns the number of winners.
-template <class Src>
-__device__ inline uint32_t finish_row(const Src& src, Refine st, uint32_t width, uint32_t L, int32_t* out,
-                                      SelectSmem& sm, uint64_t* sel, uint32_t* status, int32_t offset = 0) {
+// `sm` provides h[kHistBins], scratch[32], nsel and nres. Returns the number of
+// winners (their order in sel is arbitrary).
+template <class Src, class Smem>
+__device__ inline uint32_t finish_row(const Src& src, Refine st, uint32_t width, Smem& sm, uint64_t* sel,
+                                      uint32_t* status) {
     const int t = threadIdx.x, lane = t & 31;
     const bool take_all = st.take_all;
     int level = st.level;
@@ -168,31 +176,30 @@ __device__ inline uint32_t finish_row(const Src& src, Refine st, uint32_t width,
     uint32_t eq = st.eq;
     bool done = st.done;
     for (int lv = level + 1; lv < 6 && !done && eq > kRankDirect; ++lv) {
-        const LevelSpec up = kLevels[lv - 1];
-        const LevelSpec cur = kLevels[lv];
-        const uint32_t mask = (1u << cur.bits) - 1;
+        const int up_shift = level_shift(lv - 1), cur_shift = level_shift(lv), cur_bits = level_bits(lv);
+        const uint32_t mask = (1u << cur_bits) - 1;
         for (int i = t; i < kHistBins; i += kThreads) sm.h[i] = 0;
         __syncthreads();
         const uint32_t n = src.size();
         for (uint32_t i = t; i < n; i += kThreads) {
             uint64_t c;
-            if (src.get(i, c) && (c >> up.shift) == prefix) atomicAdd(&sm.h[(c >> cur.shift) & mask], 1u);
+            if (src.get(i, c) && (c >> up_shift) == prefix) atomicAdd(&sm.h[(c >> cur_shift) & mask], 1u);
         }
         __syncthreads();
-        const BinPick pk = pick_bin(sm.h, need, sm.scratch);
+        const BinPick pk = pick_bin(sm.h, need, pick_scratch(sm));
         if (pk.bin < 0) {  // inconsistent counts: keep what is certain
             if (t == 0) atomicOr(status, kStatusCandOverflow);
             done = true;
             break;
         }
         need -= pk.gt;
-        prefix = (prefix << cur.bits) | (uint64_t)pk.bin;
+        prefix = (prefix << cur_bits) | (uint64_t)pk.bin;
         level = lv;
         eq = pk.eq;
         done = pk.eq == need;
     }
     const bool direct = !done;  // the bin's eq (<= kRankDirect) elements are ranked below
-    const int shift = kLevels[level].shift;
+    const int shift = level_shift(level);
     uint64_t* bin_el = reinterpret_cast<uint64_t*>(sm.h);  // the threshold bin's elements
 
     if (t == 0) {
@@ -242,7 +249,6 @@ __device__ inline uint32_t finish_row(const Src& src, Refine st, uint32_t width,
     const uint32_t got = sm.nsel;
     const uint32_t nsel = got < width ? got : width;
     if (got > width && t == 0) atomicOr(status, kStatusCandOverflow);
-    if (out) write_winners(sm, sel, nsel, width, out, offset);
     return nsel;
 }
 
@@ -295,7 +301,7 @@ __device__ __forceinline__ Collected select_collect(const float* s, uint32_t L, 
     for (int i = 0; i < kHistBins / kThreads; ++i) sm.h[t + i * kThreads] = hv[i];
     __syncthreads();
     Collected r;
-    r.l0 = pick_bin(sm.h, width, sm.scratch);
+    r.l0 = pick_bin(sm.h, width, pick_scratch(sm));
     r.take_all = r.l0.total <= width;
     const uint32_t n_cand = r.take_all ? r.l0.total : r.l0.gt + r.l0.eq;
     r.b0 = r.take_all ? 0u : (uint32_t)r.l0.bin;
@@ -351,11 +357,412 @@ __device__ __forceinline__ uint32_t select_finish(const Collected& c, const floa
         BinPick l0f = c.l0;
         l0f.bin = (int)c.b0;
         const Refine st = refine_from_level0(l0f, width);
-        return finish_row(SmemCandSource{sm.cand, got < (uint32_t)kLeaderCap ? got : (uint32_t)kLeaderCap}, st, width,
-                          L, out, sm, sel, status, offset);
+        const uint32_t nsel = finish_row(
+            SmemCandSource{sm.cand, got < (uint32_t)kLeaderCap ? got : (uint32_t)kLeaderCap}, st, width, sm, sel,
+            status);
+        if (out) write_winners(sm, sel, nsel, width, out, offset);
+        return nsel;
     }
-    return finish_row(RowSource{s, L}, refine_from_level0(c.l0, width), width, L, out, sm, sel, status,
-                      offset);
+    const uint32_t nsel = finish_row(RowSource{s, L}, refine_from_level0(c.l0, width), width, sm, sel, status);
+    if (out) write_winners(sm, sel, nsel, width, out, offset);
+    return nsel;
+}
+
+// ---- all-gather selection: every CTA of the row's cluster selects locally ----
+//
+// Every CTA of a row's cluster gathers all of the row's candidates, in index
+// order, and computes the same exact threshold T (the composite of the
+// width-th best score): the winners are the candidates >= T. A winner's slot
+// is its place among the winners in index order (the attention's slot order).
+
+constexpr uint32_t kCandCap = 2048;  // candidates one CTA may contribute to its cluster
+constexpr int kRegCand = 4;          // candidates per thread held in registers by the refinement
+
+// State of the all-gather selection in each CTA of a row's cluster.
+struct GatherSmem {
+    __align__(16) uint32_t h[kHistBins];  // level-0 histogram, the refinement levels, sort buffers
+    uint32_t pick[2][32];                 // two alternating pick_bin scratch areas
+    uint32_t scan[2][16];                 // two alternating block_excl_scan scratch areas
+    uint32_t count[kCluster];             // candidates contributed by each CTA (written by that CTA)
+    uint32_t nres;
+    uint32_t nsel;
+    uint64_t thr;
+};
+__device__ __forceinline__ uint32_t* pick_scratch(GatherSmem& sm) { return sm.pick[0]; }
+static_assert(kHistBins * 4 >= 2 * kTopK * 8, "the sorts use h as two 512-entry buffers");
+
+// Exclusive prefix over the block's threads, in thread order, of one count
+// per thread, and the block's total, with one barrier. `scratch` (16 words) is
+// rewritten only after the next block barrier.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t& total, uint32_t* scratch) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    uint32_t inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += y;
+    }
+    if (lane == 31) scratch[w] = inc;
+    __syncthreads();
+    uint32_t before = 0, all = 0;
+#pragma unroll
+    for (int w2 = 0; w2 < kThreads / 32; ++w2) {
+        const uint32_t y = scratch[w2];
+        all += y;
+        before += w2 < w ? y : 0u;
+    }
+    total = all;
+    return before + inc - v;
+}
+
+// x[b] for a run-time b < 32 without indexing registers: a tree of selects.
+__device__ __forceinline__ float select32(const float (&x)[32], uint32_t b) {
+    float a16[16], a8[8], a4[4], a2[2];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) a16[k] = (b & 16) ? x[k + 16] : x[k];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a8[k] = (b & 8) ? a16[k + 8] : a16[k];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) a4[k] = (b & 4) ? a8[k + 4] : a8[k];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) a2[k] = (b & 2) ? a4[k + 2] : a4[k];
+    return (b & 1) ? a2[1] : a2[0];
+}
+
+// The cluster's candidates in this CTA's shared memory: region r (kCandCap
+// composites from its start) holds the count[r] contributed by CTA r, in index
+// order; position i of the source is in the region r with b[r] <= i < b[r + 1],
+// so positions follow the index.
+struct RegionSource {
+    const uint64_t* c;
+    uint32_t b[kCluster + 1];
+    __device__ __forceinline__ uint32_t size() const { return b[kCluster]; }
+    __device__ __forceinline__ bool get(uint32_t i, uint64_t& v) const {
+        uint32_t r = 0, base = 0;
+#pragma unroll
+        for (int k = 1; k < kCluster; ++k)
+            if (i >= b[k]) { r = (uint32_t)k; base = b[k]; }
+        v = c[(size_t)r * kCandCap + (i - base)];
+        return true;
+    }
+};
+
+struct Gathered {
+    BinPick l0;     // level-0 pick from the row's histogram
+    uint32_t b0;    // threshold bin (0 when every finite score is taken)
+    bool take_all;  // no more finite scores than the width
+    bool fast;      // the candidates were gathered (else the full row is refined)
+};
+
+// Collection phase of a row's cluster (kCluster CTAs of kThreads): every CTA
+// picks the level-0 threshold bin from the row's histogram and compacts the
+// candidates of its slice of the row (finite scores whose top 11 key bits are
+// >= that bin), as composites in index order, into region `rank` of `regions`
+// in its own shared memory. Scores are read in groups of 32 consecutive keys,
+// one group per thread, and with `gmax` (the largest score key of each group)
+// only the groups that hold a candidate are read. Then each CTA copies its
+// candidates, densely, into region `rank` of every other CTA of the cluster,
+// and its count into count[rank] of every CTA. Before the call every CTA has
+// passed a cluster barrier; after it a cluster barrier makes every CTA's
+// candidates visible to all. h is left zero.
+__device__ __forceinline__ Gathered select_collect_all(const float* s, uint32_t L, uint32_t width,
+                                                       const uint32_t* hist_row, const uint32_t* gmax,
+                                                       uint32_t rank, GatherSmem& sm, uint64_t* regions) {
+    const int t = threadIdx.x;
+    // This CTA's slice: a multiple of 2048 scores; a batch is 512 groups of 32.
+    constexpr uint32_t kGroup = 32, kBatchScores = kGroup * kThreads;
+    const uint32_t per = (((L + kCluster - 1) / kCluster) + 2047) & ~2047u;
+    const uint32_t begin = min(L, rank * per);
+    const uint32_t end = min(L, begin + per);
+    const bool vec = (reinterpret_cast<uintptr_t>(s) & 15) == 0;
+    // The histogram, and the first batch's group maxima, in one round trip.
+    uint32_t hv[kHistBins / kThreads];
+#pragma unroll
+    for (int i = 0; i < kHistBins / kThreads; ++i) hv[i] = __ldcg(hist_row + t + i * kThreads);
+    auto group_max = [&](uint32_t base) -> uint32_t {
+        const uint32_t j = base + kGroup * t;
+        if (j >= end) return 0u;
+        return gmax ? __ldcg(gmax + (j >> 5)) : 0xFFFFFFFFu;
+    };
+    uint32_t gm = group_max(begin);
+#pragma unroll
+    for (int i = 0; i < kHistBins / kThreads; ++i) sm.h[t + i * kThreads] = hv[i];
+    __syncthreads();
+    Gathered r;
+    r.l0 = pick_bin(sm.h, width, sm.pick[0], false);
+    r.take_all = r.l0.total <= width;
+    const uint32_t n_cand = r.take_all ? r.l0.total : r.l0.gt + r.l0.eq;
+    r.b0 = r.take_all ? 0u : (uint32_t)r.l0.bin;
+    r.fast = n_cand <= (uint32_t)kCluster * kCandCap;
+    // The refinement's first level counts into h: zero it (every thread has
+    // read its bins of the histogram above).
+#pragma unroll
+    for (int i = 0; i < kHistBins / kThreads; ++i) sm.h[t + i * kThreads] = 0;
+
+    uint64_t* own = regions + (size_t)rank * kCandCap;
+    uint32_t n_local = 0;
+    if (r.fast) {
+        // A finite score is a candidate when its key is >= k0 = b0 << 21; the
+        // same test on the float: score >= the smallest score of bin b0
+        // (-0.0 ties +0.0).
+        const uint32_t k0 = r.b0 << 21;
+        float thr = -FLT_MAX;
+        if (!r.take_all) {
+            const float f = __uint_as_float((k0 & 0x80000000u) ? (k0 & 0x7FFFFFFFu) : ~k0);
+            if (finite_f(f)) thr = f;
+        }
+        int par = 0;
+        for (uint32_t base = begin; base < end; base += kBatchScores) {
+            if (base != begin) gm = group_max(base);
+            const uint32_t j0 = base + kGroup * t;
+            uint32_t take = 0;
+            float v[kGroup];
+            if (j0 < end && gm >= k0) {
+#pragma unroll
+                for (int i = 0; i < kGroup / 4; ++i) {
+                    const uint32_t j = j0 + 4 * i;
+                    if (vec && j + 3 < end) {
+                        const float4 q = __ldcg(reinterpret_cast<const float4*>(s + j));
+                        v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            v[4 * i + u] = j + u < end ? __ldcg(s + j + u) : __int_as_float(0x7FC00000);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < kGroup; ++i) take |= (v[i] >= thr && v[i] < INFINITY) ? (1u << i) : 0u;
+            }
+            // Positions in index order: this thread's group follows the groups
+            // of the threads before it.
+            uint32_t total;
+            uint32_t at = n_local + block_excl_scan((uint32_t)__popc(take), total, sm.scan[par]);
+            par ^= 1;
+            n_local += total;
+            while (take) {
+                const uint32_t b = (uint32_t)__ffs(take) - 1;
+                take &= take - 1;
+                if (at < kCandCap) own[at] = composite(score_key(select32(v, b)), j0 + b);
+                ++at;
+            }
+        }
+    }
+    __syncthreads();  // this CTA's candidates are in place
+    // Dense copy into the other CTAs: 16 bytes per store, consecutive threads
+    // on consecutive addresses.
+    const uint32_t m = n_local < kCandCap ? n_local : kCandCap;
+    const uint32_t own_addr = smem_u32(own);
+    for (uint32_t i = 2 * t; i < m; i += 2 * kThreads) {
+        const uint64_t a = own[i], b = i + 1 < m ? own[i + 1] : 0ull;
+#pragma unroll
+        for (int q = 1; q < kCluster; ++q) {
+            const uint32_t d = cluster_addr(own_addr, (rank + q) % kCluster) + 8 * i;
+            if (i + 1 < m) asm volatile("st.shared::cluster.v2.u64 [%0], {%1, %2};" ::"r"(d), "l"(a), "l"(b) : "memory");
+            else st_cluster_u64(d, a);
+        }
+    }
+    if (t < kCluster) st_cluster_u32(cluster_addr(smem_u32(&sm.count[rank]), (uint32_t)t), n_local);
+    return r;
+}
+
+// The exact threshold of the winners among n <= kThreads * kRegCand gathered
+// candidates held in registers (x[k] is candidate kRegCand t + k, zero past n),
+// from the refinement state `st`: the winners are the candidates with a
+// composite >= the returned value (1 when every candidate is taken). h is zero
+// on entry.
+__device__ __forceinline__ uint64_t refine_threshold(const uint64_t (&x)[kRegCand], Refine st, GatherSmem& sm,
+                                                     uint32_t* status) {
+    const int t = threadIdx.x, lane = t & 31;
+    if (st.take_all) return 1ull;
+    int level = st.level;
+    uint64_t prefix = st.prefix;
+    uint32_t need = st.need;
+    uint32_t eq = st.eq;
+    bool done = st.done;
+    int par = 0;
+    for (int lv = level + 1; lv < 6 && !done && eq > kRankDirect; ++lv) {
+        const int up_shift = level_shift(lv - 1), cur_shift = level_shift(lv), cur_bits = level_bits(lv);
+        const uint32_t mask = (1u << cur_bits) - 1;
+        if (lv > st.level + 1) {
+            for (int i = t; i < kHistBins; i += kThreads) sm.h[i] = 0;
+            __syncthreads();
+        }
+#pragma unroll
+        for (int k = 0; k < kRegCand; ++k)
+            if (x[k] != 0 && (x[k] >> up_shift) == prefix) atomicAdd(&sm.h[(x[k] >> cur_shift) & mask], 1u);
+        __syncthreads();
+        const BinPick pk = pick_bin(sm.h, need, sm.pick[par], false);
+        par ^= 1;
+        if (pk.bin < 0) {  // inconsistent counts: keep what is certain
+            if (t == 0) atomicOr(status, kStatusCandOverflow);
+            done = true;
+            break;
+        }
+        need -= pk.gt;
+        prefix = (prefix << cur_bits) | (uint64_t)pk.bin;
+        level = lv;
+        eq = pk.eq;
+        done = pk.eq == need;
+    }
+    const int shift = level_shift(level);
+    const uint64_t whole = prefix << shift;  // the bin taken whole: every composite >= this
+    if (done) return whole;
+    // The threshold bin's eq (<= kRankDirect) elements: the need-th best of them.
+    uint64_t* bin_el = reinterpret_cast<uint64_t*>(sm.h);
+    if (t == 0) {
+        sm.nres = 0;
+        sm.thr = whole;
+    }
+    __syncthreads();  // (every thread has read h in the last pick)
+#pragma unroll
+    for (int k = 0; k < kRegCand; ++k) {
+        const bool in_bin = x[k] != 0 && (x[k] >> shift) == prefix;
+        const uint32_t m = __ballot_sync(kFull, in_bin);
+        if (m) {
+            uint32_t pos = 0;
+            if (lane == 0) pos = atomicAdd(&sm.nres, (uint32_t)__popc(m));
+            pos = __shfl_sync(kFull, pos, 0) + __popc(m & ((1u << lane) - 1u));
+            if (in_bin && pos < kRankDirect) bin_el[pos] = x[k];
+        }
+    }
+    __syncthreads();
+    const uint32_t nr = sm.nres < kRankDirect ? sm.nres : kRankDirect;
+    if (sm.nres != eq && t == 0) atomicOr(status, kStatusCandOverflow);
+    if ((uint32_t)t < nr) {
+        const uint64_t ck = bin_el[t];
+        uint32_t better = 0;
+        for (uint32_t j = 0; j < nr; ++j) better += bin_el[j] > ck ? 1u : 0u;
+        if (better == need - 1) sm.thr = ck;
+    }
+    __syncthreads();
+    return sm.thr;
+}
+
+// Slots of the winners (candidates >= T) in candidate order, for candidates in
+// registers as for refine_threshold: slot[k] of candidate kRegCand t + k (-1
+// for a non-winner). Returns the number of winners. One barrier.
+__device__ __forceinline__ uint32_t winner_slots(const uint64_t (&x)[kRegCand], uint64_t T, int32_t (&slot)[kRegCand],
+                                                 uint32_t* scratch) {
+    bool f[kRegCand];
+    uint32_t cnt = 0;
+#pragma unroll
+    for (int k = 0; k < kRegCand; ++k) {
+        f[k] = x[k] != 0 && x[k] >= T;
+        cnt += f[k] ? 1u : 0u;
+    }
+    uint32_t total;
+    uint32_t at = block_excl_scan(cnt, total, scratch);
+#pragma unroll
+    for (int k = 0; k < kRegCand; ++k) {
+        slot[k] = f[k] ? (int32_t)at : -1;
+        at += f[k] ? 1u : 0u;
+    }
+    return total;
+}
+
+// Sort 512 values in descending order, one per thread (bitonic network): the
+// strides below 32 exchange through warp shuffles, the larger ones through
+// shared memory (two 512-entry buffers of `buf`, alternating: one barrier per
+// stage, and every access of a warp is to consecutive words). Returns the
+// value of rank threadIdx.x.
+__device__ __forceinline__ uint64_t bitonic512_desc(uint64_t x, uint64_t* buf) {
+    const uint32_t t = threadIdx.x;
+    int b = 0;
+#pragma unroll
+    for (uint32_t k = 2; k <= 512; k <<= 1) {
+#pragma unroll
+        for (uint32_t j = k >> 1; j > 0; j >>= 1) {
+            uint64_t y;
+            if (j >= 32) {
+                buf[b * 512 + t] = x;
+                __syncthreads();
+                y = buf[b * 512 + (t ^ j)];
+                b ^= 1;
+            } else {
+                y = __shfl_xor_sync(kFull, x, j);
+            }
+            // The lower position of a pair keeps the larger value in blocks
+            // (of k) sorted descending, the smaller in the others.
+            const bool keep_max = ((t & j) == 0) == ((t & k) == 0);
+            x = keep_max ? (x > y ? x : y) : (x < y ? x : y);
+        }
+    }
+    return x;
+}
+
+// sel[0, 512) holds the winners' composites in any order, zero past the last:
+// returns the winner of slot threadIdx.x in index order (zero past the last).
+// Uses `buf` (1024 entries) for the sort; sel is read once per thread.
+__device__ __forceinline__ uint64_t winner_by_index(const uint64_t* sel, uint64_t* buf) {
+    const uint64_t c = sel[threadIdx.x];
+    // ~index in the high word: descending order is ascending index; zero last.
+    uint64_t k = c ? ((c << 32) | (c >> 32)) : 0ull;
+    k = bitonic512_desc(k, buf);
+    return k ? ((k << 32) | (k >> 32)) : 0ull;
+}
+
+// The row's winners from the gathered candidates after the collection and a
+// cluster barrier: sel[s] receives the composite of the winner of slot s
+// (index order), zero past the last, and idx[s - first] the index of each
+// winner whose slot is in [first, first + 128). sel is zero and idx -1 on
+// entry. When some CTA had more than kCandCap candidates, or they are more
+// than the registers hold, the row is refined from its gathered candidates or
+// its full score array instead, and its winners sorted by index. Returns the
+// number of winners. Every CTA that calls this computes the same result.
+__device__ __forceinline__ uint32_t select_slots(const Gathered& g, const float* s, uint32_t L, uint32_t width,
+                                                 GatherSmem& sm, const uint64_t* regions, uint64_t* sel,
+                                                 int32_t* idx, uint32_t first, uint32_t* status) {
+    const int t = threadIdx.x;
+    RegionSource src;
+    src.c = regions;
+    uint32_t n = 0;
+    bool fits = g.fast;
+#pragma unroll
+    for (int r = 0; r < kCluster; ++r) {
+        src.b[r] = n;
+        const uint32_t k = sm.count[r];
+        fits = fits && k <= kCandCap;
+        n += k;
+    }
+    src.b[kCluster] = n;
+    BinPick l0f = g.l0;
+    l0f.bin = (int)g.b0;
+    if (fits) {
+        const uint32_t expect = g.take_all ? g.l0.total : g.l0.gt + g.l0.eq;
+        if (n != expect && t == 0) atomicOr(status, kStatusCandOverflow);
+    }
+    if (fits && n <= (uint32_t)kThreads * kRegCand) {
+        uint64_t x[kRegCand];
+#pragma unroll
+        for (int k = 0; k < kRegCand; ++k) {
+            const uint32_t i = (uint32_t)(kRegCand * t + k);
+            x[k] = 0;
+            if (i < n) src.get(i, x[k]);
+        }
+        const uint64_t T = refine_threshold(x, refine_from_level0(l0f, width), sm, status);
+        int32_t slot[kRegCand];
+        uint32_t nsel = winner_slots(x, T, slot, sm.scan[0]);
+        if (nsel > width) {
+            if (t == 0) atomicOr(status, kStatusCandOverflow);
+            nsel = width;
+        }
+#pragma unroll
+        for (int k = 0; k < kRegCand; ++k)
+            if (slot[k] >= 0 && (uint32_t)slot[k] < nsel) {
+                sel[slot[k]] = x[k];
+                if ((uint32_t)slot[k] - first < kChunkSlotsSel) idx[slot[k] - first] = (int32_t)(~(uint32_t)x[k]);
+            }
+        return nsel;
+    }
+    // The general path: refine (gathered candidates or the full row), then
+    // order the winners by index.
+    const uint32_t nsel = fits ? finish_row(src, refine_from_level0(l0f, width), width, sm, sel, status)
+                               : finish_row(RowSource{s, L}, refine_from_level0(g.l0, width), width, sm, sel, status);
+    const uint64_t c = winner_by_index(sel, reinterpret_cast<uint64_t*>(sm.h));
+    __syncthreads();  // every thread has read its entry of sel
+    sel[t] = c;
+    if (c != 0 && (uint32_t)t - first < kChunkSlotsSel) idx[t - first] = (int32_t)(~(uint32_t)c);
+    return nsel;
 }
 
 }  // namespace rowsel

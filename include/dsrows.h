@@ -177,6 +177,9 @@ int ds_rows_topk_static(const ds_row_set_t* set, const float* scores, size_t sco
  *   out[q_row, h, :] = bf16( sum_t exp(l_t - m) * KV_e[i_t, :] / den )
  * The sink has no value row. A non-finite sink, q element or selected KV
  * element, an overflowed logit or den <= 0 zeroes the head (fail closed).
+ * The sums run over the row's valid indices in ascending order (duplicates
+ * kept), so the result does not depend on the order of the indices within
+ * [index_offset, index_offset + width): it is a function of their multiset.
  *   q_attn      bf16 [Q, 64, 512]                              (16-B aligned)
  *   sinks       fp32; head h of entry e at sinks[q_row * sinks_row_stride + h];
  *               sinks_row_stride 0 shares one [64] vector, else >= 64.
@@ -197,8 +200,9 @@ int ds_rows_sparse_attn(const ds_row_set_t* set, const ds_bf16* q_attn, const fl
  * the workspace. Arguments as in the stages above; `indices` is optional
  * (NULL: the selection is not written out) and, when given, receives the
  * selected indices best first at each entry's index_offset (ranges must not
- * overlap). The attention takes the slots in that best-first order, so `out`
- * is bitwise what ds_rows_sparse_attn gives on those indices.
+ * overlap). The attention sums over the selected rows in ascending index
+ * order, as ds_rows_sparse_attn does, so `out` is bitwise what
+ * ds_rows_sparse_attn gives on those indices.
  */
 int ds_rows_decode(const ds_row_set_t* set, const ds_bf16* q_index, const float* w_index,
                    const ds_bf16* q_attn, const float* sinks, size_t sinks_row_stride,
