@@ -46,10 +46,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 struct Layout {
     size_t status = 0;  // u32 status word at offset 0
     size_t hist = 0, flags = 0, ctl_end = 0;
-    size_t pub = 0, part = 0, scores = 0, gmax = 0, total = 0;  // gmax 0: no group maxima
+    size_t pub = 0, part = 0, scores = 0, total = 0;
     uint32_t attn_chunks = 0;
     uint64_t score_stride = 0;  // floats per row of the decode scores
-    uint64_t gmax_stride = 0;   // words per row of the group maxima (one per 32 scores)
 };
 
 // `rows` table entries (up to kVRowsMax virtual rows for the multi-query
@@ -71,9 +70,7 @@ Layout make_layout(int rows, const ds_row_t* table, bool attention = true) {
     L.attn_chunks = chunks;
     L.scores = align256(L.part + 2 * (size_t)chunks * kPartFloats * 4);  // two head halves per chunk
     L.score_stride = ((uint64_t)max_len + 63) & ~uint64_t(63);
-    L.gmax = align256(L.scores + (size_t)rows * L.score_stride * 4);
-    L.gmax_stride = L.score_stride / 32;
-    L.total = align256(L.gmax + (size_t)rows * L.gmax_stride * 4);
+    L.total = align256(L.scores + (size_t)rows * L.score_stride * 4);
     return L;
 }
 
@@ -284,9 +281,9 @@ void split_ctas(const uint32_t* tile_begin, uint32_t* cta_begin, uint32_t segs, 
 
 template <class P>
 int fill_and_launch_indexer(P& p, int group, const ds_row_set_t* set, uint32_t query_len, const ds_bf16* q_index,
-                            const float* w_index, float* scores, uint64_t stride, uint32_t* hist, uint32_t* gmax,
-                            uint64_t gmax_stride, uint32_t* status, cudaStream_t stream, uint32_t inputs_ready,
-                            const uint32_t* valid, const void* side_src, void* side_dst, size_t side_bytes) {
+                            const float* w_index, float* scores, uint64_t stride, uint32_t* hist, uint32_t* status,
+                            cudaStream_t stream, uint32_t inputs_ready, const uint32_t* valid, const void* side_src,
+                            void* side_dst, size_t side_bytes) {
     int rc = get_encoder();
     if (rc) return rc;
     std::memset(&p, 0, sizeof(p));
@@ -324,8 +321,6 @@ int fill_and_launch_indexer(P& p, int group, const ds_row_set_t* set, uint32_t q
     p.w = w_index;
     p.scores = scores;
     p.hist = hist;
-    p.gmax = gmax;
-    p.gmax_stride = gmax_stride;
     p.status = status;
     p.score_stride = stride;
     p.inputs_ready = inputs_ready;
@@ -343,25 +338,20 @@ int fill_and_launch_indexer(P& p, int group, const ds_row_set_t* set, uint32_t q
     return err == cudaSuccess ? DS_OK : cuda_fail(err, "indexer launch");
 }
 
-// `gmax`: optional per-32-score maxima (see IndexerParamsT); `side_*`: an
-// optional copy the indexer makes for the attention.
+// `side_*`: an optional copy the indexer makes for the attention (see IndexerParamsT).
 int run_indexer(const ds_row_set_t* set, uint32_t query_len, const ds_bf16* q_index, const float* w_index,
-                float* scores, uint64_t stride, uint32_t* hist, uint32_t* gmax, uint64_t gmax_stride,
-                uint32_t* status, cudaStream_t stream, uint32_t inputs_ready, const uint32_t* valid = nullptr,
-                const void* side_src = nullptr, void* side_dst = nullptr, size_t side_bytes = 0) {
+                float* scores, uint64_t stride, uint32_t* hist, uint32_t* status, cudaStream_t stream,
+                uint32_t inputs_ready, const uint32_t* valid = nullptr, const void* side_src = nullptr,
+                void* side_dst = nullptr, size_t side_bytes = 0) {
     // The tables hold CUtensorMaps (~1.3-2.2 KB); built per call on the host.
     if (query_len == 1) {
         IndexerParams1 p;
-        return fill_and_launch_indexer(p, 1, set, query_len, q_index, w_index, scores, stride, hist, gmax, gmax_stride,
-                                       status, stream, inputs_ready, valid, side_src, side_dst, side_bytes);
+        return fill_and_launch_indexer(p, 1, set, query_len, q_index, w_index, scores, stride, hist, status, stream,
+                                       inputs_ready, valid, side_src, side_dst, side_bytes);
     }
     IndexerParamsG p;
-    return fill_and_launch_indexer(p, kIndexerGroup, set, query_len, q_index, w_index, scores, stride, hist, gmax,
-                                   gmax_stride, status, stream, inputs_ready, valid, side_src, side_dst, side_bytes);
-}
-
-uint32_t* layout_gmax(uint8_t* ws, const Layout& L) {
-    return L.gmax ? reinterpret_cast<uint32_t*>(ws + L.gmax) : nullptr;
+    return fill_and_launch_indexer(p, kIndexerGroup, set, query_len, q_index, w_index, scores, stride, hist, status,
+                                   stream, inputs_ready, valid, side_src, side_dst, side_bytes);
 }
 
 // The level-0 histogram (with_hist) and the top-k kernel's selection
@@ -386,8 +376,6 @@ int run_topk(const ds_row_set_t* set, const float* scores, uint64_t stride, int3
     p.score_stride = stride;
     p.out = out;
     p.hist = reinterpret_cast<uint32_t*>(ws + L.hist);
-    p.gmax = layout_gmax(ws, L);
-    p.gmax_stride = L.gmax_stride;
     p.status = reinterpret_cast<uint32_t*>(ws + L.status);
     p.rows = (uint32_t)set->rows;
     p.total_chunks = chunks;
@@ -423,8 +411,6 @@ int run_tail(const ds_row_set_t* set, const ds_bf16* q_attn, const float* sinks,
     tp.scores = scores;
     tp.score_stride = score_stride;
     tp.hist = reinterpret_cast<const uint32_t*>(ws + L.hist);
-    tp.gmax = layout_gmax(ws, L);
-    tp.gmax_stride = L.gmax_stride;
     tp.status = reinterpret_cast<uint32_t*>(ws + L.status);
     tp.q = reinterpret_cast<const __nv_bfloat16*>(q_attn);
     tp.q_after_wait = q_after_wait ? 1u : 0u;
@@ -597,8 +583,7 @@ int ds_rows_indexer_score(const ds_row_set_t* set, const ds_bf16* q_index, const
         if (score_stride < set->table[e].kv_len)
             return fail(DS_EINVAL, "score_stride %zu is shorter than row %d (kv_len %u)", score_stride, e,
                         set->table[e].kv_len);
-    return run_indexer(set, 1, q_index, w_index, scores, score_stride, nullptr, nullptr, 0, nullptr,
-                       (cudaStream_t)stream, 0);
+    return run_indexer(set, 1, q_index, w_index, scores, score_stride, nullptr, nullptr, (cudaStream_t)stream, 0);
 }
 
 int ds_rows_topk(const ds_row_set_t* set, const float* scores, size_t score_stride, int32_t* indices,
@@ -657,8 +642,7 @@ int ds_rows_decode(const ds_row_set_t* set, const ds_bf16* q_index, const float*
     float* scores = reinterpret_cast<float*>(ws + L.scores);
     uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
     uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
-    rc = run_indexer(set, 1, q_index, w_index, scores, L.score_stride, hist, layout_gmax(ws, L), L.gmax_stride,
-                     status, s, 1);
+    rc = run_indexer(set, 1, q_index, w_index, scores, L.score_stride, hist, status, s, 1);
     if (rc) return rc;
     // Selection and attention in one kernel: one 8-CTA cluster per row keeps the
     // selection on chip and attends over it in best-first order, the order of
@@ -765,8 +749,8 @@ int ds_rows_decode_host(const ds_row_set_t* set, const ds_bf16* h_q_index, const
     // launch) and waits for that kernel (griddepcontrol.wait) before its first
     // query and key loads and before it reads the head weights.
     rc = run_indexer(set, 1, d_qI, d_wI, scores, L.score_stride, reinterpret_cast<uint32_t*>(ws + L.hist),
-                     layout_gmax(ws, L), L.gmax_stride, reinterpret_cast<uint32_t*>(ws + L.status), s,
-                     kernel_copy ? 2u : 1u, nullptr, m_qA, ws + S.q_attn, m_qA ? nq * qA_row * 2 : 0);
+                     reinterpret_cast<uint32_t*>(ws + L.status), s, kernel_copy ? 2u : 1u, nullptr, m_qA,
+                     ws + S.q_attn, m_qA ? nq * qA_row * 2 : 0);
     if (rc) return rc;
     rc = run_tail(set, d_qA, d_sk, sinks_row_stride, scale, d_out, d_inv, scores, L.score_stride, nullptr, d_idx, ws,
                   L, s, m_qA != nullptr);
@@ -857,8 +841,8 @@ int ds_rows_indexer_topk_queries(int rows, const ds_indexer_row_t* table, uint32
     if (err != cudaSuccess) return cuda_fail(err, "workspace clear");
     float* scores = reinterpret_cast<float*>(ws + L.scores);
     rc = run_indexer(&kset, query_len, q_index, w_index, scores, L.score_stride,
-                     reinterpret_cast<uint32_t*>(ws + L.hist), layout_gmax(ws, L), L.gmax_stride,
-                     reinterpret_cast<uint32_t*>(ws + L.status), s, 1, valid);
+                     reinterpret_cast<uint32_t*>(ws + L.hist), reinterpret_cast<uint32_t*>(ws + L.status), s, 1,
+                     valid);
     if (rc) return rc;
     // The indexer built the level-0 histogram of each query's valid scores.
     return run_select(&sset, scores, L.score_stride, indices, ws, L, false, s, offsets);

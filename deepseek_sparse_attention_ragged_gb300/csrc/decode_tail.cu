@@ -216,9 +216,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     if (p.given == nullptr) {
         // ---- select: gather the candidates, then every CTA selects the same winners
         const float* s = p.scores + (size_t)e * p.score_stride;
-        const Gathered gat = select_collect_all(s, L, W, p.hist + (size_t)e * kHistBins,
-                                                p.gmax ? p.gmax + (size_t)e * p.gmax_stride : nullptr, rank, gs,
-                                                regions);
+        const Gathered gat = select_collect_all(s, L, W, p.hist + (size_t)e * kHistBins, rank, gs, regions);
         cluster.sync();  // every CTA's candidates are in every CTA; no CTA touches
                          // another's shared memory after this barrier
         nsel = select_slots(gat, s, L, W, gs, regions, sel, idx_s, first, p.status);

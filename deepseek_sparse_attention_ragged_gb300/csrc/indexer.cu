@@ -338,13 +338,17 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
             for (int i = 0; i < nq; ++i) {
                 uint32_t* dst = p.hist + (size_t)(p.seg_vrow[sg] + i) * kHistBins;
                 if (G == 1) {
-                    for (int b = ep_tid; b < kHistBins; b += kEpiThreads) {
-                        const uint32_t v = hist_s[b];
-                        if (v) {
-                            atomicAdd(dst + b, v);
-                            hist_s[b] = 0;
+                    // All of this thread's bins are read first, so the reads overlap.
+                    constexpr int kPer = kHistBins / kEpiThreads;
+                    uint32_t hv[kPer];
+#pragma unroll
+                    for (int k = 0; k < kPer; ++k) hv[k] = hist_s[ep_tid + k * kEpiThreads];
+#pragma unroll
+                    for (int k = 0; k < kPer; ++k)
+                        if (hv[k]) {
+                            atomicAdd(dst + ep_tid + k * kEpiThreads, hv[k]);
+                            hist_s[ep_tid + k * kEpiThreads] = 0;
                         }
-                    }
                 } else {
                     uint32_t* h = hist_s + i * (kHistBins / 2);
                     for (int b = ep_tid; b < kHistBins / 2; b += kEpiThreads) {
@@ -420,20 +424,14 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
                 if (k >= nk) break;
                 const int vr = G == 1 ? sg : p.seg_vrow[sg] + q0 + k;
                 const float sc = head_sum(v[k], G == 1 ? wr : nullptr, w_s + (q0 + k) * kIdxHeads);
-                const bool in = j < p.valid[vr];
-                const bool fin = finite_f(sc);
-                if (in) {
+                if (j < p.valid[vr]) {
+                    const bool fin = finite_f(sc);
                     st_global_hint(p.scores + (size_t)vr * p.score_stride + j, fin ? sc : -INFINITY, keep);
                     if (want_hist && fin) {
                         const uint32_t bin = score_key(sc) >> 21;
                         if (G == 1) atomicAdd(&hist_s[bin], 1u);
                         else atomicAdd(&hist_s[(q0 + k) * (kHistBins / 2) + (bin >> 1)], (bin & 1) ? 0x10000u : 1u);
                     }
-                }
-                if (p.gmax) {
-                    // The warp's 32 keys are one group: its largest score key.
-                    const uint32_t gm = __reduce_max_sync(0xFFFFFFFFu, in && fin ? score_key(sc) : 0u);
-                    if (lane == 0 && j < p.valid[vr]) p.gmax[(size_t)vr * p.gmax_stride + (j >> 5)] = gm;
                 }
             }
         }

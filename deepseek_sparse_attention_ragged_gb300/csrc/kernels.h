@@ -26,9 +26,6 @@ struct IndexerParamsT {
     const float* w;                 // [Q, 64]
     float* scores;                  // virtual row v at v * score_stride
     uint32_t* hist;                 // optional [vrows][2048] score-key histogram
-    uint32_t* gmax;                 // optional: the largest score key of each 32 keys (0 when none is
-                                    // finite), virtual row v at v * gmax_stride
-    uint64_t gmax_stride;
     uint32_t* status;               // device status word
     uint32_t inputs_ready;          // 1: every input was complete when the launch began (it follows an
                                     // ordinary launch), so loads may start before griddepcontrol.wait;
@@ -62,8 +59,6 @@ struct TopkParams {
     uint64_t score_stride;
     int32_t* out;          // indices; entry e at out_offset[e]
     uint32_t* hist;        // [8][2048] level 0 (top 11 key bits), zero before it is built
-    uint32_t* gmax;        // optional per-32-score maximum key, entry e at e * gmax_stride
-    uint64_t gmax_stride;
     uint32_t* status;
     uint32_t rows;
     uint32_t total_chunks;    // histogram CTAs (chunks of topk_chunk() scores)
@@ -82,8 +77,6 @@ struct TailParams {
     const float* scores;          // indexer scores, entry e at e * score_stride
     uint64_t score_stride;
     const uint32_t* hist;         // [8][2048] level-0 histogram built by the indexer
-    const uint32_t* gmax;         // optional per-32-score maximum key (see IndexerParamsT)
-    uint64_t gmax_stride;
     uint32_t* status;
     const __nv_bfloat16* kv[DS_ROWS_MAX];
     const __nv_bfloat16* q;       // [Q, 64, 512]

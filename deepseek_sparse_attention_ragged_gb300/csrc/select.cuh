@@ -415,20 +415,6 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t& total,
     return before + inc - v;
 }
 
-// x[b] for a run-time b < 32 without indexing registers: a tree of selects.
-__device__ __forceinline__ float select32(const float (&x)[32], uint32_t b) {
-    float a16[16], a8[8], a4[4], a2[2];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) a16[k] = (b & 16) ? x[k + 16] : x[k];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) a8[k] = (b & 8) ? a16[k + 8] : a16[k];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) a4[k] = (b & 4) ? a8[k + 4] : a8[k];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) a2[k] = (b & 2) ? a4[k + 2] : a4[k];
-    return (b & 1) ? a2[1] : a2[0];
-}
-
 // The cluster's candidates in this CTA's shared memory: region r (kCandCap
 // composites from its start) holds the count[r] contributed by CTA r, in index
 // order; position i of the source is in the region r with b[r] <= i < b[r + 1],
@@ -458,33 +444,47 @@ struct Gathered {
 // picks the level-0 threshold bin from the row's histogram and compacts the
 // candidates of its slice of the row (finite scores whose top 11 key bits are
 // >= that bin), as composites in index order, into region `rank` of `regions`
-// in its own shared memory. Scores are read in groups of 32 consecutive keys,
-// one group per thread, and with `gmax` (the largest score key of each group)
-// only the groups that hold a candidate are read. Then each CTA copies its
-// candidates, densely, into region `rank` of every other CTA of the cluster,
-// and its count into count[rank] of every CTA. Before the call every CTA has
-// passed a cluster barrier; after it a cluster barrier makes every CTA's
-// candidates visible to all. h is left zero.
+// in its own shared memory (a slice is a multiple of 128 scores). The slice's
+// first 16384 scores are loaded with the histogram, before the threshold is
+// known; warp w holds scores
+// [1024 w, 1024 w + 1024) of a batch, thread t of it [128 i + 4 t, +4) for
+// i < 8, so every load of a warp is 512 contiguous bytes. Then each CTA copies
+// its candidates, densely, into region `rank` of every other CTA of the
+// cluster, and its count into count[rank] of every CTA. Before the call every
+// CTA has passed a cluster barrier; after it a cluster barrier makes every
+// CTA's candidates visible to all. h is left zero.
 __device__ __forceinline__ Gathered select_collect_all(const float* s, uint32_t L, uint32_t width,
-                                                       const uint32_t* hist_row, const uint32_t* gmax,
-                                                       uint32_t rank, GatherSmem& sm, uint64_t* regions) {
-    const int t = threadIdx.x;
-    // This CTA's slice: a multiple of 2048 scores; a batch is 512 groups of 32.
-    constexpr uint32_t kGroup = 32, kBatchScores = kGroup * kThreads;
-    const uint32_t per = (((L + kCluster - 1) / kCluster) + 2047) & ~2047u;
+                                                       const uint32_t* hist_row, uint32_t rank, GatherSmem& sm,
+                                                       uint64_t* regions) {
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    constexpr int kSub = 8;                                   // 128-score sub-blocks per warp and batch
+    constexpr uint32_t kBatchScores = 128 * kSub * (kThreads / 32);  // 16384
+    // A multiple of 128 scores per CTA: short rows spread over the cluster.
+    const uint32_t per = (((L + kCluster - 1) / kCluster) + 127) & ~127u;
     const uint32_t begin = min(L, rank * per);
     const uint32_t end = min(L, begin + per);
     const bool vec = (reinterpret_cast<uintptr_t>(s) & 15) == 0;
-    // The histogram, and the first batch's group maxima, in one round trip.
+    float v[kSub * 4];
+    auto load_batch = [&](uint32_t base) {
+#pragma unroll
+        for (int i = 0; i < kSub; ++i) {
+            const uint32_t j = base + 1024 * w + 128 * i + 4 * lane;
+            if (vec && j + 3 < end) {
+                const float4 q = __ldcg(reinterpret_cast<const float4*>(s + j));
+                v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    v[4 * i + u] = j + u < end ? __ldcg(s + j + u) : __int_as_float(0x7FC00000);
+            }
+        }
+    };
+    // The histogram first (the threshold pick waits for it), then the slice's
+    // scores, which stay in flight while the threshold is picked.
     uint32_t hv[kHistBins / kThreads];
 #pragma unroll
     for (int i = 0; i < kHistBins / kThreads; ++i) hv[i] = __ldcg(hist_row + t + i * kThreads);
-    auto group_max = [&](uint32_t base) -> uint32_t {
-        const uint32_t j = base + kGroup * t;
-        if (j >= end) return 0u;
-        return gmax ? __ldcg(gmax + (j >> 5)) : 0xFFFFFFFFu;
-    };
-    uint32_t gm = group_max(begin);
+    load_batch(begin);
 #pragma unroll
     for (int i = 0; i < kHistBins / kThreads; ++i) sm.h[t + i * kThreads] = hv[i];
     __syncthreads();
@@ -502,48 +502,47 @@ __device__ __forceinline__ Gathered select_collect_all(const float* s, uint32_t 
     uint64_t* own = regions + (size_t)rank * kCandCap;
     uint32_t n_local = 0;
     if (r.fast) {
-        // A finite score is a candidate when its key is >= k0 = b0 << 21; the
-        // same test on the float: score >= the smallest score of bin b0
-        // (-0.0 ties +0.0).
-        const uint32_t k0 = r.b0 << 21;
+        // The smallest score whose key falls in bin b0: for finite scores,
+        // key >= b0 << 21 is the same as score >= this value (-0.0 ties +0.0).
         float thr = -FLT_MAX;
         if (!r.take_all) {
+            const uint32_t k0 = r.b0 << 21;
             const float f = __uint_as_float((k0 & 0x80000000u) ? (k0 & 0x7FFFFFFFu) : ~k0);
             if (finite_f(f)) thr = f;
         }
+        const uint32_t below = (1u << lane) - 1u;
         int par = 0;
         for (uint32_t base = begin; base < end; base += kBatchScores) {
-            if (base != begin) gm = group_max(base);
-            const uint32_t j0 = base + kGroup * t;
-            uint32_t take = 0;
-            float v[kGroup];
-            if (j0 < end && gm >= k0) {
+            if (base != begin) load_batch(base);
+            // Within the warp, index order is (i, lane, u): ballots per (i, u).
+            uint32_t bal[kSub * 4];
+            uint32_t cnt = 0;
 #pragma unroll
-                for (int i = 0; i < kGroup / 4; ++i) {
-                    const uint32_t j = j0 + 4 * i;
-                    if (vec && j + 3 < end) {
-                        const float4 q = __ldcg(reinterpret_cast<const float4*>(s + j));
-                        v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
-                    } else {
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            v[4 * i + u] = j + u < end ? __ldcg(s + j + u) : __int_as_float(0x7FC00000);
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < kGroup; ++i) take |= (v[i] >= thr && v[i] < INFINITY) ? (1u << i) : 0u;
+            for (int i = 0; i < kSub * 4; ++i) {
+                bal[i] = __ballot_sync(kFull, v[i] >= thr && v[i] < INFINITY);
+                cnt += __popc(bal[i]);
             }
-            // Positions in index order: this thread's group follows the groups
-            // of the threads before it.
+            // The warp's candidates follow those of the warps before it.
             uint32_t total;
-            uint32_t at = n_local + block_excl_scan((uint32_t)__popc(take), total, sm.scan[par]);
+            uint32_t at = n_local + block_excl_scan(lane == 0 ? cnt : 0u, total, sm.scan[par]);
+            at = __shfl_sync(kFull, at, 0);
             par ^= 1;
             n_local += total;
-            while (take) {
-                const uint32_t b = (uint32_t)__ffs(take) - 1;
-                take &= take - 1;
-                if (at < kCandCap) own[at] = composite(score_key(select32(v, b)), j0 + b);
-                ++at;
+#pragma unroll
+            for (int i = 0; i < kSub; ++i) {
+                const uint32_t b0 = bal[4 * i], b1 = bal[4 * i + 1], b2 = bal[4 * i + 2], b3 = bal[4 * i + 3];
+                if (b0 | b1 | b2 | b3) {  // warp-uniform; the stores below are predicated, not branched
+                    uint32_t pos = at + __popc(b0 & below) + __popc(b1 & below) + __popc(b2 & below) +
+                                   __popc(b3 & below);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t bit = (bal[4 * i + u] >> lane) & 1u;
+                        const uint64_t c = composite(score_key(v[4 * i + u]), base + 1024 * w + 128 * i + 4 * lane + u);
+                        if (bit != 0 && pos < kCandCap) own[pos] = c;
+                        pos += bit;
+                    }
+                    at += __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
+                }
             }
         }
     }

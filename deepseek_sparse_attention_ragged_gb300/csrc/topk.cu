@@ -67,15 +67,8 @@ __global__ void __launch_bounds__(kThreads) topk_hist_kernel(const TopkParams p)
         v[i] = j < end ? s[j] : __int_as_float(0x7FC00000);
     }
 #pragma unroll
-    for (int i = 0; i < kChunk / kThreads; ++i) {
+    for (int i = 0; i < kChunk / kThreads; ++i)
         if (finite_f(v[i])) atomicAdd(&h[score_key(v[i]) >> 21], 1u);
-        if (p.gmax) {
-            // A warp's 32 scores of step i are one group: its largest score key.
-            const uint32_t j = begin + threadIdx.x + i * kThreads;
-            const uint32_t gm = __reduce_max_sync(0xFFFFFFFFu, finite_f(v[i]) ? score_key(v[i]) : 0u);
-            if ((threadIdx.x & 31) == 0 && j < end) p.gmax[(size_t)e * p.gmax_stride + (j >> 5)] = gm;
-        }
-    }
     __syncthreads();
     for (int i = threadIdx.x; i < kHistBins; i += kThreads)
         if (h[i]) atomicAdd(&p.hist[(size_t)e * kHistBins + i], h[i]);
