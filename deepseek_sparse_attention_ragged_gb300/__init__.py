@@ -23,6 +23,7 @@ from . import build as _build
 __all__ = [
     "DsRowsError", "Row", "load", "build", "library_path",
     "ds_rows_workspace_bytes", "workspace", "ds_rows_indexer_score", "ds_rows_topk", "ds_rows_topk_static",
+    "topk_static_status",
     "ds_rows_sparse_attn", "ds_rows_decode", "ds_rows_version",
     "ds_rows_decode_host_workspace_bytes", "host_workspace", "ds_rows_decode_host",
     "IndexerRow", "ds_rows_indexer_topk_workspace_bytes", "indexer_topk_workspace", "ds_rows_indexer_topk",
@@ -109,6 +110,8 @@ def load():
     lib.ds_rows_topk.restype = i32
     lib.ds_rows_topk_static.argtypes = [rs, vp, sz, vp, vp]
     lib.ds_rows_topk_static.restype = i32
+    lib.ds_rows_topk_static_status.argtypes = [vp, vp]
+    lib.ds_rows_topk_static_status.restype = i32
     lib.ds_rows_sparse_attn.argtypes = [rs, vp, vp, sz, vp, ctypes.c_float, vp, u32p, vp, sz, vp]
     lib.ds_rows_sparse_attn.restype = i32
     lib.ds_rows_decode.argtypes = [rs, vp, vp, vp, vp, sz, ctypes.c_float, vp, vp, u32p, vp, sz, vp]
@@ -299,7 +302,8 @@ def ds_rows_topk(rows, scores, score_stride, indices, workspace_t, stream=None):
 def ds_rows_topk_static(rows, scores, score_stride, indices, stream=None):
     """ds_rows_topk without a workspace: for callers that cannot allocate device
     memory when they run this stage. The library keeps the scratch in one fixed
-    array per device; calls that overlap on the GPU must not share a device."""
+    array per device, shared by every call on that device: calls that overlap
+    on the GPU race on it, so order them (one stream, or events)."""
     lib = load()
     rl = _rows_list(rows)
     _require(scores, "scores", torch.float32, (len(rl) - 1) * score_stride + max(r[0] for r in rl))
@@ -308,6 +312,18 @@ def ds_rows_topk_static(rows, scores, score_stride, indices, stream=None):
     rs, keep = _rowset(tab, n)
     _check(lib, lib.ds_rows_topk_static(ctypes.byref(rs), _ptr(scores), int(score_stride), _ptr(indices),
                                         _stream(stream)))
+
+
+def topk_static_status(device=None, stream=None) -> int:
+    """The status word of ds_rows_topk_static on `device` (the STATUS_* bits of
+    the last call there). Reads 4 bytes back to the host, so it waits for the
+    work queued on `stream`."""
+    lib = load()
+    dev = torch.device(device if device is not None else "cuda")
+    word = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib, lib.ds_rows_topk_static_status(word.data_ptr(), _stream(stream)))
+        return int(word.item()) & 0xFFFFFFFF
 
 
 def _attn_checks(rl, q_attn, sinks, sinks_row_stride, out, kv, invalid):

@@ -116,7 +116,7 @@ int encode_rows128(CUtensorMap* map, const void* base, uint64_t rows, uint32_t b
 }
 
 // ---- validation ----------------------------------------------------------------
-enum Needs : unsigned { kNeedKeys = 1, kNeedKv = 2, kUniqueQ = 4, kDisjointOut = 8 };
+enum Needs : unsigned { kNeedKeys = 1, kNeedKv = 2, kUniqueQ = 4, kDisjointOut = 8, kFullWidth = 16 };
 
 int check_table(int rows, const ds_row_t* table) {
     if (rows < 1 || rows > DS_ROWS_MAX) return fail(DS_EINVAL, "rows must be 1..=%d, got %d", DS_ROWS_MAX, rows);
@@ -125,6 +125,7 @@ int check_table(int rows, const ds_row_t* table) {
         const ds_row_t& r = table[e];
         if (r.kv_len == 0 || r.width == 0) return fail(DS_EINVAL, "row %d: kv_len and width must be nonzero", e);
         if (r.width > DS_TOPK) return fail(DS_EINVAL, "row %d: width %u exceeds %d", e, r.width, DS_TOPK);
+        if (r.width > r.kv_len) return fail(DS_EINVAL, "row %d: width %u exceeds kv_len %u", e, r.width, r.kv_len);
         if ((uint64_t)r.index_offset + r.width > 0xFFFFFFFFull)
             return fail(DS_ESIZE, "row %d: index range exceeds u32", e);
         if ((uint64_t)r.q_row * DS_HEADS * DS_DIM > 0xFFFFFFFFFFull)
@@ -139,6 +140,12 @@ int check_set(const ds_row_set_t* set, unsigned needs) {
     if (rc) return rc;
     const int rows = set->rows;
     for (int e = 0; e < rows; ++e) {
+        if (needs & kFullWidth) {
+            const ds_row_t& r = set->table[e];
+            const uint32_t full = r.kv_len < (uint32_t)DS_TOPK ? r.kv_len : (uint32_t)DS_TOPK;
+            if (r.width != full)
+                return fail(DS_EINVAL, "row %d: width %u must be min(%d, kv_len) = %u", e, r.width, DS_TOPK, full);
+        }
         if (needs & kNeedKeys) {
             if (!set->index_keys || !set->index_keys[e]) return fail(DS_EINVAL, "row %d: indexer keys are NULL", e);
             if (!aligned16(set->index_keys[e])) return fail(DS_EALIGN, "row %d: indexer keys not 16-B aligned", e);
@@ -418,12 +425,13 @@ int run_tail(const ds_row_set_t* set, const ds_bf16* q_attn, const float* sinks,
     for (int e = 0; e < set->rows; ++e) tp.offset[e] = offsets ? offsets[e] : 0;
     tp.sinks = sinks;
     tp.sinks_row_stride = sinks_row_stride;
-    tp.part = reinterpret_cast<float*>(ws + L.part);
-    tp.flags = reinterpret_cast<uint32_t*>(ws + L.flags);
+    // Selection only: no partials, flags or published winners are touched.
+    tp.part = attend ? reinterpret_cast<float*>(ws + L.part) : nullptr;
+    tp.flags = attend ? reinterpret_cast<uint32_t*>(ws + L.flags) : nullptr;
     // With attention, the best-first index list is ranked by one more cluster
     // from the winners each row publishes in the workspace.
     tp.ranker = attend && indices && given == nullptr && L.pub ? 1u : 0u;
-    tp.pub = L.pub ? reinterpret_cast<uint64_t*>(ws + L.pub) : nullptr;
+    tp.pub = attend && L.pub ? reinterpret_cast<uint64_t*>(ws + L.pub) : nullptr;
     tp.out = reinterpret_cast<__nv_bfloat16*>(out);
     tp.invalid = invalid;
     tp.given = given;
@@ -588,7 +596,7 @@ int ds_rows_indexer_score(const ds_row_set_t* set, const ds_bf16* q_index, const
 
 int ds_rows_topk(const ds_row_set_t* set, const float* scores, size_t score_stride, int32_t* indices,
                  void* workspace, size_t workspace_bytes, void* stream) {
-    int rc = check_set(set, kDisjointOut);
+    int rc = check_set(set, kDisjointOut | kFullWidth);
     if (rc) return rc;
     if (!scores || !indices) return fail(DS_EINVAL, "scores and indices must be non-NULL");
     for (int e = 0; e < set->rows; ++e)
@@ -626,7 +634,7 @@ int ds_rows_sparse_attn(const ds_row_set_t* set, const ds_bf16* q_attn, const fl
 int ds_rows_decode(const ds_row_set_t* set, const ds_bf16* q_index, const float* w_index, const ds_bf16* q_attn,
                    const float* sinks, size_t sinks_row_stride, float scale, ds_bf16* out, int32_t* indices,
                    uint32_t* invalid, void* workspace, size_t workspace_bytes, void* stream) {
-    int rc = check_set(set, kNeedKeys | kNeedKv | kUniqueQ | (indices ? kDisjointOut : 0u));
+    int rc = check_set(set, kNeedKeys | kNeedKv | kUniqueQ | kFullWidth | (indices ? kDisjointOut : 0u));
     if (rc) return rc;
     rc = check_indexer_args(q_index, w_index);
     if (rc) return rc;
@@ -662,7 +670,7 @@ int ds_rows_decode_host(const ds_row_set_t* set, const ds_bf16* h_q_index, const
                         const ds_bf16* h_q_attn, const float* h_sinks, size_t sinks_row_stride, float scale,
                         ds_bf16* h_out, int32_t* h_indices, uint32_t* h_invalid, void* workspace,
                         size_t workspace_bytes, void* stream) {
-    int rc = check_set(set, kNeedKeys | kNeedKv | kUniqueQ | (h_indices ? kDisjointOut : 0u));
+    int rc = check_set(set, kNeedKeys | kNeedKv | kUniqueQ | kFullWidth | (h_indices ? kDisjointOut : 0u));
     if (rc) return rc;
     if (!h_q_index || !h_w_index || !h_q_attn || !h_sinks || !h_out)
         return fail(DS_EINVAL, "host q_index, w_index, q_attn, sinks and out must be non-NULL");
@@ -774,7 +782,7 @@ int ds_rows_decode_host(const ds_row_set_t* set, const ds_bf16* h_q_index, const
 
 int ds_rows_topk_static(const ds_row_set_t* set, const float* scores, size_t score_stride, int32_t* indices,
                         void* stream) {
-    int rc = check_set(set, kDisjointOut);
+    int rc = check_set(set, kDisjointOut | kFullWidth);
     if (rc) return rc;
     if (!scores || !indices) return fail(DS_EINVAL, "scores and indices must be non-NULL");
     for (int e = 0; e < set->rows; ++e)
@@ -787,6 +795,8 @@ int ds_rows_topk_static(const ds_row_set_t* set, const float* scores, size_t sco
     uint8_t* ws = nullptr;
     rc = topk_scratch(&ws);
     if (rc) return rc;
+    // The array holds only the status word and the histograms (no partials,
+    // flags or scores: the selection-only path touches neither).
     Layout L{};
     L.hist = kStaticHist;
     cudaStream_t s = (cudaStream_t)stream;
@@ -914,6 +924,16 @@ int ds_rows_selftest_bounded_wait(uint32_t* status, uint32_t* result, uint64_t b
         return fail(DS_EINVAL, "budget_ns must be 1e3..1e10, got %llu", (unsigned long long)budget_ns);
     const cudaError_t err = launch_wait_selftest(status, result, budget_ns, (cudaStream_t)stream);
     return err == cudaSuccess ? DS_OK : cuda_fail(err, "bounded-wait self-test launch");
+}
+
+int ds_rows_topk_static_status(uint32_t* status, void* stream) {
+    if (!status) return fail(DS_EINVAL, "status is NULL");
+    if (reinterpret_cast<uintptr_t>(status) & 3) return fail(DS_EALIGN, "status must be 4-byte aligned");
+    uint8_t* ws = nullptr;
+    const int rc = topk_scratch(&ws);
+    if (rc) return rc;
+    const cudaError_t err = cudaMemcpyAsync(status, ws, sizeof(uint32_t), cudaMemcpyDefault, (cudaStream_t)stream);
+    return err == cudaSuccess ? DS_OK : cuda_fail(err, "status copy");
 }
 
 const char* ds_rows_last_error(void) { return g_error.c_str(); }

@@ -142,8 +142,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t rank = cluster.block_rank();
     const int e = blockIdx.x / kCluster;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    uint32_t* const pub_flag = p.flags + kRowsMax * kHeads + kRowsMax;  // [8] winners published
-    uint32_t* const pub_n = reinterpret_cast<uint32_t*>(p.pub + (size_t)kRowsMax * kTopK);
+    // With attention: [8] "winners published" flags after the row flags, and the
+    // winners' numbers after the published winners.
+    auto pub_flag = [&](uint32_t r) { return p.flags + kRowsMax * kHeads + kRowsMax + r; };
+    auto pub_n = [&](uint32_t r) { return reinterpret_cast<uint32_t*>(p.pub + (size_t)kRowsMax * kTopK) + r; };
 
     if (e >= (int)p.rows) {
         // ---- one more cluster ranks the rows' winners (decode with attention):
@@ -155,7 +157,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t ok = 1;
         if (t == 0) {
             const uint64_t start = global_timer_ns();
-            while (ld_acquire_gpu(pub_flag + re) == 0)
+            while (ld_acquire_gpu(pub_flag(re)) == 0)
                 if (global_timer_ns() - start > kWaitBudgetNs) {
                     atomicOr(p.status, kStatusWaitTimeout);
                     ok = 0;
@@ -165,7 +167,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         ok = __syncthreads_and(t != 0 || ok);
         __threadfence();
         const uint64_t x0 = ok ? __ldcg(p.pub + (size_t)re * kTopK + t) : 0ull;
-        const uint32_t nsel = ok ? __ldcg(pub_n + re) : 0u;
+        const uint32_t nsel = ok ? __ldcg(pub_n(re)) : 0u;
         const uint64_t x = bitonic512_desc(x0, reinterpret_cast<uint64_t*>(gs.h));
         if ((uint32_t)t < p.width[re])
             p.indices[p.index_offset[re] + t] = (uint32_t)t < nsel ? (int32_t)(~(uint32_t)x) + p.offset[re] : -1;
@@ -237,10 +239,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     if (p.ranker && rank == 0) {
         // Publish the winners (index order) for the ranking cluster.
         p.pub[(size_t)e * kTopK + t] = sel[t];
-        if (t == 0) pub_n[e] = nsel;
+        if (t == 0) *pub_n(e) = nsel;
         __threadfence();
         __syncthreads();
-        if (t == 0) st_release_gpu(pub_flag + e, 1u);
+        if (t == 0) st_release_gpu(pub_flag(e), 1u);
     }
     // The gather of the chunk's KV rows starts now.
     const size_t part0_off = ((size_t)2 * p.chunk_begin[e] + (size_t)half * nchunks) * kPartFloats;

@@ -60,9 +60,12 @@ typedef uint16_t ds_bf16;
 /*
  * One row of a call (`DeepSeekSparseAttentionRow` plus the indexer's fields).
  *   kv_len       keys / KV rows in the row's caches (> 0).
- *   width        selected slots of the row, 1..512. The decode step uses
- *                min(512, kv_len); the top-k stage writes exactly `width`
- *                indices, -1 in slots past the row's finite scores.
+ *   width        selected slots of the row: 1 <= width <= min(512, kv_len).
+ *                The top-k stage and the decode step select exactly
+ *                min(512, kv_len) (DS_EINVAL otherwise) and write that many
+ *                indices, -1 in slots past the row's finite scores; the
+ *                attention stage takes any width in that range (the caller's
+ *                index list).
  *   index_offset element offset of the row's `width` int32 indices in the
  *                indices buffer.
  *   q_row        row of the [*, 64, 128] / [*, 64, 512] queries, the [*, 64]
@@ -101,7 +104,8 @@ typedef struct {
  *                           may be incomplete. Not expected in any input.
  * Read the word once the call has completed (for example a 4-byte
  * cudaMemcpyAsync on the same stream); the next call on the workspace clears
- * it. 0: neither happened. ds_rows_topk_static keeps its word internally.
+ * it. 0: neither happened. ds_rows_topk_static keeps its word in the
+ * library (ds_rows_topk_static_status reads it).
  */
 #define DS_STATUS_WAIT_TIMEOUT 1u
 #define DS_STATUS_OVERFLOW 2u
@@ -165,6 +169,18 @@ int ds_rows_topk(const ds_row_set_t* set, const float* scores, size_t score_stri
 #define DS_TOPK_STATIC_SCRATCH_BYTES 65792
 int ds_rows_topk_static(const ds_row_set_t* set, const float* scores, size_t score_stride,
                         int32_t* indices, void* stream);
+
+/*
+ * The status word of ds_rows_topk_static on the current device (DS_STATUS_*
+ * bits, as in a workspace's first word; each ds_rows_topk_static call clears
+ * it when it starts). Enqueues a 4-byte copy of the word on `stream` into
+ * `status` (device or page-locked host memory, 4-byte aligned); read it once
+ * the stream has passed this point. Allocates nothing; like the top-k call it
+ * shares the library's array, so a call on another stream that overlaps it
+ * races. DS_EINVAL for a NULL `status`, DS_ECUDA when the copy cannot be
+ * enqueued.
+ */
+int ds_rows_topk_static_status(uint32_t* status, void* stream);
 
 /*
  * (3)+(4) Gather and sink-softmax sparse attention

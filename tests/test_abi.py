@@ -132,6 +132,29 @@ def test_topk_overlapping_outputs(lib):
     assert rc == -1 and "overlap" in _err(lib)
 
 
+def test_width_contract(lib):
+    """Every call: width <= kv_len (no more slots than keys). The top-k and the
+    decode select exactly min(512, kv_len); the attention takes any width up to
+    that (a caller's shorter index list)."""
+    assert _attn(lib, [(5, 6, 0, 0)]) == -1 and "exceeds kv_len" in _err(lib)
+    assert lib.ds_rows_workspace_bytes(1, ds._table([(5, 6, 0, 0)])[0]) == 0
+    for row in ((600, 100, 0, 0), (300, 299, 0, 0)):
+        rs, keep = _set([row])
+        rc = lib.ds_rows_topk(ctypes.byref(rs), FAKE, 600, FAKE, FAKE, 1 << 30, None)
+        assert rc == -1 and "must be min(512, kv_len)" in _err(lib)
+        rc = lib.ds_rows_topk_static(ctypes.byref(rs), FAKE, 600, FAKE, None)
+        assert rc == -1 and "must be min(512, kv_len)" in _err(lib)
+        rc = lib.ds_rows_decode(ctypes.byref(rs), FAKE, FAKE, FAKE, FAKE, 0, ctypes.c_float(0.04), FAKE, None,
+                                None, FAKE, 1 << 30, None)
+        assert rc == -1 and "must be min(512, kv_len)" in _err(lib)
+    assert lib.ds_rows_workspace_bytes(1, ds._table([(600, 100, 0, 0)])[0]) > 0  # a valid attention table
+
+
+def test_topk_static_status_checks(lib):
+    assert lib.ds_rows_topk_static_status(None, None) == -1 and "status is NULL" in _err(lib)
+    assert lib.ds_rows_topk_static_status(FAKE + 2, None) == -3 and "4-byte aligned" in _err(lib)
+
+
 def test_score_stride(lib):
     rs, keep = _set([(600, 512, 0, 0)])
     rc = lib.ds_rows_indexer_score(ctypes.byref(rs), FAKE, FAKE, FAKE, 599, None)

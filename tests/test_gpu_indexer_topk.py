@@ -53,9 +53,11 @@ def positioned_rows(wl, valid, offsets):
 def run(wl, dev, rows, entries=None):
     entries = list(range(len(rows))) if entries is None else entries
     out = torch.full((512 * len(wl.rows),), -7, dtype=torch.int32, device="cuda")
-    ds.ds_rows_indexer_topk([rows[e] for e in entries], dev.q_index, dev.w_index, [dev.keys[e] for e in entries],
-                            out)
+    sel = [rows[e] for e in entries]
+    ws = ds.indexer_topk_workspace(sel, "cuda")
+    ds.ds_rows_indexer_topk(sel, dev.q_index, dev.w_index, [dev.keys[e] for e in entries], out, workspace_t=ws)
     torch.cuda.synchronize()
+    assert ds.workspace_status(ws) == 0
     return out.cpu().numpy()
 
 

@@ -2,6 +2,7 @@
 through the C-ABI, on the five benchmark workloads and stand-alone stage inputs.
 """
 
+import dataclasses
 import functools
 
 import numpy as np
@@ -50,6 +51,9 @@ def _row_inputs(wl, e):
 
 
 def run_decode(dev, rows=None, indices=True, invalid=True, stream=None):
+    """The decode of `rows` (all of dev's by default) into NaN-, -7- and
+    7-filled out, indices and invalid buffers; the workspace's status word must
+    read 0 afterwards (no bounded wait gave up, no selection check failed)."""
     rows = dev.rows if rows is None else rows
     nq = max(r.q_row for r in dev.rows) + 1
     out = torch.full((nq, 64, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
@@ -58,10 +62,21 @@ def run_decode(dev, rows=None, indices=True, invalid=True, stream=None):
     inv = torch.full((nq, 64), 7, dtype=torch.int32, device="cuda") if invalid else None
     keys = [dev.keys[dev.rows.index(r)] for r in rows]
     kv = [dev.kv[dev.rows.index(r)] for r in rows]
+    ws = ds.workspace(rows)
     ds.ds_rows_decode(rows, dev.q_index, dev.w_index, keys, dev.q_attn, kv, dev.sinks, dev.sinks_row_stride,
-                      dev.scale, out, indices=idx, invalid=inv, stream=stream)
+                      dev.scale, out, indices=idx, invalid=inv, workspace_t=ws, stream=stream)
     torch.cuda.synchronize()
+    assert ds.workspace_status(ws) == 0
     return out, idx, inv
+
+
+def untouched_indices(idx, rows):
+    """Every index slot outside the rows' [index_offset, index_offset + width)
+    ranges still holds the -7 fill (no write past a row's width)."""
+    mask = np.ones(idx.shape[0], bool)
+    for r in rows:
+        mask[r.index_offset: r.index_offset + r.width] = False
+    return np.all(idx[mask] == -7)
 
 
 # ---------------------------------------------------------------------------
@@ -112,10 +127,12 @@ def test_topk_exact(case):
     ws = ds.workspace(rows)
     ds.ds_rows_topk(rows, scores, stride, idx, ws)
     torch.cuda.synchronize()
+    assert ds.workspace_status(ws) == 0
     got = idx.cpu().numpy()
     for e, r in enumerate(rows):
         ref = oracle.topk(rows_s[e].astype(np.float64), r.width)
         np.testing.assert_array_equal(got[r.index_offset: r.index_offset + r.width], ref, err_msg=f"row {e}")
+    assert untouched_indices(got, rows)
 
 
 def test_topk_equal_scores_slow_path():
@@ -168,8 +185,11 @@ def test_sparse_attn(case):
     idx = torch.from_numpy(idx_h).cuda()
     out = torch.full((4, 64, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
     inv = torch.full((4, 64), 7, dtype=torch.int32, device="cuda")
-    ds.ds_rows_sparse_attn(rows, dev.q_attn, dev.sinks, 64, idx, dev.scale, out, dev.kv, invalid=inv)
+    ws = ds.workspace(rows)
+    ds.ds_rows_sparse_attn(rows, dev.q_attn, dev.sinks, 64, idx, dev.scale, out, dev.kv, invalid=inv,
+                           workspace_t=ws)
     torch.cuda.synchronize()
+    assert ds.workspace_status(ws) == 0
     got = out.float().cpu().numpy()
     ginv = inv.cpu().numpy()
     for e, r in enumerate(rows):
@@ -228,7 +248,39 @@ def test_decode(i):
                                                         wl.row_sinks(e), wl.scale)
         np.testing.assert_array_equal(ginv[r.q_row], rinv.astype(np.int32))
         check_out(got[r.q_row], expect, what=f"cfg{i} row{e}")
+    assert untouched_indices(gidx, wl.rows), "an index was written outside a row's [offset, offset + width)"
     print(f"cfg{i}: near-tie swaps {swaps}")
+
+
+@pytest.mark.parametrize("i", [1, 4])
+def test_decode_canaries_around_outputs(i):
+    """Entries on odd query rows (even rows belong to no entry) and index ranges
+    with gaps between them: the gaps keep their -7 fill, the unowned query rows
+    of out and invalid keep their NaN and 7 fills, and every entry's results
+    are bitwise those of the decode on the workload's own dense layout."""
+    wl, dev = cfg(i), cfg_dev(i)
+    R = wl.num_rows
+    rows = [workloads.Row(r.kv_len, r.width, 640 * e + 7, 2 * e + 1) for e, r in enumerate(wl.rows)]
+
+    def spread(t):
+        out = torch.zeros((2 * R,) + tuple(t.shape[1:]), dtype=t.dtype, device="cuda")
+        out[1::2] = t
+        return out
+
+    sinks = spread(dev.sinks) if dev.sinks_row_stride else dev.sinks
+    moved = dataclasses.replace(dev, rows=rows, q_index=spread(dev.q_index), w_index=spread(dev.w_index),
+                                q_attn=spread(dev.q_attn), sinks=sinks)
+    out, idx, inv = run_decode(moved)
+    ref_out, ref_idx, ref_inv = run_decode(dev)
+    got_idx = idx.cpu().numpy()
+    assert untouched_indices(got_idx, rows)
+    for e, (r, r0) in enumerate(zip(rows, wl.rows)):
+        assert torch.equal(out[r.q_row].view(torch.int16), ref_out[r0.q_row].view(torch.int16)), f"row {e} out"
+        assert torch.equal(inv[r.q_row], ref_inv[r0.q_row]), f"row {e} invalid"
+        assert torch.equal(idx[r.index_offset: r.index_offset + r.width],
+                           ref_idx[r0.index_offset: r0.index_offset + r0.width]), f"row {e} indices"
+    assert torch.isnan(out[0::2].float()).all(), "a query row no entry owns was written"
+    assert bool((inv[0::2] == 7).all()), "an invalid row no entry owns was written"
 
 
 @pytest.mark.parametrize("i", [0, 1, 2, 3, 4])
@@ -245,10 +297,10 @@ def test_joint_equals_single_row(i):
 
 def test_decode_stages_agree():
     """decode == indexer_score -> topk -> sparse_attn, bitwise. The decode's
-    indices output equals ds_rows_topk's (best first), and its attention takes
-    the slots in that order, so the stand-alone attention of those indices is
-    the decode's output bit for bit. The top-k is exactly the top-width of the
-    GPU's own scores."""
+    indices output equals ds_rows_topk's (best first); both attentions sum over
+    the selected rows in ascending index order, so the stand-alone attention of
+    those indices is the decode's output bit for bit. The top-k is exactly the
+    top-width of the GPU's own scores."""
     wl, dev = cfg(2), cfg_dev(2)
     out, idx, _ = run_decode(dev)
     stride = max(r.kv_len for r in wl.rows)

@@ -3,9 +3,11 @@
 ds_rows_topk_static exists for callers that cannot allocate device memory when
 they run the top-k stage (allocation-free graph or real-time code, or code that
 cannot reach the device allocator). It keeps its scratch in one array inside
-the library, so this test calls it twice in a row, on different scores, to show
-that each call starts from a clean state, and compares every result with
-ds_rows_topk through the C-ABI. The indices are integers: they must be equal.
+the library, so these tests call it twice in a row, on different scores, to
+show that each call starts from a clean state. They compare every result with
+ds_rows_topk through the C-ABI, and with the oracle's stable sort on scores
+with exact ties and non-finite values; the indices are integers, so they must
+be equal. The status word it keeps in the library reads 0 after each call.
 
 This file sorts last so that a run stopping at the first failure has already
 run every other test.
@@ -16,6 +18,7 @@ import pytest
 import torch
 
 import deepseek_sparse_attention_ragged_gb300 as ds
+import oracle
 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -48,10 +51,26 @@ def test_static_scratch_topk_matches_workspace_topk_twice():
         got = torch.full_like(want, -9)
         ds.ds_rows_topk(rows, scores, stride, want, ws)
         ds.ds_rows_topk_static(rows, scores, stride, got)
-        torch.cuda.synchronize()
+        assert ds.topk_static_status() == 0
+        assert ds.workspace_status(ws) == 0
         for r in rows:
             sl = slice(r.index_offset, r.index_offset + r.width)
             assert torch.equal(got[sl], want[sl]), f"call {call}, row kv_len {r.kv_len}"
+
+
+def test_static_scratch_topk_matches_the_oracle_twice():
+    lens = [4096, 1000, 512, 300, 1]
+    rows = [workloads.Row(L, min(512, L), 512 * e, e) for e, L in enumerate(lens)]
+    for call in range(2):
+        scores, stride = _scores(91 + call, lens, ties=True, nonfinite=True)
+        got = torch.full((512 * len(lens),), -9, dtype=torch.int32, device="cuda")
+        ds.ds_rows_topk_static(rows, scores, stride, got)
+        assert ds.topk_static_status() == 0
+        host, g = scores.cpu().numpy(), got.cpu().numpy()
+        for e, r in enumerate(rows):
+            want = oracle.topk(host[e, : r.kv_len], r.width)
+            np.testing.assert_array_equal(g[r.index_offset: r.index_offset + r.width], want,
+                                          err_msg=f"call {call}, row kv_len {r.kv_len}")
 
 
 def test_static_scratch_topk_rejects_too_many_rows():
