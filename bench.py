@@ -46,6 +46,11 @@ def parse():
     ap.add_argument("--config", type=int, default=CONFIG_INDEX)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="skip the other workloads' step latencies")
+    ap.add_argument("--case", default="decode",
+                    choices=["decode", "decode_steps", "topk", "indexer_topk", "indexer_queries", "decode_host",
+                             "sparse_attn"],
+                    help="decode: the benchmark; any other: run only that entry point on the workload "
+                         "(--warmup + --steps calls, no timing), for a profiler to capture its kernels")
     return ap.parse_args()
 
 
@@ -212,9 +217,9 @@ class ClockSampler:
 
 
 def clock_sampler(device):
-    """NVML polling (every 2 ms) when the library loads, else nvidia-smi (every 100 ms)."""
+    """NVML polling (every 0.2 ms) when the library loads, else nvidia-smi (every 100 ms)."""
     try:
-        return NvmlClockSampler(device)
+        return NvmlClockSampler(device, period_s=0.0002)
     except (OSError, AttributeError):
         return ClockSampler(device.index or 0)
 
@@ -297,9 +302,36 @@ def run_reference(args):
 # native arm
 # ---------------------------------------------------------------------------
 
-def other_configs(ds, workloads, to_device, device, stream, flush_l2, skip, steps=10):
-    """Flushed single-step latency of the decode on the other benchmark workloads."""
+def percentiles(xs):
+    """(p10, median, p90) of a list of numbers."""
+    xs = sorted(xs)
+    pick = lambda q: xs[min(len(xs) - 1, max(0, int(round(q * (len(xs) - 1)))))]
+    return pick(0.1), pick(0.5), pick(0.9)
+
+
+def graph_step_times(graph4, stream, graphs_timed, steps_per_graph=4):
+    """Per-step device times (ms) of back-to-back replays of a graph of
+    `steps_per_graph` consecutive steps: an event after every replay, the
+    interval divided by the steps it holds."""
     import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(graphs_timed + 1)]
+    with torch.cuda.stream(stream):
+        graph4.replay()
+        ev[0].record(stream)
+        for k in range(graphs_timed):
+            graph4.replay()
+            ev[k + 1].record(stream)
+    torch.cuda.synchronize()
+    return [ev[k].elapsed_time(ev[k + 1]) / steps_per_graph for k in range(graphs_timed)]
+
+
+def other_configs(ds, workloads, to_device, device, stream, flush_l2, skip, steps=10, graphs_timed=40):
+    """The decode on the other benchmark workloads: back to back from CUDA graphs
+    of four consecutive steps (four query sets), as `value` is timed, with the
+    p10 / median / p90 of the per-step times over graphs_timed x 4 steps; and
+    the median latency of single steps with L2 flushed before each."""
+    import torch
+    from workloads.device import bf16_tensor
     res = {}
     for i in range(5):
         if i == skip:
@@ -310,29 +342,48 @@ def other_configs(ds, workloads, to_device, device, stream, flush_l2, skip, step
         out = torch.empty((nq, 64, 512), dtype=torch.bfloat16, device=device)
         idx = torch.empty((wl.index_elements,), dtype=torch.int32, device=device)
         ws = ds.workspace(wl.rows, device)
+        qsets = [(dev.q_index, dev.w_index, dev.q_attn)]
+        for k in range(3):
+            qI, wI, qA = workloads.draw_queries(wl, 1000 + k)
+            qsets.append((bf16_tensor(qI, device), torch.from_numpy(wI).to(device), bf16_tensor(qA, device)))
 
-        def step():
-            ds.ds_rows_decode(dev.rows, dev.q_index, dev.w_index, dev.keys, dev.q_attn, dev.kv, dev.sinks,
-                              dev.sinks_row_stride, dev.scale, out, indices=idx, workspace_t=ws, stream=stream)
+        def step(k=0):
+            qI, wI, qA = qsets[k]
+            ds.ds_rows_decode(dev.rows, qI, wI, dev.keys, qA, dev.kv, dev.sinks, dev.sinks_row_stride, dev.scale,
+                              out, indices=idx, workspace_t=ws, stream=stream)
 
         with torch.cuda.stream(stream):
-            for _ in range(3):
-                step()
+            for k in range(4):
+                step(k)
         torch.cuda.synchronize(device)
+        g4 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g4, stream=stream):
+            for k in range(4):
+                step(k)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g4.replay()
+        per_step = graph_step_times(g4, stream, graphs_timed)
+        p10, p50, p90 = percentiles(per_step)
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         with torch.cuda.stream(stream):
             for k in range(steps):
                 flush_l2(k)
                 starts[k].record(stream)
-                step()
+                step(k % 4)
                 ends[k].record(stream)
         torch.cuda.synchronize(device)
-        ms = sorted(s.elapsed_time(e) for s, e in zip(starts, ends))[steps // 2]
-        res[str(i)] = {"workload": wl.name, "rows": wl.num_rows, "us_per_step_flushed_median": ms * 1e3,
-                       "rows_per_s": wl.num_rows / (ms / 1e3),
-                       "gbs": wl.algorithmic_bytes() / (ms / 1e3) / 1e9}
-        del dev, out, idx, ws
+        ms = percentiles([s.elapsed_time(e) for s, e in zip(starts, ends)])[1]
+        alg = wl.algorithmic_bytes()
+        res[str(i)] = {"workload": wl.name, "rows": wl.num_rows,
+                       "us_per_step": p50 * 1e3, "us_per_step_p10": p10 * 1e3, "us_per_step_p90": p90 * 1e3,
+                       "steps_timed": 4 * graphs_timed,
+                       "rows_per_s": wl.num_rows / (p50 / 1e3), "gbs": alg / (p50 / 1e3) / 1e9,
+                       "us_per_step_flushed_median": ms * 1e3,
+                       "launch": "back to back from CUDA graphs of 4 consecutive steps (as value); the flushed "
+                                 "figure is single steps with L2 flushed before each"}
+        del dev, out, idx, ws, g4, qsets
         torch.cuda.empty_cache()
     return res
 
@@ -422,6 +473,68 @@ def indexer_queries_timings(ds, workloads, wl, dev, device, stream, counts=(2, 4
     return res
 
 
+def run_case(args, ds, workloads, wl, dev, qsets, stream, device):
+    """One entry point on the workload, --warmup + --steps calls back to back and
+    no timing: the command a profiler wraps to capture that entry point's
+    kernels on the benchmark workload (or on --config)."""
+    import torch
+    from workloads.device import bf16_tensor
+    R = wl.num_rows
+    calls = max(1, args.warmup) + max(1, args.steps)
+    stride = max(r.kv_len for r in wl.rows)
+    if args.case == "decode_steps":
+        nq = max(r.q_row for r in wl.rows) + 1
+        out = torch.empty((nq, 64, 512), dtype=torch.bfloat16, device=device)
+        idx = torch.empty((wl.index_elements,), dtype=torch.int32, device=device)
+        ws = ds.workspace(wl.rows, device)
+        for k in range(calls):
+            qI, wI, qA = qsets[k % 4]
+            ds.ds_rows_decode(dev.rows, qI, wI, dev.keys, qA, dev.kv, dev.sinks, dev.sinks_row_stride, dev.scale,
+                              out, indices=idx, workspace_t=ws, stream=stream)
+    elif args.case in ("topk", "sparse_attn"):
+        scores = torch.empty((R, stride), dtype=torch.float32, device=device)
+        ds.ds_rows_indexer_score(dev.rows, dev.q_index, dev.w_index, dev.keys, scores, stride, stream=stream)
+        idx = torch.empty((wl.index_elements,), dtype=torch.int32, device=device)
+        ws = ds.workspace(wl.rows, device)
+        ds.ds_rows_topk(dev.rows, scores, stride, idx, ws, stream=stream)
+        nq = max(r.q_row for r in wl.rows) + 1
+        out = torch.empty((nq, 64, 512), dtype=torch.bfloat16, device=device)
+        for _ in range(calls):
+            if args.case == "topk":
+                ds.ds_rows_topk(dev.rows, scores, stride, idx, ws, stream=stream)
+            else:
+                ds.ds_rows_sparse_attn(dev.rows, dev.q_attn, dev.sinks, dev.sinks_row_stride, idx, dev.scale, out,
+                                       dev.kv, workspace_t=ws, stream=stream)
+    elif args.case == "indexer_topk":
+        rows = [ds.IndexerRow(r.kv_len, 4 * r.kv_len - 1, 0, r.q_row, 512 * e) for e, r in enumerate(wl.rows)]
+        pidx = torch.empty((512 * R,), dtype=torch.int32, device=device)
+        pws = ds.indexer_topk_workspace(rows, device)
+        for k in range(calls):
+            ds.ds_rows_indexer_topk(rows, qsets[k % 4][0], qsets[k % 4][1], dev.keys, pidx, workspace_t=pws,
+                                    stream=stream)
+    elif args.case == "indexer_queries":
+        Q = 4
+        qI, wI = workloads.draw_index_queries(wl, 900 + Q, R * Q)
+        q, w = bf16_tensor(qI, device), torch.from_numpy(wI).to(device)
+        rows = [ds.IndexerRow(r.kv_len, 4 * r.kv_len - Q, 0, e * Q, 512 * Q * e) for e, r in enumerate(wl.rows)]
+        qout = torch.empty((512 * Q * R,), dtype=torch.int32, device=device)
+        qws = ds.indexer_topk_workspace(rows, device, Q)
+        for _ in range(calls):
+            ds.ds_rows_indexer_topk_queries(rows, Q, q, w, dev.keys, qout, workspace_t=qws, stream=stream)
+    elif args.case == "decode_host":
+        h_sets = [tuple(t.cpu().pin_memory() for t in qs) for qs in qsets]
+        h_sk = dev.sinks.cpu().pin_memory()
+        nq = max(r.q_row for r in wl.rows) + 1
+        h_out = torch.empty((nq, 64, 512), dtype=torch.bfloat16).pin_memory()
+        hws = ds.host_workspace(wl.rows, dev.sinks_row_stride, device)
+        for k in range(calls):
+            qI, wI, qA = h_sets[k % 4]
+            ds.ds_rows_decode_host(dev.rows, qI, wI, dev.keys, qA, dev.kv, h_sk, dev.sinks_row_stride, dev.scale,
+                                   h_out, workspace_t=hws, stream=stream)
+    torch.cuda.synchronize(device)
+    print(json.dumps({"case": args.case, "calls": calls, "workload": wl.name}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -454,14 +567,6 @@ def main():
     idx = torch.empty((wl.index_elements,), dtype=torch.int32, device=device)
     ws = ds.workspace(wl.rows, device)
     stream = torch.cuda.Stream(device)
-    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device)
-    flush_read = torch.ones(128 * 2 ** 20, dtype=torch.int32, device=device)
-
-    def flush_l2(k):
-        # Write 512 MiB (evicts L2), then read 512 MiB so that the lines left in L2
-        # are clean and no write-back of the flush lands in the timed step.
-        flush.fill_(k & 0xFF)
-        flush_read.max()
 
     # Four query sets for the same caches (the workload's own and three more drawn
     # with its recipe): consecutive steps select different KV rows, as real
@@ -476,6 +581,19 @@ def main():
         qI, wI, qA = qsets[i]
         ds.ds_rows_decode(dev.rows, qI, wI, dev.keys, qA, dev.kv, dev.sinks, dev.sinks_row_stride, dev.scale, out,
                           indices=idx, workspace_t=ws, stream=stream)
+
+    if args.case != "decode":
+        run_case(args, ds, workloads, wl, dev, qsets, stream, device)
+        return
+
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=device)
+    flush_read = torch.ones(128 * 2 ** 20, dtype=torch.int32, device=device)
+
+    def flush_l2(k):
+        # Write 512 MiB (evicts L2), then read 512 MiB so that the lines left in L2
+        # are clean and no write-back of the flush lands in the timed step.
+        flush.fill_(k & 0xFF)
+        flush_read.max()
 
     def barrier():
         torch.cuda.synchronize(device)
@@ -521,6 +639,9 @@ def main():
             t_end.record(stream)
         barrier()
     total_ms = t_start.elapsed_time(t_end)
+    # The spread of the step time: the same graphs again, an event after each
+    # replay of four steps (outside the timed region above).
+    s10, s50, s90 = percentiles(graph_step_times(graph4, stream, max(10, args.steps // 4)))
 
     def flushed(run_step):
         """Mean latency of single steps with L2 flushed before each (write, then read)."""
@@ -574,6 +695,9 @@ def main():
     idx_ms = graph_ms_per_call(lambda i: ds.ds_rows_indexer_score(dev.rows, qsets[i][0], qsets[i][1], dev.keys,
                                                                   scores, stride, stream=stream))
     idx_bytes = sum(256 * r.kv_len + 4 * r.kv_len + 16384 + 256 for r in wl.rows)
+    # The step formula's share of the indexer: its keys and query (the score
+    # write is the stand-alone stage's own output, the head weights are small).
+    idx_bytes_alg = sum(256 * r.kv_len + 16384 for r in wl.rows)
     peak, peak_kind = peaks()
     idx_gbs = idx_bytes / (idx_ms / 1e3) / 1e9
     # DRAM bytes of one indexer launch on this workload, read + written, from an
@@ -666,7 +790,12 @@ def main():
             "roofline": {"kernel": "indexer_score_kernel", "bound": "hbm", "achieved": idx_gbs, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": idx_gbs / peak, "traffic": idx_traffic,
                          "bytes_per_launch": idx_bytes, "ms_per_launch": idx_ms,
+                         "bytes_per_launch_keys_and_query": idx_bytes_alg,
+                         "frac_keys_and_query": idx_bytes_alg / (idx_ms / 1e3) / 1e9 / peak,
                          "tensor": idx_tensor},
+            "spread": {"ms_per_step_p10": s10, "ms_per_step_median": s50, "ms_per_step_p90": s90,
+                       "steps": 4 * max(10, args.steps // 4),
+                       "how": "back-to-back replays of the 4-step graph, an event after each replay"},
             "e2e": {"value": job_rate(world, R, 1, e2e_ms), "unit": "rows/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": 3 * args.steps,

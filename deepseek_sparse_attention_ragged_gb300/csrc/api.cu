@@ -8,6 +8,7 @@
 // and alignment. Everything is checked before anything is enqueued.
 
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstdarg>
 #include <cstdio>
@@ -39,6 +40,15 @@ int cuda_fail(cudaError_t err, const char* what) {
 }
 
 constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// An NVTX range over the host-side enqueue of one stage ("dsrows.<stage>"), so
+// a profiler can attribute each launch to its stage; free without a tool.
+struct StageRange {
+    explicit StageRange(const char* name) { nvtxRangePushA(name); }
+    ~StageRange() { nvtxRangePop(); }
+    StageRange(const StageRange&) = delete;
+    StageRange& operator=(const StageRange&) = delete;
+};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
@@ -234,6 +244,11 @@ int check_workspace(const ds_row_set_t* set, void* ws, size_t bytes, const Layou
 }
 
 // ---- stage launchers ---------------------------------------------------------------
+cudaError_t launch_clear_stage(uint32_t* p, uint32_t words, cudaStream_t stream) {
+    StageRange range("dsrows.clear");
+    return launch_clear(p, words, stream);
+}
+
 // Entry e of `set` has query_len consecutive queries, virtual rows
 // v = e * query_len + j with query row q_row + j; with `valid`, virtual row v
 // scores only its keys j < valid[v] (the tensor map still spans the entry's
@@ -350,6 +365,7 @@ int run_indexer(const ds_row_set_t* set, uint32_t query_len, const ds_bf16* q_in
                 float* scores, uint64_t stride, uint32_t* hist, uint32_t* status, cudaStream_t stream,
                 uint32_t inputs_ready, const uint32_t* valid = nullptr, const void* side_src = nullptr,
                 void* side_dst = nullptr, size_t side_bytes = 0) {
+    StageRange range("dsrows.indexer");
     // The tables hold CUtensorMaps (~1.3-2.2 KB); built per call on the host.
     if (query_len == 1) {
         IndexerParams1 p;
@@ -367,6 +383,7 @@ int run_topk(const ds_row_set_t* set, const float* scores, uint64_t stride, int3
              uint8_t* ws, const Layout& L, bool with_hist, cudaStream_t stream,
              const int32_t* offsets = nullptr, bool select = true) {
     if (set->rows > kVRowsMax) return fail(DS_EINVAL, "too many top-k rows");
+    StageRange range("dsrows.topk");
     TopkParams p;
     std::memset(&p, 0, sizeof(p));
     const uint32_t chunk = topk_chunk();
@@ -402,6 +419,7 @@ int run_tail(const ds_row_set_t* set, const ds_bf16* q_attn, const float* sinks,
              float scale, ds_bf16* out, uint32_t* invalid, const float* scores, uint64_t score_stride,
              const int32_t* given, int32_t* indices, uint8_t* ws, const Layout& L, cudaStream_t stream,
              bool q_after_wait = false, bool attend = true, const int32_t* offsets = nullptr) {
+    StageRange range(attend ? (given ? "dsrows.attention" : "dsrows.select+attention") : "dsrows.select");
     TailParams tp;
     std::memset(&tp, 0, sizeof(tp));
     uint32_t chunks = 0;
@@ -608,7 +626,7 @@ int ds_rows_topk(const ds_row_set_t* set, const float* scores, size_t score_stri
     if (rc) return rc;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t err = launch_clear(reinterpret_cast<uint32_t*>(ws), (uint32_t)(L.ctl_end / 4), s);
+    cudaError_t err = launch_clear_stage(reinterpret_cast<uint32_t*>(ws), (uint32_t)(L.ctl_end / 4), s);
     if (err != cudaSuccess) return cuda_fail(err, "workspace clear");
     return run_select(set, scores, score_stride, indices, ws, L, true, s);
 }
@@ -626,7 +644,7 @@ int ds_rows_sparse_attn(const ds_row_set_t* set, const ds_bf16* q_attn, const fl
     if (rc) return rc;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t err = launch_clear(reinterpret_cast<uint32_t*>(ws), (uint32_t)(L.ctl_end / 4), s);
+    cudaError_t err = launch_clear_stage(reinterpret_cast<uint32_t*>(ws), (uint32_t)(L.ctl_end / 4), s);
     if (err != cudaSuccess) return cuda_fail(err, "workspace clear");
     return run_tail(set, q_attn, sinks, sinks_row_stride, scale, out, invalid, nullptr, 0, indices, nullptr, ws, L, s);
 }
@@ -645,7 +663,7 @@ int ds_rows_decode(const ds_row_set_t* set, const ds_bf16* q_index, const float*
     if (rc) return rc;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t err = launch_clear(reinterpret_cast<uint32_t*>(ws), (uint32_t)(L.ctl_end / 4), s);
+    cudaError_t err = launch_clear_stage(reinterpret_cast<uint32_t*>(ws), (uint32_t)(L.ctl_end / 4), s);
     if (err != cudaSuccess) return cuda_fail(err, "workspace clear");
     float* scores = reinterpret_cast<float*>(ws + L.scores);
     uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
@@ -847,7 +865,7 @@ int ds_rows_indexer_topk_queries(int rows, const ds_indexer_row_t* table, uint32
     if (rc) return rc;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t err = launch_clear(reinterpret_cast<uint32_t*>(ws), (uint32_t)(L.ctl_end / 4), s);
+    cudaError_t err = launch_clear_stage(reinterpret_cast<uint32_t*>(ws), (uint32_t)(L.ctl_end / 4), s);
     if (err != cudaSuccess) return cuda_fail(err, "workspace clear");
     float* scores = reinterpret_cast<float*>(ws + L.scores);
     rc = run_indexer(&kset, query_len, q_index, w_index, scores, L.score_stride,
