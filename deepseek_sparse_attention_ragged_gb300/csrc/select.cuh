@@ -376,7 +376,8 @@ __device__ __forceinline__ uint32_t select_finish(const Collected& c, const floa
 // is its place among the winners in index order (the attention's slot order).
 
 constexpr uint32_t kCandCap = 2048;  // candidates one CTA may contribute to its cluster
-constexpr int kRegCand = 4;          // candidates per thread held in registers by the refinement
+constexpr int kRegCandSmall = 4;     // candidates per thread in registers while they fit
+constexpr int kRegCand = 12;         // at most this many per thread, else the general path
 
 // State of the all-gather selection in each CTA of a row's cluster.
 struct GatherSmem {
@@ -564,12 +565,14 @@ __device__ __forceinline__ Gathered select_collect_all(const float* s, uint32_t 
     return r;
 }
 
-// The exact threshold of the winners among n <= kThreads * kRegCand gathered
-// candidates held in registers (x[k] is candidate kRegCand t + k, zero past n),
+// The exact threshold of the winners among the gathered candidates held in
+// registers, R per thread (each candidate in one x[k] of one thread, the
+// unused entries zero),
 // from the refinement state `st`: the winners are the candidates with a
 // composite >= the returned value (1 when every candidate is taken). h is zero
 // on entry.
-__device__ __forceinline__ uint64_t refine_threshold(const uint64_t (&x)[kRegCand], Refine st, GatherSmem& sm,
+template <int R>
+__device__ __forceinline__ uint64_t refine_threshold(const uint64_t (&x)[R], Refine st, GatherSmem& sm,
                                                      uint32_t* status) {
     const int t = threadIdx.x, lane = t & 31;
     if (st.take_all) return 1ull;
@@ -587,7 +590,7 @@ __device__ __forceinline__ uint64_t refine_threshold(const uint64_t (&x)[kRegCan
             __syncthreads();
         }
 #pragma unroll
-        for (int k = 0; k < kRegCand; ++k)
+        for (int k = 0; k < R; ++k)
             if (x[k] != 0 && (x[k] >> up_shift) == prefix) atomicAdd(&sm.h[(x[k] >> cur_shift) & mask], 1u);
         __syncthreads();
         const BinPick pk = pick_bin(sm.h, need, sm.pick[par], false);
@@ -614,7 +617,7 @@ __device__ __forceinline__ uint64_t refine_threshold(const uint64_t (&x)[kRegCan
     }
     __syncthreads();  // (every thread has read h in the last pick)
 #pragma unroll
-    for (int k = 0; k < kRegCand; ++k) {
+    for (int k = 0; k < R; ++k) {
         const bool in_bin = x[k] != 0 && (x[k] >> shift) == prefix;
         const uint32_t m = __ballot_sync(kFull, in_bin);
         if (m) {
@@ -638,21 +641,23 @@ __device__ __forceinline__ uint64_t refine_threshold(const uint64_t (&x)[kRegCan
 }
 
 // Slots of the winners (candidates >= T) in candidate order, for candidates in
-// registers as for refine_threshold: slot[k] of candidate kRegCand t + k (-1
-// for a non-winner). Returns the number of winners. One barrier.
-__device__ __forceinline__ uint32_t winner_slots(const uint64_t (&x)[kRegCand], uint64_t T, int32_t (&slot)[kRegCand],
+// registers as for refine_threshold, where thread t's candidates follow those
+// of threads < t and x[k] precedes x[k + 1]: slot[k] of x[k] (-1 for a
+// non-winner). Returns the number of winners. One barrier.
+template <int R>
+__device__ __forceinline__ uint32_t winner_slots(const uint64_t (&x)[R], uint64_t T, int32_t (&slot)[R],
                                                  uint32_t* scratch) {
-    bool f[kRegCand];
+    bool f[R];
     uint32_t cnt = 0;
 #pragma unroll
-    for (int k = 0; k < kRegCand; ++k) {
+    for (int k = 0; k < R; ++k) {
         f[k] = x[k] != 0 && x[k] >= T;
         cnt += f[k] ? 1u : 0u;
     }
     uint32_t total;
     uint32_t at = block_excl_scan(cnt, total, scratch);
 #pragma unroll
-    for (int k = 0; k < kRegCand; ++k) {
+    for (int k = 0; k < R; ++k) {
         slot[k] = f[k] ? (int32_t)at : -1;
         at += f[k] ? 1u : 0u;
     }
@@ -700,6 +705,37 @@ __device__ __forceinline__ uint64_t winner_by_index(const uint64_t* sel, uint64_
     return k ? ((k << 32) | (k >> 32)) : 0ull;
 }
 
+// The winners among n <= kThreads * R gathered candidates, held R per thread
+// in registers (thread t: candidates [R t, R t + R)), written as select_slots
+// does. Returns the number of winners.
+template <int R>
+__device__ __forceinline__ uint32_t select_in_registers(const RegionSource& src, uint32_t n, Refine st,
+                                                        uint32_t width, GatherSmem& sm, uint64_t* sel, int32_t* idx,
+                                                        uint32_t first, uint32_t* status) {
+    const int t = threadIdx.x;
+    uint64_t x[R];
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+        const uint32_t i = (uint32_t)(R * t + k);
+        x[k] = 0;
+        if (i < n) src.get(i, x[k]);
+    }
+    const uint64_t T = refine_threshold(x, st, sm, status);
+    int32_t slot[R];
+    uint32_t nsel = winner_slots(x, T, slot, sm.scan[0]);
+    if (nsel > width) {
+        if (t == 0) atomicOr(status, kStatusCandOverflow);
+        nsel = width;
+    }
+#pragma unroll
+    for (int k = 0; k < R; ++k)
+        if (slot[k] >= 0 && (uint32_t)slot[k] < nsel) {
+            sel[slot[k]] = x[k];
+            if ((uint32_t)slot[k] - first < kChunkSlotsSel) idx[slot[k] - first] = (int32_t)(~(uint32_t)x[k]);
+        }
+    return nsel;
+}
+
 // The row's winners from the gathered candidates after the collection and a
 // cluster barrier: sel[s] receives the composite of the winner of slot s
 // (index order), zero past the last, and idx[s - first] the index of each
@@ -730,29 +766,12 @@ __device__ __forceinline__ uint32_t select_slots(const Gathered& g, const float*
         const uint32_t expect = g.take_all ? g.l0.total : g.l0.gt + g.l0.eq;
         if (n != expect && t == 0) atomicOr(status, kStatusCandOverflow);
     }
-    if (fits && n <= (uint32_t)kThreads * kRegCand) {
-        uint64_t x[kRegCand];
-#pragma unroll
-        for (int k = 0; k < kRegCand; ++k) {
-            const uint32_t i = (uint32_t)(kRegCand * t + k);
-            x[k] = 0;
-            if (i < n) src.get(i, x[k]);
-        }
-        const uint64_t T = refine_threshold(x, refine_from_level0(l0f, width), sm, status);
-        int32_t slot[kRegCand];
-        uint32_t nsel = winner_slots(x, T, slot, sm.scan[0]);
-        if (nsel > width) {
-            if (t == 0) atomicOr(status, kStatusCandOverflow);
-            nsel = width;
-        }
-#pragma unroll
-        for (int k = 0; k < kRegCand; ++k)
-            if (slot[k] >= 0 && (uint32_t)slot[k] < nsel) {
-                sel[slot[k]] = x[k];
-                if ((uint32_t)slot[k] - first < kChunkSlotsSel) idx[slot[k] - first] = (int32_t)(~(uint32_t)x[k]);
-            }
-        return nsel;
-    }
+    if (fits && n <= (uint32_t)kThreads * kRegCandSmall)
+        return select_in_registers<kRegCandSmall>(src, n, refine_from_level0(l0f, width), width, sm, sel, idx, first,
+                                                  status);
+    if (fits && n <= (uint32_t)kThreads * kRegCand)
+        return select_in_registers<kRegCand>(src, n, refine_from_level0(l0f, width), width, sm, sel, idx, first,
+                                             status);
     // The general path: refine (gathered candidates or the full row), then
     // order the winners by index.
     const uint32_t nsel = fits ? finish_row(src, refine_from_level0(l0f, width), width, sm, sel, status)

@@ -254,16 +254,25 @@ def draw_index_queries(wl: Workload, seed: int, count: int):
 # ---------------------------------------------------------------------------
 
 def random_scores(seed: int, kv_lens, *, ties: bool = False, nonfinite: bool = False,
-                  signed_zeros: bool = False) -> List[np.ndarray]:
+                  signed_zeros: bool = False, crowd=None) -> List[np.ndarray]:
     """fp32 score rows for the top-k stage alone.
 
     ties: draw from a small set of values so that exact ties are frequent.
     nonfinite: sprinkle NaN / +-Inf entries. signed_zeros: mix -0.0 and +0.0.
+    crowd: per row, a number m of scores, at random positions, that share the
+    top 11 bits of their order key (values 1 + k/4096, k < 1024, so with ties),
+    above the rest of the row (uniform in [0, 0.5)): the best ones are all in
+    one crowded bin of a top-11-bit histogram.
     """
     rng = np.random.default_rng(seed)
     out = []
-    for L in kv_lens:
-        if ties:
+    for e, L in enumerate(kv_lens):
+        if crowd is not None:
+            s = rng.uniform(0.0, 0.5, size=L).astype(np.float32)
+            m = min(int(crowd[e]), L)
+            at = rng.choice(L, size=m, replace=False)
+            s[at] = (1.0 + rng.integers(0, 1024, size=m) / 4096.0).astype(np.float32)
+        elif ties:
             s = rng.integers(-20, 20, size=L).astype(np.float32) * np.float32(0.25)
         else:
             s = rng.standard_normal(size=L, dtype=np.float32)
