@@ -35,9 +35,11 @@ def device_decode(dev, rows, keys, kv):
     n_idx = max(r.index_offset + r.width for r in rows)
     idx = torch.full((n_idx,), -7, dtype=torch.int32, device="cuda")
     inv = torch.full((nq, 64), 7, dtype=torch.int32, device="cuda")
+    ws = ds.workspace(rows)
     ds.ds_rows_decode(rows, dev.q_index, dev.w_index, keys, dev.q_attn, kv, dev.sinks, dev.sinks_row_stride,
-                      dev.scale, out, indices=idx, invalid=inv)
+                      dev.scale, out, indices=idx, invalid=inv, workspace_t=ws)
     torch.cuda.synchronize()
+    assert ds.workspace_status(ws) == 0
     return out.cpu(), idx.cpu(), inv.cpu()
 
 
@@ -49,9 +51,11 @@ def host_decode(dev, rows, keys, kv, stream=None, pinned=True):
     n_idx = max(r.index_offset + r.width for r in rows)
     idx = pin(torch.full((n_idx,), -7, dtype=torch.int32))
     inv = pin(torch.full((nq, 64), 7, dtype=torch.int32))
+    ws = ds.host_workspace(rows, dev.sinks_row_stride)
     ds.ds_rows_decode_host(rows, h_qI, h_wI, keys, h_qA, kv, h_sk, dev.sinks_row_stride, dev.scale, out,
-                           indices=idx, invalid=inv, stream=stream)
+                           indices=idx, invalid=inv, workspace_t=ws, stream=stream)
     (stream or torch.cuda.current_stream()).synchronize()
+    assert ds.workspace_status(ws) == 0
     return out, idx, inv
 
 
@@ -106,6 +110,7 @@ def test_host_decode_repeated_calls_on_one_workspace():
         ds.ds_rows_decode_host(dev.rows, h[0], h[1], dev.keys, h[2], dev.kv, h[3], dev.sinks_row_stride,
                                dev.scale, out, workspace_t=ws, stream=s)
     s.synchronize()
+    assert ds.workspace_status(ws) == 0
     for k, (h, out) in enumerate(pinned):
         ref = torch.empty((8, 64, 512), dtype=torch.bfloat16, device="cuda")
         ds.ds_rows_decode(dev.rows, h[0].cuda(), h[1].cuda(), dev.keys, h[2].cuda(), dev.kv, h[3].cuda(),
@@ -141,6 +146,7 @@ def test_host_decode_in_a_cuda_graph():
     with torch.cuda.stream(s):
         g.replay()
     s.synchronize()
+    assert ds.workspace_status(ws) == 0
     ref = torch.empty((8, 64, 512), dtype=torch.bfloat16, device="cuda")
     ds.ds_rows_decode(dev.rows, h_qI.cuda(), h_wI.cuda(), dev.keys, h_qA.cuda(), dev.kv, dev.sinks,
                       dev.sinks_row_stride, dev.scale, ref)

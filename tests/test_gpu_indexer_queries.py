@@ -56,8 +56,11 @@ def run(i, Q, rows, seed, entries=None):
     _, _, q, w = queries(i, len(wl.rows) * Q, seed)
     entries = list(range(len(rows))) if entries is None else entries
     out = torch.full((512 * Q * len(wl.rows),), -7, dtype=torch.int32, device="cuda")
-    ds.ds_rows_indexer_topk_queries([rows[e] for e in entries], Q, q, w, [dev.keys[e] for e in entries], out)
+    sub = [rows[e] for e in entries]
+    ws = ds.indexer_topk_workspace(sub, "cuda", Q)
+    ds.ds_rows_indexer_topk_queries(sub, Q, q, w, [dev.keys[e] for e in entries], out, workspace_t=ws)
     torch.cuda.synchronize()
+    assert ds.workspace_status(ws) == 0
     return out.cpu().numpy().reshape(len(wl.rows), Q, 512)
 
 
@@ -122,8 +125,10 @@ def test_each_query_equals_the_one_query_call(Q):
         one = [ds.IndexerRow(r.kv_len, r.start_pos + j, r.offset, r.q_row + j, 512 * e)
                for e, r in enumerate(rows)]
         out = torch.full((512 * len(wl.rows),), -7, dtype=torch.int32, device="cuda")
-        ds.ds_rows_indexer_topk(one, q, w, dev.keys, out)
+        ws = ds.indexer_topk_workspace(one, "cuda")
+        ds.ds_rows_indexer_topk(one, q, w, dev.keys, out, workspace_t=ws)
         torch.cuda.synchronize()
+        assert ds.workspace_status(ws) == 0
         single = out.cpu().numpy().reshape(len(wl.rows), 512)
         np.testing.assert_array_equal(got[:, j], single, err_msg=f"query {j}")
 
