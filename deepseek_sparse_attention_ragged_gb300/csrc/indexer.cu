@@ -135,6 +135,10 @@ __device__ __forceinline__ void named_bar(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+__device__ __forceinline__ void named_bar_arrive(int id, int count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 }  // namespace
 
 template <int G>
@@ -182,40 +186,49 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
     if (!p.inputs_ready) pdl_wait();
 
     // ---- setup -------------------------------------------------------------
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S::kStages; ++s) {
-            mbar_init(&bar->k_full[s], 1);
-            mbar_init(&bar->k_empty[s], 1);
+    // The producer warp only initialises the barriers: it announces them on the
+    // setup barrier without waiting and starts the key stream at once, while
+    // the other warps allocate TMEM, load the head weights and zero the
+    // histogram, then wait on the setup barrier.
+    constexpr int kSetupBar = 2;
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int s = 0; s < S::kStages; ++s) {
+                mbar_init(&bar->k_full[s], 1);
+                mbar_init(&bar->k_empty[s], 1);
+            }
+            for (int b = 0; b < S::kQBufs; ++b) {
+                mbar_init(&bar->q_full[b], 1);
+                mbar_init(&bar->q_empty[b], 1);
+            }
+            for (int a = 0; a < 2; ++a) {
+                mbar_init(&bar->acc_full[a], 1);
+                mbar_init(&bar->acc_empty[a], S::kEpiWarps);
+            }
+            bar->abort_flag = 0;
+            fence_barrier_init();
+            for (int e = 0; e < (int)p.rows; ++e) tma_prefetch_map(&p.kmap[e]);
+            tma_prefetch_map(&p.qmap);
         }
-        for (int b = 0; b < S::kQBufs; ++b) {
-            mbar_init(&bar->q_full[b], 1);
-            mbar_init(&bar->q_empty[b], 1);
+        __syncwarp();
+        named_bar_arrive(kSetupBar, S::kThreads);
+    } else {
+        if (warp == 1) {
+            tmem_alloc(&bar->tmem_base, S::kTmemCols);
+            tmem_relinquish();
         }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(&bar->acc_full[a], 1);
-            mbar_init(&bar->acc_empty[a], S::kEpiWarps);
-        }
-        bar->abort_flag = 0;
-        fence_barrier_init();
+        const int tid = threadIdx.x - 32;
+        if (G == 1 && p.inputs_ready != 2)
+            for (int i = tid; i < (int)p.vrows * kIdxHeads; i += S::kThreads - 32) {
+                const int v = i / kIdxHeads, h = i % kIdxHeads;
+                w_s[i] = p.w[(size_t)p.q_row[v] * kIdxHeads + h];
+            }
+        for (int i = tid; i < S::kHistWords; i += S::kThreads - 32) hist_s[i] = 0;
+        tc_fence_before();
+        named_bar(kSetupBar, S::kThreads);
+        tc_fence_after();
     }
-    if (warp == 0 && lane == 0) {
-        for (int e = 0; e < (int)p.rows; ++e) tma_prefetch_map(&p.kmap[e]);
-        tma_prefetch_map(&p.qmap);
-    }
-    if (warp == 1) {
-        tmem_alloc(&bar->tmem_base, S::kTmemCols);
-        tmem_relinquish();
-    }
-    if (G == 1 && p.inputs_ready != 2)
-        for (int i = threadIdx.x; i < (int)p.vrows * kIdxHeads; i += S::kThreads) {
-            const int v = i / kIdxHeads, h = i % kIdxHeads;
-            w_s[i] = p.w[(size_t)p.q_row[v] * kIdxHeads + h];
-        }
-    for (int i = threadIdx.x; i < S::kHistWords; i += S::kThreads) hist_s[i] = 0;
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = bar->tmem_base;
+    const uint32_t tmem_base = warp == 0 ? 0u : bar->tmem_base;
     pdl_trigger();
 
     if (warp == 0) {
