@@ -109,9 +109,10 @@ TOPK_CASES = {
     "nonfinite": dict(lens=[20, 600, 9000, 33000], kw=dict(nonfinite=True)),
     "zeros": dict(lens=[513, 5000, 16385], kw=dict(signed_zeros=True, ties=True)),
     "long": dict(lens=[262144, 131072, 3], kw={}),
-    # The threshold bin holds m candidates: 4, 8 and 12 per thread in
-    # registers, then the refinement from the gathered candidates (m > 6144)
-    # and from the full row (one CTA's slice has more than 2048).
+    # The threshold bin holds m candidates: held in registers, 4 per thread
+    # (m <= 2048) or 12 (m <= 6144), then refined from the gathered
+    # candidates and sorted by index (m > 6144), and refined from the full row
+    # (one CTA's slice has more than 2048).
     "crowded": dict(lens=[20000, 40000, 60000, 100000, 120000],
                     kw=dict(crowd=(1500, 3000, 5000, 10000, 60000))),
 }
