@@ -22,7 +22,9 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // Combine feature columns [f0, f0 + F) of H heads over the n chunk partials of
 // one row (or head half) with NT threads: thread -> one head and F H / NT
 // consecutive features. A partial is m[H], l[H], acc[H][512] (fp32), `stride`
-// floats apart from part0; flags[h] marks a head with a non-finite logit,
+// floats apart from part0, except that chunk own_c's accumulators of these
+// columns are read from `own` ([H][F] in shared memory; own_c < 0: none);
+// flags[h] marks a head with a non-finite logit,
 // *row_flag the whole row; the heads' outputs start at out (rows of 512 bf16),
 // and invalid (optional) receives each head's flag. Per head, in chunk order
 // (the order depends on the number of chunks alone):
@@ -32,7 +34,8 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // denominator is not finite (or den <= 0); any non-finite element as zero.
 // Every thread of a head computes the head's factors itself: no block barrier.
 template <int H, int NT, int F>
-__device__ __forceinline__ void combine_slice(const float* part0, size_t stride, int n, int f0, const float* sinks,
+__device__ __forceinline__ void combine_slice(const float* part0, size_t stride, int n, int f0, const float* own,
+                                              int own_c, const float* sinks,
                                               const uint32_t* row_flag, const uint32_t* flags, __nv_bfloat16* out,
                                               uint32_t* invalid) {
     constexpr int FPT = F * H / NT;  // features per thread
@@ -49,9 +52,15 @@ __device__ __forceinline__ void combine_slice(const float* part0, size_t stride,
     for (int c = 0; c < kAttnChunksMax; ++c)
         if (c < n) {
             const float* pc = part0 + (size_t)c * stride;
-            const float* src = pc + 2 * H + (size_t)h * kDim + f;
+            if (c == own_c) {
+                const float* src = own + h * F + (f - f0);
 #pragma unroll
-            for (int u = 0; u < FPT / 4; ++u) v[c][u] = __ldcg(reinterpret_cast<const float4*>(src + 4 * u));
+                for (int u = 0; u < FPT / 4; ++u) v[c][u] = *reinterpret_cast<const float4*>(src + 4 * u);
+            } else {
+                const float* src = pc + 2 * H + (size_t)h * kDim + f;
+#pragma unroll
+                for (int u = 0; u < FPT / 4; ++u) v[c][u] = __ldcg(reinterpret_cast<const float4*>(src + 4 * u));
+            }
             mc[c] = __ldcg(pc + h);
             lc[c] = __ldcg(pc + H + h);
         }

@@ -136,6 +136,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     uint64_t* mma_bar = reinterpret_cast<uint64_t*>(smem + T::misc + 8);
     float* sinks_s = reinterpret_cast<float*>(smem + T::sinks);
     uint64_t* regions = reinterpret_cast<uint64_t*>(smem + T::regions);
+    float* own_s = reinterpret_cast<float*>(smem + T::g);  // after P·G: this CTA's combined feature block
     GatherSmem& gs = *reinterpret_cast<GatherSmem*>(smem + T::gather);
 
     cg::cluster_group cluster = cg::this_cluster();
@@ -408,10 +409,18 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_ld_x32(tcol, ahi);
             tmem_ld_x32(tcol + kHalfHeads, alo);
             tmem_ld_wait();
-            float* pacc = part + 2 * kHalfHeads + 128 * b + 32 * qt + lane;
+            if (b == (int)c) {
+                // Feature block c is combined by this CTA: it stays in shared
+                // memory (the KV buffer is free once P·G is done), [32 heads][128].
+                float* o = own_s + 32 * qt + lane;
 #pragma unroll
-            for (int h = 0; h < kHalfHeads; ++h)
-                pacc[(size_t)h * kDim] = __uint_as_float(ahi[h]) + __uint_as_float(alo[h]);
+                for (int h = 0; h < kHalfHeads; ++h) o[h * 128] = __uint_as_float(ahi[h]) + __uint_as_float(alo[h]);
+            } else {
+                float* pacc = part + 2 * kHalfHeads + 128 * b + 32 * qt + lane;
+#pragma unroll
+                for (int h = 0; h < kHalfHeads; ++h)
+                    pacc[(size_t)h * kDim] = __uint_as_float(ahi[h]) + __uint_as_float(alo[h]);
+            }
         }
     }
     // A CTA whose tensor-core wait gave up has no valid partial: the whole row
@@ -427,7 +436,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
 
     // ---- combine: feature columns [128 c, 128 c + 128) of the 32 heads ----------
     combine_slice<kHalfHeads, kThreads, 128>(
-        p.part + part0_off, kPartFloats, (int)nchunks, (int)(128 * c), sinks_s,
+        p.part + part0_off, kPartFloats, (int)nchunks, (int)(128 * c), own_s, has_chunk ? (int)c : -1, sinks_s,
         p.flags + kRowsMax * kHeads + e, p.flags + e * kHeads + head0,
         p.out + ((size_t)q_row * kHeads + head0) * kDim,
         p.invalid && c == 0 ? p.invalid + (size_t)q_row * kHeads + head0 : nullptr);
