@@ -377,8 +377,9 @@ __device__ __forceinline__ uint32_t select_finish(const Collected& c, const floa
 
 constexpr uint32_t kCandCap = 2048;  // candidates one CTA may contribute to its cluster
 constexpr int kRegCandSmall = 4;     // candidates per thread in registers while they fit
-constexpr int kRegCandMid = 6;       // then this many
-constexpr int kRegCand = 12;         // at most this many per thread, else the general path
+constexpr int kRegCandMid = 6;       // then this many,
+constexpr int kRegCandLarge = 8;     // this many,
+constexpr int kRegCand = 12;         // and at most this many per thread, else the general path
 
 // State of the all-gather selection in each CTA of a row's cluster.
 struct GatherSmem {
@@ -773,6 +774,9 @@ __device__ __forceinline__ uint32_t select_slots(const Gathered& g, const float*
     if (fits && n <= (uint32_t)kThreads * kRegCandMid)
         return select_in_registers<kRegCandMid>(src, n, refine_from_level0(l0f, width), width, sm, sel, idx, first,
                                                 status);
+    if (fits && n <= (uint32_t)kThreads * kRegCandLarge)
+        return select_in_registers<kRegCandLarge>(src, n, refine_from_level0(l0f, width), width, sm, sel, idx, first,
+                                                  status);
     if (fits && n <= (uint32_t)kThreads * kRegCand)
         return select_in_registers<kRegCand>(src, n, refine_from_level0(l0f, width), width, sm, sel, idx, first,
                                              status);
