@@ -18,9 +18,12 @@
 // GB300 design: one 8-CTA cluster per row; CTA r owns output features
 // [r D/8, (r+1) D/8) in float4 columns, 16 threads per column splitting the
 // window's rows (a fixed-order shuffle tree combines them), so a CTA keeps
-// its whole share of the window in flight. Each thread owns its features in
-// every state row, so the token write, the pooling and the shift need no
-// barrier beyond the block's; the RMS sum and the fail-closed flags cross the
+// its whole share of the window in flight: every window row it pools is loaded
+// before any is used, and the token's own row comes from the thread that
+// computes it (a shuffle within the column's lanes), so the loads do not wait
+// for the token's write. Each thread owns its features in every state row, so
+// the token write, the pooling and the shift need no barrier beyond the
+// block's; the RMS sum and the fail-closed flags cross the
 // cluster as st.async pushes into every CTA (counted on mbarriers) and are
 // added in rank order.
 
@@ -37,7 +40,10 @@ namespace {
 
 constexpr int kCompCluster = 8;
 constexpr int kCompThreads = 256;
-constexpr int kSplit = 16;  // threads per float4 column
+constexpr int kSplit = 16;        // threads per float4 column
+// Window rows per thread: 128 / 16 with ratio 128, one (2 * 4 rows over 16 threads) with ratio 4.
+constexpr int kRowsRatio128 = 8;
+constexpr int kRowsRatio4 = 1;
 
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
@@ -59,6 +65,7 @@ struct __align__(8) CompSmem {
 
 }  // namespace
 
+template <int kRowsPerThread>
 __global__ void __cluster_dims__(kCompCluster, 1, 1) __launch_bounds__(kCompThreads)
     compressor_kernel(const CompressorParams p) {
     __shared__ CompSmem sm;
@@ -94,13 +101,31 @@ __global__ void __cluster_dims__(kCompCluster, 1, 1) __launch_bounds__(kCompThre
     // before it reads anything (griddepcontrol.wait).
     pdl_trigger();
 
+    const bool complete = (pos + 1) % (uint32_t)R == 0;  // the same for the whole cluster
+    const int items = coff * R;
+    // ---- 2a. pooling: this thread takes window rows sub, sub + 16, ...; all of
+    // them but the token's own row are loaded before anything is used, so their
+    // round trips overlap each other and the token's.
+    float4 sw[kRowsPerThread], vw[kRowsPerThread];
+    if (complete && active) {
+#pragma unroll
+        for (int q = 0; q < kRowsPerThread; ++q) {
+            const int i = sub + q * kSplit;
+            if (i < items && i != slot) {
+                const int sf = (overlap && i >= R) ? D + f0 : f0;
+                sw[q] = ld4(scs + (size_t)i * P + sf);
+                vw[q] = ld4(kvs + (size_t)i * P + sf);
+            }
+        }
+    }
+
     // ---- 1. the token's state row, for this column's features ----------------
+    float4 vk = make_float4(0.f, 0.f, 0.f, 0.f), sk = vk;
     if (active && sub < coff) {
         const int sf = sub * D + f0;
         const float4 v = ld4(p.kv + (size_t)row * P + sf);
         const float4 s0 = ld4(p.score + (size_t)row * P + sf);
         const float4 a = ld4(p.ape + (size_t)token * P + sf);
-        float4 vk, sk;
         float* vo = &vk.x;
         float* so = &sk.x;
 #pragma unroll
@@ -114,31 +139,48 @@ __global__ void __cluster_dims__(kCompCluster, 1, 1) __launch_bounds__(kCompThre
         st4(kvs + (size_t)slot * P + sf, vk);
         st4(scs + (size_t)slot * P + sf, sk);
     }
-    __syncthreads();  // the row is visible to the column's other threads
 
-    const bool complete = (pos + 1) % (uint32_t)R == 0;  // the same for the whole cluster
     if (!complete) {
         if (active && sub == 0)
             *reinterpret_cast<uint2*>(p.out + (size_t)row * D + f0) = make_uint2(0u, 0u);
         return;
     }
 
-    // ---- 2. pooling: this thread takes window rows sub, sub + 16, ... ---------
-    const int items = coff * R;
+    // ---- 2b. the token's row enters the window from the thread that wrote it:
+    // the column's 16 threads are consecutive lanes of one warp, and the row's
+    // features of this column belong to thread sub = 1 when the windows
+    // overlap (the token's row reads features D + f0) and sub = 0 otherwise.
+    {
+        const int lane = t & 31;
+        const int src = (lane & ~(kSplit - 1)) | (overlap ? 1 : 0);
+        float4 vt, st;
+        vt.x = __shfl_sync(0xFFFFFFFFu, vk.x, src);
+        vt.y = __shfl_sync(0xFFFFFFFFu, vk.y, src);
+        vt.z = __shfl_sync(0xFFFFFFFFu, vk.z, src);
+        vt.w = __shfl_sync(0xFFFFFFFFu, vk.w, src);
+        st.x = __shfl_sync(0xFFFFFFFFu, sk.x, src);
+        st.y = __shfl_sync(0xFFFFFFFFu, sk.y, src);
+        st.z = __shfl_sync(0xFFFFFFFFu, sk.z, src);
+        st.w = __shfl_sync(0xFFFFFFFFu, sk.w, src);
+#pragma unroll
+        for (int q = 0; q < kRowsPerThread; ++q)
+            if (sub + q * kSplit == slot) {
+                sw[q] = st;
+                vw[q] = vt;
+            }
+    }
     float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     uint32_t bad = 0;
     if (active) {
-        for (int i = sub; i < items; i += kSplit) {
-            const int sf = (overlap && i >= R) ? D + f0 : f0;
-            const float4 s4 = ld4(scs + (size_t)i * P + sf);
-            const float4 v4 = ld4(kvs + (size_t)i * P + sf);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float s = comp(s4, k);
-                bad |= (s != s || s == INFINITY || !finite_f(comp(v4, k))) ? 1u : 0u;
-                m[k] = fmaxf(m[k], s);
-            }
-        }
+        for (int q = 0; q < kRowsPerThread; ++q)
+            if (sub + q * kSplit < items)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float s = comp(sw[q], k);
+                    bad |= (s != s || s == INFINITY || !finite_f(comp(vw[q], k))) ? 1u : 0u;
+                    m[k] = fmaxf(m[k], s);
+                }
     }
 #pragma unroll
     for (int o = kSplit / 2; o > 0; o >>= 1) {
@@ -148,17 +190,15 @@ __global__ void __cluster_dims__(kCompCluster, 1, 1) __launch_bounds__(kCompThre
     }
     float den[4] = {0, 0, 0, 0}, num[4] = {0, 0, 0, 0};
     if (active) {
-        for (int i = sub; i < items; i += kSplit) {
-            const int sf = (overlap && i >= R) ? D + f0 : f0;
-            const float4 s4 = ld4(scs + (size_t)i * P + sf);
-            const float4 v4 = ld4(kvs + (size_t)i * P + sf);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float w = expf(comp(s4, k) - m[k]);
-                den[k] += w;
-                num[k] = fmaf(w, comp(v4, k), num[k]);
-            }
-        }
+        for (int q = 0; q < kRowsPerThread; ++q)
+            if (sub + q * kSplit < items)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float w = expf(comp(sw[q], k) - m[k]);
+                    den[k] += w;
+                    num[k] = fmaf(w, comp(vw[q], k), num[k]);
+                }
     }
 #pragma unroll
     for (int o = kSplit / 2; o > 0; o >>= 1)
@@ -248,7 +288,13 @@ __global__ void __cluster_dims__(kCompCluster, 1, 1) __launch_bounds__(kCompThre
 
 cudaError_t launch_compressor(const CompressorParams& p, cudaStream_t stream, bool pdl) {
     if (p.rows == 0) return cudaSuccess;
-    return launch_kernel(compressor_kernel, dim3(p.rows * kCompCluster), dim3(kCompThreads), 0, stream, pdl, p);
+    if (p.ratio == 4)
+        return launch_kernel(compressor_kernel<kRowsRatio4>, dim3(p.rows * kCompCluster), dim3(kCompThreads), 0,
+                             stream, pdl, p);
+    if (p.ratio == 128)
+        return launch_kernel(compressor_kernel<kRowsRatio128>, dim3(p.rows * kCompCluster), dim3(kCompThreads), 0,
+                             stream, pdl, p);
+    return cudaErrorInvalidValue;  // the boundary admits ratios 4 and 128 only
 }
 
 }  // namespace dsrows
