@@ -41,6 +41,8 @@ namespace {
 constexpr int kCompCluster = 8;
 constexpr int kCompThreads = 256;
 constexpr int kSplit = 16;        // threads per float4 column
+// No output can overflow while every norm is at most this: |output| <= sqrt(512) |norm|.
+constexpr float kNormSafe = 1e37f;
 // Window rows per thread: 128 / 16 with ratio 128, one (2 * 4 rows over 16 threads) with ratio 4.
 constexpr int kRowsRatio128 = 8;
 constexpr int kRowsRatio4 = 1;
@@ -216,6 +218,7 @@ __global__ void __cluster_dims__(kCompCluster, 1, 1) __launch_bounds__(kCompThre
         const bool ok = finite_f(pooled);
         c[k] = bf16_round(ok ? pooled : 0.0f);
         bad |= (!ok || !finite_f(comp(nrm, k))) ? 1u : 0u;
+        bad |= fabsf(comp(nrm, k)) > kNormSafe ? 2u : 0u;
         sq = fmaf(c[k], c[k], sq);
     }
 
@@ -247,7 +250,7 @@ __global__ void __cluster_dims__(kCompCluster, 1, 1) __launch_bounds__(kCompThre
         total += __uint_as_float(sm.sq_all[r]);
         any_bad |= sm.bad_all[r];
     }
-    bool invalid = any_bad != 0 || !finite_f(total);
+    bool invalid = (any_bad & 1u) != 0 || !finite_f(total);
     const float scale = invalid ? 0.0f : 1.0f / sqrtf(total / (float)D + p.eps);
     if (!finite_f(scale)) invalid = true;
     float y[4];
@@ -257,16 +260,23 @@ __global__ void __cluster_dims__(kCompCluster, 1, 1) __launch_bounds__(kCompThre
         y[k] = c[k] * scale * comp(nrm, k);
         ybad |= finite_f(y[k]) ? 0u : 1u;
     }
-    if (t == 0) sm.cta_ybad = 0;
-    __syncthreads();
-    if (active && sub == 0 && ybad) atomicOr(&sm.cta_ybad, 1u);
-    __syncthreads();
-    if (t == 0) {
-        mbar_arrive_expect_tx(&sm.bar_yb, 4 * kCompCluster);
-        for (int r = 0; r < kCompCluster; ++r) st_async_remote(&sm.yb_all[rank], sm.cta_ybad, &sm.bar_yb, (uint32_t)r);
+    // |c scale| <= sqrt(D) (every c^2 is at most the total), so a non-finite
+    // output needs a norm above kNormSafe somewhere in the row. Only then does
+    // the cluster exchange the output flags; every CTA sees the same bits and
+    // takes the same branch.
+    if (any_bad & 2u) {
+        if (t == 0) sm.cta_ybad = 0;
+        __syncthreads();
+        if (active && sub == 0 && ybad) atomicOr(&sm.cta_ybad, 1u);
+        __syncthreads();
+        if (t == 0) {
+            mbar_arrive_expect_tx(&sm.bar_yb, 4 * kCompCluster);
+            for (int r = 0; r < kCompCluster; ++r)
+                st_async_remote(&sm.yb_all[rank], sm.cta_ybad, &sm.bar_yb, (uint32_t)r);
+        }
+        mbar_wait_cluster(&sm.bar_yb, 0, nullptr);
+        for (int r = 0; r < kCompCluster; ++r) invalid = invalid || sm.yb_all[r];
     }
-    mbar_wait_cluster(&sm.bar_yb, 0, nullptr);
-    for (int r = 0; r < kCompCluster; ++r) invalid = invalid || sm.yb_all[r];
 
     if (active && sub == 0) {
         __align__(8) __nv_bfloat16 o[4];
@@ -283,7 +293,8 @@ __global__ void __cluster_dims__(kCompCluster, 1, 1) __launch_bounds__(kCompThre
         st4(scs + dst, ld4(scs + src));
     }
     // No CTA reads another's shared memory, and every store into this CTA's
-    // has landed (both barriers completed): the CTAs leave independently.
+    // has landed (every barrier it waited on completed; all CTAs skip or run
+    // the output-flag exchange together): the CTAs leave independently.
 }
 
 cudaError_t launch_compressor(const CompressorParams& p, cudaStream_t stream, bool pdl) {

@@ -96,8 +96,13 @@ def test_consecutive_tokens_through_blocks(ratio, head_dim):
         state_k, state_s = ks, ss
 
 
-@pytest.mark.parametrize("what", ["kv_nan_read_half", "norm_inf", "state_score_inf", "kv_nan_unread_half"])
+@pytest.mark.parametrize("what", ["kv_nan_read_half", "norm_inf", "state_score_inf", "kv_nan_unread_half",
+                                  "norm_all_max", "norm_big_finite"])
 def test_fail_closed(what):
+    """A bad input zeroes its row (or every row, for the shared norm). With a
+    norm of fp32's largest value every output overflows, so the rows are
+    zeroed; a norm of 5e37 makes the kernel compare the outputs' flags across
+    the cluster, though none overflows."""
     rng = np.random.default_rng(11)
     ratio, head_dim = 4, 512
     a = _inputs(rng, 2, ratio, head_dim)
@@ -107,6 +112,10 @@ def test_fail_closed(what):
         a["norm"][9] = np.inf
     elif what == "state_score_inf":
         a["score_state"][0][2, 9] = np.inf
+    elif what == "norm_all_max":
+        a["norm"][:] = np.finfo(np.float32).max
+    elif what == "norm_big_finite":
+        a["norm"][9] = np.float32(5e37)
     else:
         a["kv"][0, 9] = np.nan          # first half: only read by the next block
     pos = [7, 7]
@@ -115,8 +124,10 @@ def test_fail_closed(what):
         _check(out[e], ks[e], ss[e], _ref(a, e, pos[e], ratio, head_dim), f"{what} row {e}")
     if what in ("kv_nan_read_half", "state_score_inf"):
         assert not out[0].any() and out[1].any()
-    elif what == "norm_inf":
+    elif what in ("norm_inf", "norm_all_max"):
         assert not out.any()
+    elif what == "norm_big_finite":
+        assert out[0].any() and out[1].any()
     else:
         assert out[0].any()
 
