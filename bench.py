@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--no-per-config", action="store_true", help="skip the other workloads' step latencies")
     ap.add_argument("--case", default="decode",
                     choices=["decode", "decode_steps", "topk", "indexer_topk", "indexer_queries", "decode_host",
-                             "sparse_attn"],
+                             "sparse_attn", "compressor"],
                     help="decode: the benchmark; any other: run only that entry point on the workload "
                          "(--warmup + --steps calls, no timing), for a profiler to capture its kernels")
     return ap.parse_args()
@@ -523,6 +523,21 @@ def run_case(args, ds, workloads, wl, dev, qsets, stream, device):
         qws = ds.indexer_topk_workspace(rows, device, Q)
         for _ in range(calls):
             ds.ds_rows_indexer_topk_queries(rows, Q, q, w, dev.keys, qout, workspace_t=qws, stream=stream)
+    elif args.case == "compressor":
+        # (ratio, head_dim) = (128, 512) for `calls` calls, then (4, 128): 8 rows that all
+        # complete a block, so every call pools its window.
+        g = torch.Generator(device="cpu").manual_seed(5)
+        f = lambda *sh: torch.randn(*sh, generator=g).to(device)
+        for ratio, head_dim in ((128, 512), (4, 128)):
+            coff = 2 if ratio == 4 else 1
+            P = coff * head_dim
+            ks = [f(coff * ratio, P) for _ in range(8)]
+            ss = [f(coff * ratio, P) for _ in range(8)]
+            kv, sc, ape, norm = f(8, P), f(8, P), f(ratio, P), f(head_dim)
+            out = torch.empty((8, head_dim), dtype=torch.bfloat16, device=device)
+            pos = [ratio * (e + 1) - 1 for e in range(8)]
+            for _ in range(calls):
+                ds.ds_rows_compress_kv(ks, ss, pos, kv, sc, ape, norm, ratio, head_dim, 1e-6, out, stream=stream)
     elif args.case == "decode_host":
         h_sets = [tuple(t.cpu().pin_memory() for t in qs) for qs in qsets]
         h_sk = dev.sinks.cpu().pin_memory()
