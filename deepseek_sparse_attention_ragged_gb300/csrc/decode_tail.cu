@@ -139,6 +139,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     float* own_s = reinterpret_cast<float*>(smem + T::g);  // after P·G: this CTA's combined feature block
     GatherSmem& gs = *reinterpret_cast<GatherSmem*>(smem + T::gather);
 
+    // The stream's next kernel may launch while this one runs: it waits for this
+    // grid to complete (griddepcontrol.wait) before it reads or writes anything
+    // this kernel uses.
+    pdl_trigger();
     cg::cluster_group cluster = cg::this_cluster();
     const uint32_t rank = cluster.block_rank();
     const int e = blockIdx.x / kCluster;

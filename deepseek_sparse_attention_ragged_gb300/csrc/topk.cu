@@ -117,13 +117,18 @@ cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t stream, bool pd
                          pdl, p);
 }
 
+// The first kernel of a call. It may be launched while the stream's previous
+// kernel runs (programmatic launch); it waits for that kernel to complete
+// before it writes anything, and only then lets the next kernel launch, so
+// every input of the call is complete when that one starts.
 __global__ void __launch_bounds__(1024) clear_kernel(uint32_t* __restrict__ p, uint32_t words) {
+    pdl_wait();
     pdl_trigger();
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < words; i += gridDim.x * blockDim.x) p[i] = 0;
 }
 
 cudaError_t launch_clear(uint32_t* p, uint32_t words, cudaStream_t stream) {
-    return launch_kernel(clear_kernel, dim3(16), dim3(1024), 0, stream, false, p, words);
+    return launch_kernel(clear_kernel, dim3(16), dim3(1024), 0, stream, true, p, words);
 }
 
 // The library's bounded mbarrier wait on two phases of a shared-memory barrier
@@ -145,13 +150,14 @@ cudaError_t launch_wait_selftest(uint32_t* status, uint32_t* result, uint64_t bu
 }
 
 // clear_kernel plus two 16-byte-granular copies (the indexer's query and head
-// weights, from pinned host memory into device staging). The next kernel may
-// start early; it waits for this one (griddepcontrol.wait) before it reads
-// the copies.
+// weights, from pinned host memory into device staging), with the same launch
+// rules. The next kernel may start early; it waits for this one
+// (griddepcontrol.wait) before it reads the copies.
 __global__ void __launch_bounds__(1024) clear_copy_kernel(uint32_t* __restrict__ p, uint32_t words,
                                                           const uint4* __restrict__ a_src, uint4* __restrict__ a_dst,
                                                           uint32_t a_n, const uint4* __restrict__ b_src,
                                                           uint4* __restrict__ b_dst, uint32_t b_n) {
+    pdl_wait();
     pdl_trigger();
     const uint32_t stride = gridDim.x * blockDim.x;
     const uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x;
@@ -162,7 +168,7 @@ __global__ void __launch_bounds__(1024) clear_copy_kernel(uint32_t* __restrict__
 
 cudaError_t launch_clear_copy(uint32_t* p, uint32_t words, const void* a_src, void* a_dst, size_t a_bytes,
                               const void* b_src, void* b_dst, size_t b_bytes, cudaStream_t stream) {
-    return launch_kernel(clear_copy_kernel, dim3(16), dim3(1024), 0, stream, false, p, words,
+    return launch_kernel(clear_copy_kernel, dim3(16), dim3(1024), 0, stream, true, p, words,
                          static_cast<const uint4*>(a_src), static_cast<uint4*>(a_dst), (uint32_t)(a_bytes / 16),
                          static_cast<const uint4*>(b_src), static_cast<uint4*>(b_dst), (uint32_t)(b_bytes / 16));
 }
