@@ -29,6 +29,13 @@
  *   width alone.
  * - Calls that share a workspace or an output must not overlap in time
  *   (order them on one stream).
+ * - A call's kernels are chained with programmatic dependent launch. Its first
+ *   kernel may become resident while the stream's previous kernel still runs,
+ *   but it waits for that kernel to complete before it reads or writes
+ *   anything. Its last kernel lets the stream's next kernel launch early: a
+ *   kernel the caller launches next with programmatic stream serialization
+ *   must wait (griddepcontrol.wait, cudaGridDependencySynchronize) before it
+ *   touches this call's outputs. Ordinary launches need nothing.
  */
 #ifndef DSROWS_H
 #define DSROWS_H
