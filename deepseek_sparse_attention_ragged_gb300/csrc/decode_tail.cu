@@ -11,14 +11,16 @@
 // One 8-CTA thread-block cluster per row, 512 threads per CTA. CTA r owns the
 // 128-slot chunk c = r / 2 and the head half r % 2 (32 heads).
 //   1. select (decode only): every CTA streams its slice of the row's scores
-//      and stores the candidates at or above the level-0 threshold bin into
-//      the shared memory of every CTA of the cluster (an all-gather); after one
-//      cluster barrier each CTA refines the threshold over the gathered
-//      candidates, sorts the winners best first and takes its chunk's slots:
-//      slot t holds the t-th best index, both in the caller's best-first index
-//      list and in the attention. Every CTA computes the same selection, so no
-//      winner or slot crosses the cluster. With indices given by the caller,
-//      each CTA reads its chunk's slots instead;
+//      and stores the candidates at or above the level-0 threshold bin, in
+//      index order, into the shared memory of every CTA of the cluster (an
+//      all-gather); after one cluster barrier each CTA refines the exact
+//      threshold over the gathered candidates and places the winners in index
+//      order: slot t holds the winner with the t-th smallest index. Every CTA
+//      computes the same selection, so no winner or slot crosses the cluster.
+//      The caller's best-first index list comes from a ninth cluster, which
+//      sorts each row's published winners best first (or, without attention,
+//      from each CTA ranking its 64 slots). With indices given by the caller,
+//      each CTA sorts them ascending (sentinels last) into the same slot order;
 //   2. attend, on tcgen05 tensor cores with fp32 accumulators in TMEM: gather
 //      the chunk's 128 KV rows into the 128-byte-swizzled K-major layout, then
 //        logits  D[128 slots x 32 heads] = KV_chunk . Q_half^T   (K = 512,
@@ -29,13 +31,16 @@
 //      for the four 128-feature blocks, where the same KV buffer is the
 //      MN-major operand and P enters as a bf16 hi + lo pair stacked along N
 //      (acc = D[:, h] + D[:, 32 + h]);
-//   3. combine: after a cluster barrier CTA r combines feature columns
-//      [128 c, 128 c + 128) of its 32 heads over the chunks in chunk order:
+//   3. combine: the chunk partials go to the workspace (the feature block a
+//      CTA combines itself stays in its shared memory); after a cluster
+//      barrier CTA r combines feature columns [128 c, 128 c + 128) of its 32
+//      heads over the chunks in chunk order:
 //        m = max(sink, m_c), den = exp(sink - m) + sum_c l_c exp(m_c - m),
 //        out = sum_c acc_c exp(m_c - m) / den.
-// Every reduction order depends on the row's width alone, and the stand-alone
-// attention runs this kernel on the caller's indices, so the decode's output
-// is bitwise the attention of its own best-first index list.
+// Every reduction order depends on the row's width and its indices alone, and
+// the stand-alone attention runs this kernel on the caller's indices in the
+// same ascending order, so the decode's output is bitwise the attention of
+// its own best-first index list.
 //
 // Fail-closed rules: a caller's index < -1 or >= kv_len flags the whole row; a
 // non-finite logit (non-finite q or KV element, or overflow) flags its head;
