@@ -15,7 +15,9 @@
 // the key's data and the query (bitwise, wherever the tile sits).
 //
 // Warp roles (192 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
-// issues the MMAs, warps 2..5 run the epilogue. Key tiles flow through a
+// issues the MMAs, warps 2..5 run the epilogue. Warp 0 starts loading key
+// tiles as soon as the barriers exist, while the other warps allocate TMEM
+// and stage the head weights. Key tiles flow through a
 // 5-stage ring; the query of the current row is double-buffered; the
 // accumulator is double-buffered in TMEM so the epilogue of tile i overlaps
 // the MMAs of tile i+1. Keys are streamed with an L2 evict-first policy.

@@ -24,6 +24,10 @@
 //      merge rounds by binary search.
 // A row whose threshold bin overflows the leader's candidate space is refined
 // by the leader from the row's full score array (correct, slower).
+// This kernel serves row sets of more than 8 rows (several queries per row).
+// Up to 8 rows, the library selects with the attention kernel in
+// selection-only mode instead: there every CTA of the cluster gathers all
+// candidates and ranks its own slots, which beats one leader's sort.
 
 #include "common.cuh"
 #include "kernels.h"
