@@ -159,6 +159,31 @@ __device__ __forceinline__ void write_winners(SelectSmem& sm, const uint64_t* se
     if ((uint32_t)t < width) out[t] = (uint32_t)t < nsel ? (int32_t)(~(uint32_t)x[0]) + offset : -1;
 }
 
+// Ranks inside a threshold bin of nr <= kRankDirect elements bin[0, nr):
+// element i = threadIdx.x / 4 (held in `ck`) is compared with every element
+// of the bin by four threads, each taking every fourth one (the four
+// addresses of a load fall in different banks), and their counts are summed
+// by shuffles. Returns how many elements of the bin are greater than element
+// i, valid in threads with threadIdx.x % 4 == 0 and i < nr. Called by whole
+// warps: those holding elements, warps w with 8 w < nr; the bin may hold
+// anything past nr.
+__device__ __forceinline__ uint32_t count_better(const uint64_t* bin, uint32_t nr, uint64_t& ck) {
+    static_assert(kThreads >= 4 * kRankDirect, "four threads per element of the bin");
+    const uint32_t t = threadIdx.x, i = t >> 2, q = t & 3;
+    ck = i < nr ? bin[i] : 0ull;
+    uint32_t better = 0;
+    const uint32_t iters = (nr + 3) >> 2;  // 4 iters <= kRankDirect: j stays inside the bin buffer
+#pragma unroll 4
+    for (uint32_t u = 0; u < iters; ++u) {
+        const uint32_t j = 4 * u + q;
+        const uint64_t y = bin[j];
+        better += j < nr && y > ck ? 1u : 0u;
+    }
+    better += __shfl_xor_sync(kFull, better, 1);
+    better += __shfl_xor_sync(kFull, better, 2);
+    return better;
+}
+
 // Refine digit by digit until the threshold bin is taken whole or holds at
 // most kRankDirect elements, then keep the winners' composites in sel[0, 512)
 // (zero past the last): every element above the bin, and the `need` best of
@@ -235,11 +260,10 @@ __device__ inline uint32_t finish_row(const Src& src, Refine st, uint32_t width,
     if (direct) {
         const uint32_t nr = sm.nres < kRankDirect ? sm.nres : kRankDirect;
         if (sm.nres != eq && t == 0) atomicOr(status, kStatusCandOverflow);
-        for (uint32_t k = t; k < nr; k += kThreads) {
-            const uint64_t ck = bin_el[k];
-            uint32_t better = 0;
-            for (uint32_t j = 0; j < nr; ++j) better += bin_el[j] > ck ? 1u : 0u;
-            if (better < need) {
+        if ((uint32_t)(t >> 5) * 8 < nr) {  // warp-uniform: the warps holding elements
+            uint64_t ck;
+            const uint32_t better = count_better(bin_el, nr, ck);
+            if ((t & 3) == 0 && (uint32_t)(t >> 2) < nr && better < need) {
                 const uint32_t pos = atomicAdd(&sm.nsel, 1u);
                 if (pos < (uint32_t)kTopK) sel[pos] = ck;
             }
@@ -387,9 +411,10 @@ struct GatherSmem {
     uint32_t pick[2][32];                 // two alternating pick_bin scratch areas
     uint32_t scan[2][16];                 // two alternating block_excl_scan scratch areas
     uint32_t count[kCluster];             // candidates contributed by each CTA (written by that CTA)
-    uint32_t nres;
+    uint32_t nres;                        // elements of the final threshold bin (zeroed by the collection)
     uint32_t nsel;
     uint64_t thr;
+    uint64_t bin[kRankDirect];            // the final threshold bin's elements
 };
 __device__ __forceinline__ uint32_t* pick_scratch(GatherSmem& sm) { return sm.pick[0]; }
 static_assert(kHistBins * 4 >= 2 * kTopK * 8, "the sorts use h as two 512-entry buffers");
@@ -498,9 +523,10 @@ __device__ __forceinline__ Gathered select_collect_all(const float* s, uint32_t 
     r.b0 = r.take_all ? 0u : (uint32_t)r.l0.bin;
     r.fast = n_cand <= (uint32_t)kCluster * kCandCap;
     // The refinement's first level counts into h: zero it (every thread has
-    // read its bins of the histogram above).
+    // read its bins of the histogram above), and the final bin's count.
 #pragma unroll
     for (int i = 0; i < kHistBins / kThreads; ++i) sm.h[t + i * kThreads] = 0;
+    if (t == 0) sm.nres = 0;
 
     uint64_t* own = regions + (size_t)rank * kCandCap;
     uint32_t n_local = 0;
@@ -571,8 +597,8 @@ __device__ __forceinline__ Gathered select_collect_all(const float* s, uint32_t 
 // registers, R per thread (each candidate in one x[k] of one thread, the
 // unused entries zero),
 // from the refinement state `st`: the winners are the candidates with a
-// composite >= the returned value (1 when every candidate is taken). h is zero
-// on entry.
+// composite >= the returned value (1 when every candidate is taken). h and
+// nres are zero on entry.
 template <int R>
 __device__ __forceinline__ uint64_t refine_threshold(const uint64_t (&x)[R], Refine st, GatherSmem& sm,
                                                      uint32_t* status) {
@@ -611,13 +637,10 @@ __device__ __forceinline__ uint64_t refine_threshold(const uint64_t (&x)[R], Ref
     const int shift = level_shift(level);
     const uint64_t whole = prefix << shift;  // the bin taken whole: every composite >= this
     if (done) return whole;
-    // The threshold bin's eq (<= kRankDirect) elements: the need-th best of them.
-    uint64_t* bin_el = reinterpret_cast<uint64_t*>(sm.h);
-    if (t == 0) {
-        sm.nres = 0;
-        sm.thr = whole;
-    }
-    __syncthreads();  // (every thread has read h in the last pick)
+    // The threshold bin's eq (<= kRankDirect) elements go to their own buffer
+    // (no barrier against the last pick's reads of h; nres was zeroed by the
+    // collection), and the need-th best of them is the threshold.
+    if (t == 0) sm.thr = whole;  // kept if the counts disagree
 #pragma unroll
     for (int k = 0; k < R; ++k) {
         const bool in_bin = x[k] != 0 && (x[k] >> shift) == prefix;
@@ -626,17 +649,17 @@ __device__ __forceinline__ uint64_t refine_threshold(const uint64_t (&x)[R], Ref
             uint32_t pos = 0;
             if (lane == 0) pos = atomicAdd(&sm.nres, (uint32_t)__popc(m));
             pos = __shfl_sync(kFull, pos, 0) + __popc(m & ((1u << lane) - 1u));
-            if (in_bin && pos < kRankDirect) bin_el[pos] = x[k];
+            if (in_bin && pos < kRankDirect) sm.bin[pos] = x[k];
         }
     }
     __syncthreads();
-    const uint32_t nr = sm.nres < kRankDirect ? sm.nres : kRankDirect;
-    if (sm.nres != eq && t == 0) atomicOr(status, kStatusCandOverflow);
-    if ((uint32_t)t < nr) {
-        const uint64_t ck = bin_el[t];
-        uint32_t better = 0;
-        for (uint32_t j = 0; j < nr; ++j) better += bin_el[j] > ck ? 1u : 0u;
-        if (better == need - 1) sm.thr = ck;
+    const uint32_t nres = sm.nres;
+    const uint32_t nr = nres < kRankDirect ? nres : kRankDirect;
+    if (nres != eq && t == 0) atomicOr(status, kStatusCandOverflow);
+    if ((uint32_t)(t >> 5) * 8 < nr) {  // warp-uniform: the warps holding elements
+        uint64_t ck;
+        const uint32_t better = count_better(sm.bin, nr, ck);
+        if ((t & 3) == 0 && (uint32_t)(t >> 2) < nr && better == need - 1) sm.thr = ck;
     }
     __syncthreads();
     return sm.thr;
