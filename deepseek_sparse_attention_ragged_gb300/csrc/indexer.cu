@@ -119,12 +119,34 @@ __device__ __forceinline__ float relu_nan(float x) {
 // sum_h w[h] relu(x[h]) over the 64 head dot products x of one key, with w in
 // registers (wr) or shared memory (w_s): four chains (heads h = c mod 4, in
 // head order), added pairwise.
+// Two fp32 FMAs in one instruction (each rounded as fmaf): d = a * b + c lane-wise.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)),
+          "l"(*reinterpret_cast<const uint64_t*>(&c)));
+    return *reinterpret_cast<const float2*>(&d);
+}
+
 __device__ __forceinline__ float head_sum(const uint32_t (&x)[64], const float* wr, const float* w_s) {
+    if (wr) {
+        // Weights in registers: chains 0 and 1 (heads h = 0, 1 mod 4) and chains
+        // 2 and 3 advance in pairs, two FMAs per instruction.
+        float2 s01 = make_float2(0.0f, 0.0f), s23 = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int h = 0; h < kIdxHeads; h += 4) {
+            const float2 r01 = make_float2(relu_nan(__uint_as_float(x[h])), relu_nan(__uint_as_float(x[h + 1])));
+            const float2 r23 = make_float2(relu_nan(__uint_as_float(x[h + 2])), relu_nan(__uint_as_float(x[h + 3])));
+            s01 = fma2(r01, make_float2(wr[h], wr[h + 1]), s01);
+            s23 = fma2(r23, make_float2(wr[h + 2], wr[h + 3]), s23);
+        }
+        return (s01.x + s01.y) + (s23.x + s23.y);
+    }
     float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int h = 0; h < kIdxHeads; h += 4) {
-        const float4 w4 = wr ? make_float4(wr[h], wr[h + 1], wr[h + 2], wr[h + 3])
-                             : *reinterpret_cast<const float4*>(w_s + h);
+        const float4 w4 = *reinterpret_cast<const float4*>(w_s + h);
         s4[0] = fmaf(relu_nan(__uint_as_float(x[h])), w4.x, s4[0]);
         s4[1] = fmaf(relu_nan(__uint_as_float(x[h + 1])), w4.y, s4[1]);
         s4[2] = fmaf(relu_nan(__uint_as_float(x[h + 2])), w4.z, s4[2]);
