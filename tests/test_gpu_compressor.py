@@ -132,6 +132,41 @@ def test_fail_closed(what):
         assert out[0].any()
 
 
+@pytest.mark.parametrize("what", ["kv_nan", "window_score_inf", "window_score_nan", "window_kv_inf", "norm_inf",
+                                  "norm_all_max", "norm_big_finite"])
+def test_fail_closed_ratio128(what):
+    """The same rules on the (128, 512) path, whose pooling reduces over warps
+    through shared memory: a bad token value, window score or window value
+    zeroes its row only, a bad norm zeroes every row."""
+    rng = np.random.default_rng(12)
+    ratio, head_dim = 128, 512
+    a = _inputs(rng, 2, ratio, head_dim)
+    if what == "kv_nan":
+        a["kv"][0, 300] = np.nan                   # the token's own row, feature 300
+    elif what == "window_score_inf":
+        a["score_state"][0][37, 5] = np.inf
+    elif what == "window_score_nan":
+        a["score_state"][0][126, 511] = np.nan
+    elif what == "window_kv_inf":
+        a["kv_state"][0][64, 200] = -np.inf
+    elif what == "norm_inf":
+        a["norm"][100] = np.inf
+    elif what == "norm_all_max":
+        a["norm"][:] = np.finfo(np.float32).max
+    else:
+        a["norm"][100] = np.float32(5e37)
+    pos = [127, 255]                               # both complete a block; tokens 127 and 127
+    out, ks, ss = _run(a, pos, ratio, head_dim)
+    for e in range(2):
+        _check(out[e], ks[e], ss[e], _ref(a, e, pos[e], ratio, head_dim), f"{what} row {e}")
+    if what in ("norm_inf", "norm_all_max"):
+        assert not out.any()
+    elif what == "norm_big_finite":
+        assert out[0].any() and out[1].any()
+    else:
+        assert not out[0].any() and out[1].any()
+
+
 @pytest.mark.parametrize("ratio,head_dim", SHAPES)
 def test_joint_equals_single_row(ratio, head_dim):
     rng = np.random.default_rng(3 * ratio + head_dim)
