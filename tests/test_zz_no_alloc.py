@@ -7,7 +7,8 @@ the library, so these tests call it twice in a row, on different scores, to
 show that each call starts from a clean state. They compare every result with
 ds_rows_topk through the C-ABI, and with the oracle's stable sort on scores
 with exact ties and non-finite values; the indices are integers, so they must
-be equal. The status word it keeps in the library reads 0 after each call.
+be equal. The status word it keeps in the library reads 0 after each call. One
+test captures the call in a CUDA graph and replays it on new scores.
 
 This file sorts last so that a run stopping at the first failure has already
 run every other test.
@@ -71,6 +72,35 @@ def test_static_scratch_topk_matches_the_oracle_twice():
             want = oracle.topk(host[e, : r.kv_len], r.width)
             np.testing.assert_array_equal(g[r.index_offset: r.index_offset + r.width], want,
                                           err_msg=f"call {call}, row kv_len {r.kv_len}")
+
+
+def test_static_scratch_topk_replays_from_a_cuda_graph():
+    """The stated use: a warm-up call (it looks up the array), then the call
+    captured in a CUDA graph and replayed after the scores change in place.
+    Each replay's indices equal the oracle's, and the status reads 0."""
+    lens = [70000, 4096, 513, 300]
+    rows = [workloads.Row(L, min(512, L), 512 * e, e) for e, L in enumerate(lens)]
+    scores, stride = _scores(101, lens, ties=True, nonfinite=True)
+    got = torch.full((512 * len(lens),), -9, dtype=torch.int32, device="cuda")
+    ds.ds_rows_topk_static(rows, scores, stride, got)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        ds.ds_rows_topk_static(rows, scores, stride, got)
+    for seed in (102, 103):
+        new, _ = _scores(seed, lens, ties=seed == 103, nonfinite=seed == 103)
+        scores.copy_(new)
+        got.fill_(-9)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert ds.topk_static_status() == 0
+        host, g = scores.cpu().numpy(), got.cpu().numpy()
+        for e, r in enumerate(rows):
+            want = oracle.topk(host[e, : r.kv_len], r.width)
+            np.testing.assert_array_equal(g[r.index_offset: r.index_offset + r.width], want,
+                                          err_msg=f"replay with seed {seed}, row kv_len {r.kv_len}")
 
 
 def test_static_scratch_topk_rejects_too_many_rows():
