@@ -205,8 +205,8 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
     // Inputs may still be in flight from the previous kernel (programmatic
     // launch): then nothing is read before it completes. With inputs_ready 2
     // only the query and head weights are: the CTA sets up at once, and the
-    // producer (before its first query load, ahead of the first key tile) and
-    // the epilogue (before the weights) wait.
+    // producer (after the first stages of key tiles, before its first query
+    // load) and the epilogue (before the weights) wait.
     if (!p.inputs_ready) pdl_wait();
 
     // ---- setup -------------------------------------------------------------
@@ -268,6 +268,25 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
             bool used[S::kStages];
             for (int s = 0; s < S::kStages; ++s) used[s] = false;
             bool ok = true;
+            // The queries of segment sg into the next query buffer.
+            auto load_query = [&](int sg) -> bool {
+                const uint32_t qb = q_uses % S::kQBufs, use = q_uses / S::kQBufs;
+                if (!mbar_wait(&bar->q_empty[qb], (use & 1) ^ 1, p.status)) return false;
+                const int nq = G == 1 ? 1 : p.seg_queries[sg];
+                mbar_arrive_expect_tx(&bar->q_full[qb], (uint32_t)nq * 2 * kQBoxBytes);
+                uint8_t* dst = q_s + (size_t)qb * S::kQBytes;
+                for (int i = 0; i < nq; ++i) {
+                    const int y = (int)(p.q_row[p.seg_vrow[sg] + i] * kIdxHeads);
+                    tma_load_2d(dst + i * kQBoxBytes, &p.qmap, &bar->q_full[qb], 0, y, q_policy);
+                    tma_load_2d(dst + S::kQHalfBytes + i * kQBoxBytes, &p.qmap, &bar->q_full[qb], 64, y, q_policy);
+                }
+                ++q_uses;
+                return true;
+            };
+            // With inputs_ready 2 the first query is still being written by the
+            // previous kernel: the key tiles of the first stages (complete
+            // inputs) are requested first, then the wait, then that query.
+            bool q_deferred = false;
             for (;; ++it) {
                 const uint32_t g = tile_of(it);
                 if (g >= T || !ok) break;
@@ -276,18 +295,8 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
                 const uint32_t tile = g - p.tile_begin[sg];
                 if (sg != cur) {
                     cur = sg;
-                    if (p.inputs_ready == 2 && q_uses == 0) pdl_wait();
-                    const uint32_t qb = q_uses % S::kQBufs, use = q_uses / S::kQBufs;
-                    if (!mbar_wait(&bar->q_empty[qb], (use & 1) ^ 1, p.status)) { ok = false; break; }
-                    const int nq = G == 1 ? 1 : p.seg_queries[sg];
-                    mbar_arrive_expect_tx(&bar->q_full[qb], (uint32_t)nq * 2 * kQBoxBytes);
-                    uint8_t* dst = q_s + (size_t)qb * S::kQBytes;
-                    for (int i = 0; i < nq; ++i) {
-                        const int y = (int)(p.q_row[p.seg_vrow[sg] + i] * kIdxHeads);
-                        tma_load_2d(dst + i * kQBoxBytes, &p.qmap, &bar->q_full[qb], 0, y, q_policy);
-                        tma_load_2d(dst + S::kQHalfBytes + i * kQBoxBytes, &p.qmap, &bar->q_full[qb], 64, y, q_policy);
-                    }
-                    ++q_uses;
+                    if (p.inputs_ready == 2 && q_uses == 0) q_deferred = true;
+                    else if (!load_query(sg)) { ok = false; break; }
                 }
                 const uint32_t s = it % S::kStages;
                 const uint32_t ph = (it / S::kStages) & 1;
@@ -299,6 +308,15 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
                 tma_load_2d(dst + kHalfBytes, &p.kmap[e], &bar->k_full[s], 64, y, policy);
                 used[s] = true;
                 last_parity[s] = ph;
+                if (q_deferred) {
+                    // Before the ring would wait, or before another segment's query.
+                    const uint32_t gn = tile_of(it + 1);
+                    if (it + 1 == (uint32_t)S::kStages || gn >= T || segment_of_tile(p, gn) != cur) {
+                        pdl_wait();
+                        q_deferred = false;
+                        if (!load_query(cur)) { ok = false; break; }
+                    }
+                }
             }
             if (!ok) atomicExch(&bar->abort_flag, 1u);
             // Drain: every load this thread issued has landed before the CTA exits.
