@@ -165,14 +165,25 @@ __global__ void __launch_bounds__(1024) clear_copy_kernel(uint32_t* __restrict__
     pdl_trigger();
     const uint32_t stride = gridDim.x * blockDim.x;
     const uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x;
-    for (uint32_t i = i0; i < a_n; i += stride) a_dst[i] = a_src[i];
-    for (uint32_t i = i0; i < b_n; i += stride) b_dst[i] = b_src[i];
+    const uint32_t n = a_n > b_n ? a_n : b_n;
+    // Both host loads of an element are in flight before either store: one
+    // round trip over the host link per element, not two.
+    for (uint32_t i = i0; i < n; i += stride) {
+        const bool ha = i < a_n, hb = i < b_n;
+        uint4 av = make_uint4(0, 0, 0, 0), bv = av;
+        if (ha) av = a_src[i];
+        if (hb) bv = b_src[i];
+        if (ha) a_dst[i] = av;
+        if (hb) b_dst[i] = bv;
+    }
     for (uint32_t i = i0; i < words; i += stride) p[i] = 0;
 }
 
+// 64 CTAs of 256 threads: the host loads go out from 64 SMs. The CTAs are
+// small enough to share an SM with the indexer's.
 cudaError_t launch_clear_copy(uint32_t* p, uint32_t words, const void* a_src, void* a_dst, size_t a_bytes,
                               const void* b_src, void* b_dst, size_t b_bytes, cudaStream_t stream) {
-    return launch_kernel(clear_copy_kernel, dim3(16), dim3(1024), 0, stream, true, p, words,
+    return launch_kernel(clear_copy_kernel, dim3(64), dim3(256), 0, stream, true, p, words,
                          static_cast<const uint4*>(a_src), static_cast<uint4*>(a_dst), (uint32_t)(a_bytes / 16),
                          static_cast<const uint4*>(b_src), static_cast<uint4*>(b_dst), (uint32_t)(b_bytes / 16));
 }
