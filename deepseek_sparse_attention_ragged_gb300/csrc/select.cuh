@@ -39,9 +39,10 @@ struct BinPick {
 // `scratch` is >= 24 words of shared memory; h is 16-byte aligned. Every
 // thread has read h when the call returns, so h may be overwritten then.
 // Without `sync_after`, the next call must use other scratch words.
-__device__ inline BinPick pick_bin(const uint32_t* h, uint32_t need, uint32_t* scratch, bool sync_after = true) {
+// The same, with thread t's bins 4t..4t+3 already in registers.
+__device__ inline BinPick pick_bin_regs(const uint4 hv, uint32_t need, uint32_t* scratch, bool sync_after = true) {
+    static_assert(4 * kThreads == kHistBins, "four bins per thread");
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-    const uint4 hv = reinterpret_cast<const uint4*>(h)[t];
     const uint32_t v0 = hv.x, v1 = hv.y, v2 = hv.z, v3 = hv.w;
     const uint32_t tot = v0 + v1 + v2 + v3;
     uint32_t x = tot;
@@ -79,6 +80,10 @@ __device__ inline BinPick pick_bin(const uint32_t* h, uint32_t need, uint32_t* s
     if (r.bin < 0) r.gt = r.eq = 0;
     if (sync_after) __syncthreads();
     return r;
+}
+
+__device__ inline BinPick pick_bin(const uint32_t* h, uint32_t need, uint32_t* scratch, bool sync_after = true) {
+    return pick_bin_regs(reinterpret_cast<const uint4*>(h)[threadIdx.x], need, scratch, sync_after);
 }
 
 
@@ -507,26 +512,22 @@ __device__ __forceinline__ Gathered select_collect_all(const float* s, uint32_t 
             }
         }
     };
-    // The histogram first (the threshold pick waits for it), then the slice's
-    // scores, which stay in flight while the threshold is picked.
-    uint32_t hv[kHistBins / kThreads];
-#pragma unroll
-    for (int i = 0; i < kHistBins / kThreads; ++i) hv[i] = __ldcg(hist_row + t + i * kThreads);
+    // The histogram first (the threshold pick waits for it; thread t takes bins
+    // 4t..4t+3 straight into registers), then the slice's scores, which stay in
+    // flight while the threshold is picked.
+    const uint4 hv = __ldcg(reinterpret_cast<const uint4*>(hist_row) + t);
     load_batch(begin);
+    // The refinement's first level counts into h (not used by the pick): zero
+    // it, and the final bin's count.
 #pragma unroll
-    for (int i = 0; i < kHistBins / kThreads; ++i) sm.h[t + i * kThreads] = hv[i];
-    __syncthreads();
+    for (int i = 0; i < kHistBins / kThreads; ++i) sm.h[t + i * kThreads] = 0;
+    if (t == 0) sm.nres = 0;
     Gathered r;
-    r.l0 = pick_bin(sm.h, width, sm.pick[0], false);
+    r.l0 = pick_bin_regs(hv, width, sm.pick[0], false);
     r.take_all = r.l0.total <= width;
     const uint32_t n_cand = r.take_all ? r.l0.total : r.l0.gt + r.l0.eq;
     r.b0 = r.take_all ? 0u : (uint32_t)r.l0.bin;
     r.fast = n_cand <= (uint32_t)kCluster * kCandCap;
-    // The refinement's first level counts into h: zero it (every thread has
-    // read its bins of the histogram above), and the final bin's count.
-#pragma unroll
-    for (int i = 0; i < kHistBins / kThreads; ++i) sm.h[t + i * kThreads] = 0;
-    if (t == 0) sm.nres = 0;
 
     uint64_t* own = regions + (size_t)rank * kCandCap;
     uint32_t n_local = 0;
