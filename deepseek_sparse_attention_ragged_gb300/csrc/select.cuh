@@ -406,7 +406,7 @@ __device__ __forceinline__ uint32_t select_finish(const Collected& c, const floa
 
 constexpr uint32_t kCandCap = 2048;  // candidates one CTA may contribute to its cluster
 constexpr int kRegCandSmall = 4;     // candidates per thread in registers while they fit
-constexpr int kRegCandMid = 6;       // then this many,
+constexpr int kRegCandMid = 5;       // then this many,
 constexpr int kRegCandLarge = 9;     // this many,
 constexpr int kRegCand = 12;         // and at most this many per thread, else the general path
 

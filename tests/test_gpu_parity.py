@@ -109,12 +109,12 @@ TOPK_CASES = {
     "nonfinite": dict(lens=[20, 600, 9000, 33000], kw=dict(nonfinite=True)),
     "zeros": dict(lens=[513, 5000, 16385], kw=dict(signed_zeros=True, ties=True)),
     "long": dict(lens=[262144, 131072, 3], kw={}),
-    # The threshold bin holds m candidates: held in registers, 4, 6, 9 or 12
-    # per thread (m <= 2048, 3072, 4608, 6144), then refined from the gathered
+    # The threshold bin holds m candidates: held in registers, 4, 5, 9 or 12
+    # per thread (m <= 2048, 2560, 4608, 6144), then refined from the gathered
     # candidates and sorted by index (m > 6144), and refined from the full row
     # (one CTA's slice has more than 2048).
-    "crowded": dict(lens=[20000, 40000, 50000, 60000, 100000, 120000, 70000],
-                    kw=dict(crowd=(1500, 3000, 3800, 5000, 10000, 60000, 4500))),
+    "crowded": dict(lens=[20000, 40000, 50000, 60000, 100000, 120000, 70000, 30000],
+                    kw=dict(crowd=(1500, 3000, 3800, 5000, 10000, 60000, 4500, 2400))),
 }
 
 
