@@ -156,6 +156,14 @@ class NvmlClockSampler:
                 return
             self.stop.wait(self.period_s)
 
+    def poll(self):
+        """One more sample from the calling thread (a short timed region may
+        end before the sampling thread is scheduled again)."""
+        try:
+            self._sample()
+        except OSError:
+            pass
+
     def __enter__(self):
         self.thread = threading.Thread(target=self._run, daemon=True)
         self.thread.start()
@@ -195,6 +203,9 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
+
+    def poll(self):
+        """nvidia-smi samples on its own period; nothing to add."""
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -654,6 +665,11 @@ def main():
             for k in range(args.steps % 4):
                 graphs[k].replay()
             t_end.record(stream)
+        # While the timed work runs, this thread also samples the clocks, then
+        # the barrier.
+        while not t_end.query():
+            clocks.poll()
+            time.sleep(5e-5)
         barrier()
     total_ms = t_start.elapsed_time(t_end)
     # The spread of the step time: the same graphs again, an event after each

@@ -73,6 +73,21 @@ def test_nvml_sampler_throttle_bits():
     assert out["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
 
 
+def test_nvml_sampler_poll_from_the_caller():
+    """A short timed region samples from the waiting thread too: each poll adds
+    one sample, whatever the sampling thread has done."""
+    fake = FakeNvml([2070, 1980], 0x4)
+    s = bench.NvmlClockSampler(Dev(), period_s=10.0, lib=fake)  # the thread samples once
+    with s:
+        n0 = len(s.samples)
+        for _ in range(4):
+            s.poll()
+        assert len(s.samples) >= n0 + 4
+    out = s.summary()
+    assert out["samples"] >= 4 and out["reasons"] == ["sw_power_cap"]
+    bench.ClockSampler(0).poll()  # nvidia-smi samples on its own; poll is a no-op
+
+
 def test_nvidia_smi_parser_and_empty_summary():
     c = bench.ClockSampler(0)
     c.lines = ["2070, 2070, Not Active, Not Active, Not Active, Active",
