@@ -33,7 +33,7 @@ if ROOT not in sys.path:
 
 # DRAM bytes (read + write) of one indexer launch on the 8 x 131072 workload, from an
 # ncu capture of dram__bytes_read.sum and dram__bytes_write.sum (one pass) of the current kernel.
-INDEXER_DRAM_BYTES_8x131072 = 268_698_880 + 2_954_496
+INDEXER_DRAM_BYTES_8x131072 = 268_619_008 + 2_567_936
 CONFIG_INDEX = 3
 METRIC = "decode rows/s (8 rows, 128K ctx) and achieved HBM GB/s vs GB300 peak"
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal

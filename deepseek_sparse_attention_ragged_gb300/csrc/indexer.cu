@@ -18,9 +18,11 @@
 // issues the MMAs, warps 2..5 run the epilogue. Warp 0 starts loading key
 // tiles as soon as the barriers exist, while the other warps allocate TMEM
 // and stage the head weights. Key tiles flow through a
-// 5-stage ring; the query of the current row is double-buffered; the
-// accumulator is double-buffered in TMEM so the epilogue of tile i overlaps
-// the MMAs of tile i+1. Keys are streamed with an L2 evict-first policy.
+// 4-stage ring (with the HBM saturated by all SMs, a fifth or sixth stage in
+// flight per SM only lengthened the memory queues); the query of the current
+// row is double-buffered; the accumulator is double-buffered in TMEM so the
+// epilogue of tile i overlaps the MMAs of tile i+1. Keys are streamed with an
+// L2 evict-first policy.
 //
 // Optional fused output: a 2048-bin histogram of the order-preserving score
 // keys per row (top 11 bits), used by the top-k stage to find its threshold.
@@ -49,7 +51,7 @@ constexpr int kTileBytes = 2 * kHalfBytes;      // 32 KiB
 constexpr int kQBoxBytes = 64 * 64 * 2;         // one query's 64 heads x 64 columns: 8 KiB
 
 // Shape of the kernel for G queries per key tile.
-//   G = 1: 5-stage key ring, double-buffered query, 4 epilogue warps (one
+//   G = 1: 4-stage key ring, double-buffered query, 4 epilogue warps (one
 //          key per thread), accumulators 2 x 64 TMEM columns, the head
 //          weights of every row and a 2048-bin u32 histogram in shared memory;
 //   G = 4: 4-stage key ring, one query buffer (up to 4 x 16 KiB), 8 epilogue
@@ -60,7 +62,7 @@ constexpr int kQBoxBytes = 64 * 64 * 2;         // one query's 64 heads x 64 col
 //          tiles, so a count stays below 2^16).
 template <int G>
 struct Shape {
-    static constexpr int kStages = G == 1 ? 5 : 4;
+    static constexpr int kStages = 4;
     static constexpr int kQBufs = G == 1 ? 2 : 1;
     static constexpr int kEpiWarps = G == 1 ? 4 : 8;
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
