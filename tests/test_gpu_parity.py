@@ -118,6 +118,37 @@ TOPK_CASES = {
 }
 
 
+def _bin_of_120(L, seed):
+    """Scores whose 512th best falls among 120 distinct values that share the
+    top 22 bits of their order key (1.0f plus 0..119 ulps): the refinement
+    ends with a threshold bin of 120 elements, ranked directly."""
+    rng = np.random.default_rng(seed)
+    s = -1.0 - rng.random(L).astype(np.float32)          # far below
+    top = rng.permutation(L)[:450 + 120]
+    s[top[:450]] = 10.0 + rng.random(450).astype(np.float32)  # certain winners
+    s[top[450:]] = (np.uint32(0x3F800000) + rng.permutation(120).astype(np.uint32)).view(np.float32)
+    return s
+
+
+def test_topk_direct_ranking_of_a_full_bin():
+    lens = [4096, 70000]
+    rows = [workloads.Row(L, 512, 512 * e, e) for e, L in enumerate(lens)]
+    stride = max(lens)
+    host = np.full((len(lens), stride), np.nan, np.float32)
+    for e, L in enumerate(lens):
+        host[e, :L] = _bin_of_120(L, 7 + e)
+    scores = torch.from_numpy(host).cuda()
+    idx = torch.full((512 * len(lens),), -7, dtype=torch.int32, device="cuda")
+    ws = ds.workspace(rows)
+    ds.ds_rows_topk(rows, scores, stride, idx, ws)
+    torch.cuda.synchronize()
+    assert ds.workspace_status(ws) == 0
+    got = idx.cpu().numpy()
+    for e, L in enumerate(lens):
+        want = oracle.topk(host[e, :L], 512)
+        np.testing.assert_array_equal(got[512 * e: 512 * e + 512], want, err_msg=f"row {e}")
+
+
 @pytest.mark.parametrize("case", sorted(TOPK_CASES))
 def test_topk_exact(case):
     spec = TOPK_CASES[case]
