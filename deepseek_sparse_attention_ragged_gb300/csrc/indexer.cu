@@ -32,9 +32,10 @@
 // segment is an entry with up to four consecutive queries, whose query rows
 // stack along N, so each key tile is read from HBM once for all of them:
 // D[128 keys x 64 nq] = K_tile . [q_0; ...; q_{nq-1}]^T. Eight epilogue warps
-// split the queries, two warps per TMEM lane quarter; each
-// query's score of a key is the same arithmetic as with one query, so it does
-// not depend on its neighbours.
+// split the queries, two warps per TMEM lane quarter; a warp reads one query's
+// columns at a time, its first query's head weights held in registers for the
+// segment. Each query's score of a key is the same arithmetic as with one
+// query, so it does not depend on its neighbours.
 
 #include <type_traits>
 
@@ -421,8 +422,10 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
         };
         int cur = -1;
         uint32_t it = 0, since_flush = 0;
-        // One query: the row's head weights stay in registers.
+        // One query: the row's head weights stay in registers. Several: the weights
+        // of this warp's first query of the segment do.
         float wr[G == 1 ? kIdxHeads : 4];
+        float wq0[G == 1 ? 4 : kIdxHeads];
         for (;; ++it) {
             const uint32_t g = tile_of(it);
             if (g >= T) break;
@@ -447,6 +450,15 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
                         w_s[i] = p.w[(size_t)p.q_row[p.seg_vrow[sg] + i / kIdxHeads] * kIdxHeads + i % kIdxHeads];
                 }
                 named_bar(1, kEpiThreads);
+                if (G != 1 && sg != cur) {
+                    const int nq_n = p.seg_queries[sg];
+                    const int q0_n = sub * ((nq_n + kGroups - 1) / kGroups);
+                    if (q0_n < nq_n)
+#pragma unroll
+                        for (int h = 0; h < kIdxHeads; h += 4)
+                            *reinterpret_cast<float4*>(&wq0[h]) =
+                                *reinterpret_cast<const float4*>(w_s + q0_n * kIdxHeads + h);
+                }
                 since_flush = 0;
             }
             cur = sg;
@@ -462,25 +474,46 @@ __device__ __forceinline__ void indexer_score_body(const ParamsOf<G>& p) {
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + a * S::kAccCols;
             const uint32_t j = tile * kTileKeys + quarter * 32 + lane;
-            uint32_t v[S::kQPerWarp][64];
-#pragma unroll
-            for (int k = 0; k < S::kQPerWarp; ++k)
-                if (k < nk) {
+            float scs[S::kQPerWarp];
+            if constexpr (G == 1) {
+                uint32_t v[64];
+                tmem_ld_x16(taddr + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                tmem_ld_x16(taddr + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                tmem_ld_x16(taddr + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
+                tmem_ld_x16(taddr + 48, *reinterpret_cast<uint32_t(*)[16]>(&v[48]));
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar->acc_empty[a]);
+                scs[0] = head_sum(v, wr, nullptr);
+            } else {
+                // One query's 64 columns at a time: the first query's sum uses the
+                // weights in registers, the second's those in shared memory.
+                static_assert(S::kQPerWarp == 2, "two queries per epilogue thread");
+                uint32_t v[64];
+                auto load = [&](int k) {
                     const uint32_t c = taddr + 64 * (q0 + k);
-                    tmem_ld_x16(c + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[k][0]));
-                    tmem_ld_x16(c + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[k][16]));
-                    tmem_ld_x16(c + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[k][32]));
-                    tmem_ld_x16(c + 48, *reinterpret_cast<uint32_t(*)[16]>(&v[k][48]));
+                    tmem_ld_x16(c + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                    tmem_ld_x16(c + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                    tmem_ld_x16(c + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
+                    tmem_ld_x16(c + 48, *reinterpret_cast<uint32_t(*)[16]>(&v[48]));
+                    tmem_ld_wait();
+                };
+                if (nk > 0) {
+                    load(0);
+                    scs[0] = head_sum(v, wq0, nullptr);
                 }
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar->acc_empty[a]);
+                if (nk > 1) load(1);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar->acc_empty[a]);
+                if (nk > 1) scs[1] = head_sum(v, nullptr, w_s + (q0 + 1) * kIdxHeads);
+            }
 #pragma unroll
             for (int k = 0; k < S::kQPerWarp; ++k) {
                 if (k >= nk) break;
                 const int vr = G == 1 ? sg : p.seg_vrow[sg] + q0 + k;
-                const float sc = head_sum(v[k], G == 1 ? wr : nullptr, w_s + (q0 + k) * kIdxHeads);
+                const float sc = scs[k];
                 if (j < p.valid[vr]) {
                     const bool fin = finite_f(sc);
                     st_global_hint(p.scores + (size_t)vr * p.score_stride + j, fin ? sc : -INFINITY, keep);
