@@ -246,13 +246,14 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         if ((uint32_t)t - first < (uint32_t)kChunkSlots && v != 0) idx_s[t - first] = (int32_t)(~(uint32_t)v);
     }
     __syncthreads();  // this chunk's slots are in place (and the candidates consumed)
-    if (p.ranker && rank == 0) {
-        // Publish the winners (index order) for the ranking cluster.
+    // Publish the winners (index order) for the ranking cluster. The flag that
+    // releases them is set after the gather is issued, by a thread that issues
+    // no MMA, so the fence does not delay this CTA's attention.
+    constexpr int kPublisher = kThreads - 32;
+    const bool publish = p.ranker && rank == 0;
+    if (publish) {
         p.pub[(size_t)e * kTopK + t] = sel[t];
         if (t == 0) *pub_n(e) = nsel;
-        __threadfence();
-        __syncthreads();
-        if (t == 0) st_release_gpu(pub_flag(e), 1u);
     }
     // The gather of the chunk's KV rows starts now.
     const size_t part0_off = ((size_t)2 * p.chunk_begin[e] + (size_t)half * nchunks) * kPartFloats;
@@ -301,6 +302,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (publish && t == kPublisher) {
+        // Every thread's winner store precedes the barrier above.
+        __threadfence();
+        st_release_gpu(pub_flag(e), 1u);
+    }
 
     // `alive`: every tensor-core wait of this CTA has succeeded (uniform over the
     // CTA); `pending`: the mma_bar phase of MMAs whose completion was not seen.
