@@ -516,6 +516,7 @@ __device__ __forceinline__ Gathered select_collect_all(const float* s, uint32_t 
     // 4t..4t+3 straight into registers), then the slice's scores, which stay in
     // flight while the threshold is picked.
     const uint4 hv = __ldcg(reinterpret_cast<const uint4*>(hist_row) + t);
+    __syncthreads();  // every warp's histogram load is issued before any score load
     load_batch(begin);
     // The refinement's first level counts into h (not used by the pick): zero
     // it, and the final bin's count.
